@@ -1,0 +1,159 @@
+/*
+ * specv.h -- C ABI of the batched speculative-decoding verify step on one
+ * GB300 (sm_103a).
+ *
+ * For every sequence b of a batch the library scores k draft tokens against
+ * the target model's k+1 output distributions and emits between 1 and k+1
+ * tokens whose distribution is exactly the target's:
+ *
+ *   1. p_i = softmax(target_logits[b,i,:] / T_b) at each position i = 0..k
+ *      ("Speculative decoding." lesson, "First: what an output distribution
+ *      is": softmax of the logits, temperature divides them first);
+ *   2. draft token x_i is kept iff U[b,i,0] < min(1, p_i(x_i) / q_i(x_i)),
+ *      q_i(x_i) clamped below at 1e-12 ("LLM Inference & Speculative
+ *      Decoding: From Roofline Physics to Lossless Acceleration", s.2,
+ *      acceptance rule and its PyTorch verification step);
+ *   3. the walk stops at the first rejected position j ("Speculative
+ *      Decoding: Mathematical Foundations, ...", "The Modified Rejection
+ *      Sampling Algorithm": later drafts are discarded);
+ *   4. at j < k one token is drawn from max(0, p_j - q_j) normalised, by
+ *      inverse CDF with U[b,j,1]; if all k drafts are kept, the bonus token is
+ *      drawn from p_k with U[b,k,1] (same sources, residual distribution and
+ *      bonus token).  If the residual has zero mass, p_j is sampled instead
+ *      ("Speculative Decoding: Draft, Verify, Accept", demo script part B).
+ *   Rows with T_b == 0 use the greedy rule: keep x_i while it equals
+ *   argmax p_i (lowest index on ties), emit the argmax at the first mismatch
+ *   or at position k ("LLM Inference & Speculative Decoding ...", s.4 fix for
+ *   T -> 0; "Speculative Decoding: Mathematical Foundations, ...", "Greedy
+ *   Decoding Equivalence").
+ *
+ * Inverse CDF: the emitted token is the smallest v (vocabulary order) with
+ *   u * W < w(0) + ... + w(v), W the total weight ("Speculative decoding."
+ *   lesson: lay the probabilities end to end and take the slice u lands in).
+ *
+ * Layouts (all row-major, contiguous, device memory unless stated):
+ *   target_logits [B, k+1, V]  bf16 (SPECV_BF16) or fp32 (SPECV_F32)
+ *   draft_probs   [B, k, V]    fp32, the distribution the drafts were drawn
+ *                              from, used as given (never re-tempered)
+ *   draft_tokens  [B, k]       int32
+ *   uniforms      [B, k+1, 2]  fp32 in [0,1); [b,i,0] drives the accept test
+ *                              at i < k, [b,j,1] the residual/bonus draw at
+ *                              the stop position j; [b,k,0] is unused
+ *   temperature   [B]          fp32; 0 = greedy row; otherwise a finite
+ *                              normal positive float
+ *   num_accepted  [B]          int32 out, j in [0, k]; the row emits j+1 tokens
+ *   out_tokens    [B, k+1]     int32 out: x_0..x_{j-1}, then the fixed or
+ *                              bonus token at index j, then -1
+ *   row_status    [B]          int32 out (nullable), bit mask:
+ *                                1  non-finite logits at an examined position
+ *                                   (a NaN or +inf, or all -inf; greedy rows:
+ *                                   a NaN)
+ *                                2  draft token outside [0, V)
+ *                                4  uniform outside [0, 1)
+ *                                8  temperature negative, NaN, infinite or
+ *                                   subnormal
+ *                               16  (information) residual mass was zero, the
+ *                                   token was drawn from p_j
+ *                               32  draft probability NaN, negative or
+ *                                   infinite at an examined entry
+ *                               64  an internal wait timed out (the result of
+ *                                   this row is not valid)
+ *                              The walk checks position 0, 1, ... in order and
+ *                              stops at the first position with an error; a
+ *                              row with any of the bits 1, 2, 4, 8, 32, 64 set
+ *                              reports num_accepted = 0 and out_tokens = -1.
+ *
+ * Ownership and execution: the caller owns every buffer.  Calls are
+ * asynchronous on the given CUDA stream (a cudaStream_t passed as void*;
+ * NULL is the legacy default stream) and allocate nothing; argument errors
+ * are reported synchronously before anything is launched.  A handle may be
+ * used from one host thread at a time.  Pointers need no particular
+ * alignment; sizes are limited by the handle (batch <= max_batch,
+ * 1 <= k <= max_k, V <= vocab).
+ */
+#ifndef SPECV_H
+#define SPECV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct specv_ctx *specv_handle;
+
+typedef enum {
+    SPECV_OK = 0,
+    SPECV_ERR_INVALID_ARGUMENT = 1, /* bad pointer, size or dtype; nothing launched */
+    SPECV_ERR_UNSUPPORTED = 2,      /* device is not sm_103 or lacks a needed feature */
+    SPECV_ERR_CUDA = 3,             /* a CUDA runtime call failed (see specv_last_cuda_error) */
+    SPECV_ERR_TIMEOUT = 4           /* reserved: reported per row as row_status bit 64 */
+} specv_status;
+
+typedef enum { SPECV_F32 = 0, SPECV_BF16 = 1 } specv_dtype;
+
+/* Optional intermediates, all device pointers, each nullable.  For greedy
+ * rows row_sumexp, p_at_draft, q_at_draft and residual_mass are 0. */
+typedef struct {
+    float *p_at_draft;    /* [B, k]   p_i(x_i) (0 if x_i is out of range) */
+    float *q_at_draft;    /* [B, k]   q_i(x_i) as read (0 if out of range) */
+    float *row_max;       /* [B, k+1] max_v logits[b,i,v] */
+    float *row_sumexp;    /* [B, k+1] sum_v exp((logits[b,i,v] - row_max) / T) */
+    float *residual_mass; /* [B]      sum_v max(0, p_j(v) - q_j(v)) at a rejected
+                                      position, else 0 */
+} specv_debug;
+
+/* Create a handle on CUDA device `device` for batches up to max_batch rows,
+ * 1 <= k <= max_k (max_k <= 32) and vocabularies up to `vocab` entries.
+ * Queries the device; allocates no device memory.  Returns
+ * SPECV_ERR_UNSUPPORTED if the device is not compute capability 10.3. */
+specv_status specv_create(specv_handle *out, int device, int max_batch, int max_k, int64_t vocab);
+
+/* Sampled verification (rows with temperature 0 take the greedy rule).
+ * target_logits: dtype logits_dtype; every other pointer as in the layout
+ * table above; dbg may be NULL.  V = vocabulary size of this call. */
+specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const void *target_logits,
+                                 const float *draft_probs, const int32_t *draft_tokens,
+                                 const float *uniforms, const float *temperature, int batch, int k,
+                                 int64_t V, int32_t *num_accepted, int32_t *out_tokens,
+                                 int32_t *row_status, const specv_debug *dbg, void *stream);
+
+/* Greedy verification of every row (no draft probabilities, uniforms or
+ * temperatures): keep x_i while it equals the target argmax. */
+specv_status specv_verify_greedy(specv_handle h, specv_dtype logits_dtype, const void *target_logits,
+                                 const int32_t *draft_tokens, int batch, int k, int64_t V,
+                                 int32_t *num_accepted, int32_t *out_tokens, int32_t *row_status,
+                                 void *stream);
+
+/* Same as specv_verify_sample, but every pointer is HOST memory (pinned
+ * memory gives the fastest copies).  The handle copies the inputs to device
+ * buffers it owns (allocated on the first call, grown when a larger call
+ * comes; this is the one call that may allocate), verifies, copies the three
+ * outputs back and synchronises `stream` before returning. */
+specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, const void *target_logits,
+                                      const float *draft_probs, const int32_t *draft_tokens,
+                                      const float *uniforms, const float *temperature, int batch,
+                                      int k, int64_t V, int32_t *num_accepted, int32_t *out_tokens,
+                                      int32_t *row_status, void *stream);
+
+/* Number of CTAs per sequence (thread-block cluster size, 1..16) that the
+ * next call with these sizes would use; 0 if the sizes are invalid. */
+int specv_plan_cluster(specv_handle h, specv_dtype logits_dtype, int batch, int k, int64_t V);
+
+/* Kernel launches issued by this handle since it was created. */
+int64_t specv_launch_count(specv_handle h);
+
+/* Release the handle and any buffers it owns.  NULL is ignored. */
+void specv_destroy(specv_handle h);
+
+/* Static description of a status code. */
+const char *specv_status_string(specv_status s);
+
+/* Text of the last CUDA error seen by this library on the calling thread. */
+const char *specv_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECV_H */

@@ -1,0 +1,444 @@
+/*
+ * specv_oracle.c -- plain, slow, float64 CPU oracle for the batched
+ * speculative-decoding verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker that the CUDA path is
+ * compared against.  Only the tests, the smoke check and the benchmark's CPU
+ * baseline leg may load it; the product library never links, imports or
+ * calls it, and it shares no code, header, table or helper with the CUDA
+ * sources.  It is written for a reader who wants to check it against the
+ * pages by eye: one row at a time, one position at a time, every sum a plain
+ * left-to-right loop in double precision, in the order the pages give.
+ *
+ * Sources (page title, section):
+ *  [A] "LLM Inference & Speculative Decoding: From Roofline Physics to
+ *      Lossless Acceleration" -- s.2 "Speculative Decoding: Exact Modified
+ *      Rejection Sampling Proof" (acceptance rule, residual distribution,
+ *      bonus token, PyTorch verification step with its q clamp) and s.4
+ *      "Failure Modes" (greedy T = 0 rule, FP32-or-better arithmetic).
+ *  [B] "Speculative Decoding: Mathematical Foundations, Distribution
+ *      Preservation Proofs, ..." -- "The Modified Rejection Sampling
+ *      Algorithm" (stop at the first rejection, discard later drafts, bonus
+ *      token) and "Greedy Decoding Equivalence".
+ *  [C] "Speculative decoding." (learn-cs lesson) -- "First: what an output
+ *      distribution is" (softmax of logits / T, sampling by laying the
+ *      probabilities end to end), "Draft, then verify", "The acceptance rule".
+ *  [D] "Speculative Decoding: Draft, Verify, Accept" -- demo script part B
+ *      (residual with a zero-mass fallback to p, inverse-CDF sampling).
+ *
+ * Readings where the pages leave a step open (each one is listed, with its
+ * reason, in the design notes of the repository):
+ *  - accept iff u < min(1, p(x)/max(q(x), 1e-12))  (strict '<' and the clamp
+ *    follow the code of [A] s.2 and [D]);
+ *  - inverse CDF: the token is the smallest v, in vocabulary order, with
+ *    u * W < sum_{w<=v} weight(w), W = sum of all weights; if no v qualifies
+ *    the last v with positive weight is taken;
+ *  - residual mass W = 0: sample from p_j instead ([D] residual()) and set
+ *    the informational status bit 16;
+ *  - uniforms U[b,i,0] drive the accept test at position i < k, U[j,1] the
+ *    residual or bonus draw at the stop position j;
+ *  - temperature divides the target logits only; q is used as given;
+ *  - T == 0 selects the greedy rule of [A] s.4 / [C] (argmax, lowest index
+ *    on ties); any other T must be a finite normal positive float;
+ *  - data errors end the row's walk at the position where they are met
+ *    (bits: 1 non-finite logits, 2 draft token out of range, 4 uniform not
+ *    in [0,1), 8 bad temperature, 32 q value NaN, negative or infinite);
+ *    an error row reports num_accepted = 0 and out_tokens = -1.
+ */
+#include <float.h>
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ST_NONFINITE 1
+#define ST_TOKEN_RANGE 2
+#define ST_UNIFORM_RANGE 4
+#define ST_TEMPERATURE 8
+#define ST_ZERO_RESIDUAL 16
+#define ST_Q_INVALID 32
+#define ST_ERROR_MASK (ST_NONFINITE | ST_TOKEN_RANGE | ST_UNIFORM_RANGE | ST_TEMPERATURE | ST_Q_INVALID)
+
+/* Exact decoding of one stored logit to double. dtype 0 = float32,
+ * dtype 1 = bfloat16 (the upper 16 bits of a float32). */
+static double logit_at(int dtype, const void *base, int64_t idx) {
+    if (dtype == 1) {
+        uint32_t bits = (uint32_t)((const uint16_t *)base)[idx] << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return (double)((const float *)base)[idx];
+}
+
+/* ---------------------------------------------------------------- step 1
+ * Target distribution at one position: p(v) = exp((l(v) - M) / T) / s with
+ * M = max_v l(v) and s = sum_v exp((l(v) - M) / T)  ([C] "First: what an
+ * output distribution is": softmax of the logits, temperature divides them
+ * first).  Subtracting M leaves p unchanged and keeps exp() finite.
+ * Returns 0 if the row is usable, ST_NONFINITE if a logit is NaN or +inf,
+ * or every logit is -inf (then p does not exist).
+ * e_out (nullable) receives exp((l - M)/T) for every v.                   */
+int specv_oracle_softmax_stats(int dtype, const void *row, int64_t V, double T,
+                               double *M_out, double *s_out, double *e_out) {
+    double M = -INFINITY;
+    for (int64_t v = 0; v < V; ++v) {
+        double l = logit_at(dtype, row, v);
+        if (isnan(l) || l == INFINITY) {
+            *M_out = NAN;
+            *s_out = NAN;
+            return ST_NONFINITE;
+        }
+        if (l > M) M = l;
+    }
+    if (M == -INFINITY) {
+        *M_out = M;
+        *s_out = NAN;
+        return ST_NONFINITE;
+    }
+    double s = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        double e = exp((logit_at(dtype, row, v) - M) / T);
+        if (e_out) e_out[v] = e;
+        s += e;
+    }
+    *M_out = M;
+    *s_out = s;
+    return 0;
+}
+
+/* Greedy target token: argmax_v l(v), the lowest index among equal maxima
+ * ([A] s.4 fix for T = 0; [C] "The acceptance rule", greedy case).
+ * Returns ST_NONFINITE if any logit is NaN (the argmax is then undefined).  */
+int specv_oracle_argmax(int dtype, const void *row, int64_t V, int64_t *arg_out, double *max_out) {
+    int64_t best = 0;
+    double bestv = logit_at(dtype, row, 0);
+    if (isnan(bestv)) return ST_NONFINITE;
+    for (int64_t v = 1; v < V; ++v) {
+        double l = logit_at(dtype, row, v);
+        if (isnan(l)) return ST_NONFINITE;
+        if (l > bestv) {
+            bestv = l;
+            best = v;
+        }
+    }
+    *arg_out = best;
+    *max_out = bestv;
+    return 0;
+}
+
+/* ---------------------------------------------------------------- step 4
+ * Residual weights r(v) = max(0, p(v) - q(v)) and their total
+ * S = sum_v r(v)  ([A] s.2 residual distribution; [B] P'(x); [D] residual()).
+ * The normaliser is applied by the sampler, which compares u * S with the
+ * running sum of r.  Returns ST_Q_INVALID if some q(v) is NaN, negative or
+ * infinite.                                                                */
+int specv_oracle_residual(const double *p, const float *q, int64_t V, double *r_out, double *S_out) {
+    double S = 0.0;
+    int st = 0;
+    for (int64_t v = 0; v < V; ++v) {
+        double qv = (double)q[v];
+        if (!(qv >= 0.0 && qv <= (double)FLT_MAX)) st = ST_Q_INVALID;
+        double r = p[v] - qv;
+        if (r < 0.0) r = 0.0;
+        r_out[v] = r;
+        S += r;
+    }
+    *S_out = S;
+    return st;
+}
+
+/* Inverse-CDF sampling over non-negative weights w[0..V): lay the weights
+ * end to end in vocabulary order and take the slot that u * W lands in
+ * ([C] "First: what an output distribution is", sampling; [D] sample()).
+ * W is the sum of w in the same order.  The token is the smallest v with
+ * u * W < C(v), C(v) = w[0] + ... + w[v]; if none qualifies the last v with
+ * positive weight is returned.  lo/hi (nullable) receive C(v-1)/W and C(v)/W
+ * of the returned token, the edges of its slot on [0,1).                  */
+int64_t specv_oracle_inverse_cdf(const double *w, int64_t V, double u, double *lo, double *hi) {
+    double W = 0.0;
+    for (int64_t v = 0; v < V; ++v) W += w[v];
+    double target = u * W;
+    double C = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        double before = C;
+        C += w[v];
+        if (target < C) {
+            if (lo) *lo = before / W;
+            if (hi) *hi = C / W;
+            return v;
+        }
+    }
+    int64_t last = V - 1;
+    while (last > 0 && !(w[last] > 0.0)) --last;
+    if (lo) *lo = 1.0;
+    if (hi) *hi = 1.0;
+    return last;
+}
+
+/* ---------------------------------------------------------------- the row */
+
+typedef struct {
+    int dtype;
+    const void *logits;        /* [B, k+1, V] */
+    const float *q;            /* [B, k, V] or NULL when every row is greedy */
+    const int32_t *x;          /* [B, k] */
+    const float *u;            /* [B, k+1, 2] or NULL when every row is greedy */
+    const float *T;            /* [B] or NULL: every row greedy */
+    int64_t B;
+    int k;
+    int64_t V;
+    int32_t *num_accepted;     /* [B] */
+    int32_t *out_tokens;       /* [B, k+1] */
+    int32_t *row_status;       /* [B] */
+    double *p_at_draft;        /* [B, k] nullable */
+    double *q_at_draft;        /* [B, k] nullable */
+    double *row_max;           /* [B, k+1] nullable */
+    double *row_sumexp;        /* [B, k+1] nullable */
+    double *residual_mass;     /* [B] nullable */
+    int32_t *boundary;         /* [B] nullable: 0, or 1 + 2*i + slot of U[b,i,slot] */
+    double eps;
+} job_t;
+
+static int temperature_ok(float T) { return T == 0.0f || (T >= FLT_MIN && T <= FLT_MAX); }
+
+static int uniform_ok(float u) { return u >= 0.0f && u < 1.0f; }
+
+static void note_boundary(const job_t *J, int64_t b, int i, int slot, double u, double edge) {
+    if (!J->boundary || J->boundary[b] != 0) return;
+    if (fabs(u - edge) <= J->eps) J->boundary[b] = 1 + 2 * i + slot;
+}
+
+static void finish_error(const job_t *J, int64_t b, int status) {
+    J->row_status[b] = status;
+    J->num_accepted[b] = 0;
+    for (int i = 0; i <= J->k; ++i) J->out_tokens[b * (J->k + 1) + i] = -1;
+}
+
+static void finish_ok(const job_t *J, int64_t b, int j, int64_t token, int status) {
+    const int k = J->k;
+    J->row_status[b] = status;
+    J->num_accepted[b] = j;
+    for (int i = 0; i < j; ++i) J->out_tokens[b * (k + 1) + i] = J->x[b * k + i];
+    J->out_tokens[b * (k + 1) + j] = (int32_t)token;
+    for (int i = j + 1; i <= k; ++i) J->out_tokens[b * (k + 1) + i] = -1;
+}
+
+static const void *row_ptr(const job_t *J, int64_t b, int i) {
+    int64_t off = (b * (J->k + 1) + i) * J->V;
+    return J->dtype == 1 ? (const void *)((const uint16_t *)J->logits + off)
+                         : (const void *)((const float *)J->logits + off);
+}
+
+/* Debug intermediates for every position, independent of the walk:
+ * row_max = M_i, row_sumexp = s_i (0 for greedy rows), p_at_draft =
+ * p_i(x_i), q_at_draft = q_i(x_i) (0 for greedy rows or out-of-range x).  */
+static void fill_debug(const job_t *J, int64_t b, int greedy, double T) {
+    const int k = J->k;
+    for (int i = 0; i <= k; ++i) {
+        const void *row = row_ptr(J, b, i);
+        double M = NAN, s = 0.0;
+        if (greedy) {
+            int64_t a;
+            if (specv_oracle_argmax(J->dtype, row, J->V, &a, &M) != 0) M = NAN;
+        } else {
+            specv_oracle_softmax_stats(J->dtype, row, J->V, T, &M, &s, NULL);
+        }
+        if (J->row_max) J->row_max[b * (k + 1) + i] = M;
+        if (J->row_sumexp) J->row_sumexp[b * (k + 1) + i] = greedy ? 0.0 : s;
+        if (i == k) continue;
+        int32_t x = J->x[b * k + i];
+        double p = 0.0, q = 0.0;
+        if (!greedy && x >= 0 && x < J->V) {
+            p = exp((logit_at(J->dtype, row, x) - M) / T) / s;
+            q = (double)J->q[(b * k + i) * J->V + x];
+        }
+        if (J->p_at_draft) J->p_at_draft[b * k + i] = p;
+        if (J->q_at_draft) J->q_at_draft[b * k + i] = q;
+    }
+}
+
+/* Greedy verification ([A] s.4; [B] "Greedy Decoding Equivalence"; [C]
+ * "The acceptance rule", greedy case): keep x_i while it equals the target
+ * argmax a_i; at the first mismatch emit a_i; if all k match, emit a_k.   */
+static void verify_greedy_row(const job_t *J, int64_t b) {
+    const int k = J->k;
+    for (int i = 0; i <= k; ++i) {
+        int st = 0;
+        int32_t x = -1;
+        if (i < k) {
+            x = J->x[b * k + i];
+            if (x < 0 || x >= J->V) st |= ST_TOKEN_RANGE;
+        }
+        int64_t a;
+        double M;
+        st |= specv_oracle_argmax(J->dtype, row_ptr(J, b, i), J->V, &a, &M);
+        if (st) {
+            finish_error(J, b, st);
+            return;
+        }
+        if (i == k || x != a) {
+            finish_ok(J, b, i, a, 0);
+            return;
+        }
+    }
+}
+
+/* Sampled verification, the modified rejection sampling of [A] s.2 and
+ * [B], in the order of [C] "Draft, then verify": accept left to right,
+ * stop at the first rejection, then fix (residual) or bonus.              */
+static void verify_sampled_row(const job_t *J, int64_t b, double T, double *buf_p, double *buf_w) {
+    const int k = J->k;
+    const int64_t V = J->V;
+    int j = k; /* stop position: first rejection, or k when all are kept */
+    for (int i = 0; i < k; ++i) {
+        int st = 0;
+        int32_t x = J->x[b * k + i];
+        float u = J->u[(b * (k + 1) + i) * 2 + 0];
+        if (x < 0 || x >= V) st |= ST_TOKEN_RANGE;
+        if (!uniform_ok(u)) st |= ST_UNIFORM_RANGE;
+        double M, s;
+        st |= specv_oracle_softmax_stats(J->dtype, row_ptr(J, b, i), V, T, &M, &s, NULL);
+        double q = 0.0;
+        if (x >= 0 && x < V) {
+            q = (double)J->q[(b * k + i) * V + x];
+            if (!(q >= 0.0 && q <= (double)FLT_MAX)) st |= ST_Q_INVALID;
+        }
+        if (st) {
+            finish_error(J, b, st);
+            return;
+        }
+        /* p_i(x) and the acceptance probability min(1, p/q), q clamped
+         * below at 1e-12 as in the verification step of [A] s.2. */
+        double p = exp((logit_at(J->dtype, row_ptr(J, b, i), x) - M) / T) / s;
+        double rho = p / (q > 1e-12 ? q : 1e-12);
+        if (rho > 1.0) rho = 1.0;
+        note_boundary(J, b, i, 0, (double)u, rho);
+        if (!((double)u < rho)) {
+            j = i;
+            break;
+        }
+    }
+
+    float u1 = J->u[(b * (k + 1) + j) * 2 + 1];
+    double M, s;
+    int st = specv_oracle_softmax_stats(J->dtype, row_ptr(J, b, j), V, T, &M, &s, buf_w);
+    if (!uniform_ok(u1)) st |= ST_UNIFORM_RANGE;
+    if (st) {
+        finish_error(J, b, st);
+        return;
+    }
+    int status = 0;
+    int64_t token;
+    double lo, hi;
+    if (j == k) {
+        /* Bonus token: sample from p_{k+1} = e / s.  The unnormalised
+         * weights e give the same slots as p. */
+        token = specv_oracle_inverse_cdf(buf_w, V, (double)u1, &lo, &hi);
+        if (J->residual_mass) J->residual_mass[b] = 0.0;
+    } else {
+        for (int64_t v = 0; v < V; ++v) buf_p[v] = buf_w[v] / s;
+        double S;
+        int qst = specv_oracle_residual(buf_p, J->q + (b * k + j) * V, V, buf_w, &S);
+        if (qst) {
+            finish_error(J, b, qst);
+            return;
+        }
+        if (J->residual_mass) J->residual_mass[b] = S;
+        if (S > 0.0) {
+            token = specv_oracle_inverse_cdf(buf_w, V, (double)u1, &lo, &hi);
+        } else {
+            /* zero residual mass: fall back to p ([D] residual()) */
+            status |= ST_ZERO_RESIDUAL;
+            token = specv_oracle_inverse_cdf(buf_p, V, (double)u1, &lo, &hi);
+        }
+    }
+    note_boundary(J, b, j, 1, (double)u1, lo);
+    note_boundary(J, b, j, 1, (double)u1, hi);
+    finish_ok(J, b, j, token, status);
+}
+
+typedef struct {
+    const job_t *J;
+    int64_t b0, b1;
+    int err;
+} range_t;
+
+static void *run_range(void *arg) {
+    range_t *R = (range_t *)arg;
+    const job_t *J = R->J;
+    double *buf_p = (double *)malloc(sizeof(double) * (size_t)J->V);
+    double *buf_w = (double *)malloc(sizeof(double) * (size_t)J->V);
+    if (!buf_p || !buf_w) {
+        free(buf_p);
+        free(buf_w);
+        R->err = 1;
+        return NULL;
+    }
+    for (int64_t b = R->b0; b < R->b1; ++b) {
+        if (J->boundary) J->boundary[b] = 0;
+        if (J->residual_mass) J->residual_mass[b] = 0.0;
+        float Tf = J->T ? J->T[b] : 0.0f;
+        int greedy = (Tf == 0.0f);
+        if (J->p_at_draft || J->q_at_draft || J->row_max || J->row_sumexp)
+            fill_debug(J, b, greedy || !temperature_ok(Tf), (double)Tf);
+        if (!temperature_ok(Tf)) {
+            finish_error(J, b, ST_TEMPERATURE);
+            continue;
+        }
+        if (greedy)
+            verify_greedy_row(J, b);
+        else
+            verify_sampled_row(J, b, (double)Tf, buf_p, buf_w);
+    }
+    free(buf_p);
+    free(buf_w);
+    return NULL;
+}
+
+/* The whole batch.  Rows are independent; nthreads > 1 splits them into
+ * contiguous ranges, one per POSIX thread (nthreads <= 0: one per online
+ * core).  Returns 0, or -1 on a bad argument, -2 if memory ran out.       */
+int specv_oracle_verify(int dtype, const void *logits, const float *q, const int32_t *x,
+                        const float *u, const float *T, int64_t B, int k, int64_t V,
+                        int32_t *num_accepted, int32_t *out_tokens, int32_t *row_status,
+                        double *p_at_draft, double *q_at_draft, double *row_max,
+                        double *row_sumexp, double *residual_mass, int32_t *boundary,
+                        double boundary_eps, int nthreads) {
+    if (B < 0 || k < 1 || V < 1 || (dtype != 0 && dtype != 1)) return -1;
+    if (!logits || !x || !num_accepted || !out_tokens || !row_status) return -1;
+    if (T && (!q || !u)) return -1;
+    job_t J = {dtype, logits, q, x, u, T, B, k, V, num_accepted, out_tokens, row_status,
+               p_at_draft, q_at_draft, row_max, row_sumexp, residual_mass, boundary, boundary_eps};
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if ((int64_t)nthreads > B) nthreads = B > 0 ? (int)B : 1;
+    range_t *R = (range_t *)calloc((size_t)nthreads, sizeof(range_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!R || !th) {
+        free(R);
+        free(th);
+        return -2;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        R[t].J = &J;
+        R[t].b0 = B * t / nthreads;
+        R[t].b1 = B * (t + 1) / nthreads;
+    }
+    int err = 0;
+    if (nthreads == 1) {
+        run_range(&R[0]);
+        err = R[0].err;
+    } else {
+        for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, run_range, &R[t]);
+        for (int t = 0; t < nthreads; ++t) {
+            pthread_join(th[t], NULL);
+            err |= R[t].err;
+        }
+    }
+    free(R);
+    free(th);
+    return err ? -2 : 0;
+}
