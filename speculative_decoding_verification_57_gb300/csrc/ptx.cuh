@@ -29,6 +29,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Plain arrival (one count) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Arrival counting `count` at once.
+__device__ __forceinline__ void mbar_arrive_cnt(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
     uint32_t ok;
     asm volatile(
@@ -105,12 +115,41 @@ __device__ __forceinline__ double ld_cluster_f64(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t r;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(r));
+    return r;
+}
+
+// Stores into the shared memory of another CTA of the cluster (visible to
+// it after the next cluster barrier); they do not wait for a reply.
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
 // ------------------------------------------------------------------ loads
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ unsigned short ld_shared_u16(uint32_t addr) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
     return v;
 }
 
@@ -202,6 +241,79 @@ __device__ __forceinline__ void df_add(float& hi, float& lo, float a_hi, float a
     two_sum(hi, a_hi, s, e);
     hi = s;
     lo = __fadd_rn(lo, __fadd_rn(e, a_lo));
+}
+
+// Unevaluated pairs of floats ("double-float"): value = hi + lo, |lo| small.
+// All sums and comparisons of the stop-row weights use them: the GB300's
+// float64 units are far too slow for the critical path.
+struct df {
+    float hi, lo;
+};
+
+__device__ __forceinline__ df df_make(float h, float l = 0.0f) { return df{h, l}; }
+
+__device__ __forceinline__ df df_sum(df a, df b) {
+    df r = a;
+    df_add(r.hi, r.lo, b.hi, b.lo);
+    return r;
+}
+
+__device__ __forceinline__ df df_neg(df a) { return df{-a.hi, -a.lo}; }
+
+// a * b for a float b: exact product of the high parts plus the low part.
+__device__ __forceinline__ df df_mul_f(df a, float b) {
+    const float p = a.hi * b;
+    const float e = fmaf(a.hi, b, -p);
+    return df{p, fmaf(a.lo, b, e)};
+}
+
+// sign of a - b as -1, 0, +1 (to the pairs' precision)
+__device__ __forceinline__ bool df_less(df a, df b) {
+    float s, e;
+    two_sum(a.hi, -b.hi, s, e);
+    return s + (e + (a.lo - b.lo)) < 0.0f;
+}
+
+__device__ __forceinline__ float df_val(df a) { return a.hi + a.lo; }
+
+__device__ __forceinline__ df df_shfl_up(df a, int off) {
+    return df{__shfl_up_sync(0xffffffffu, a.hi, off), __shfl_up_sync(0xffffffffu, a.lo, off)};
+}
+
+__device__ __forceinline__ df df_shfl_down(df a, int off) {
+    return df{__shfl_down_sync(0xffffffffu, a.hi, off), __shfl_down_sync(0xffffffffu, a.lo, off)};
+}
+
+__device__ __forceinline__ df df_shfl(df a, int src) {
+    return df{__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+
+// Warp-wide inclusive prefix sum of pairs, lane order.
+__device__ __forceinline__ df df_warp_incl_scan(df v, int lane) {
+    for (int off = 1; off < 32; off <<= 1) {
+        const df o = df_shfl_up(v, off);
+        if (lane >= off) v = df_sum(o, v);
+    }
+    return v;
+}
+
+// Warp-wide total of pairs (valid in lane 0), fixed tree order.
+__device__ __forceinline__ df df_warp_total(df v) {
+    for (int off = 16; off > 0; off >>= 1) v = df_sum(v, df_shfl_down(v, off));
+    return v;
+}
+
+// log2(e) / T as a pair: the quotient of the high part of log2(e), its
+// exact remainder (one fma), and the low part of log2(e).
+__device__ __forceinline__ df log2e_over(float T) {
+    const float l2e_hi = 1.44269502162933349609375f;  // float(log2 e)
+    const float l2e_lo = 1.9259629911266175e-8f;     // log2 e - l2e_hi
+    const float qh = l2e_hi / T;
+    const float rem = fmaf(-qh, T, l2e_hi);
+    const float ql = (rem + l2e_lo) / T;
+    float h, l;
+    two_sum(qh, ql, h, l);
+    return df{h, l};
 }
 
 }  // namespace specv

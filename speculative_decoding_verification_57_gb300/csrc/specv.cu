@@ -25,6 +25,9 @@ struct specv_ctx {
     int max_k = 0;
     int64_t vocab = 0;
     std::atomic<int64_t> launches{0};
+    // most clusters of each size (1..16) that can be resident at once, per
+    // logits type (index 0: fp32, 1: bf16); 0 if that size cannot launch
+    int max_clusters[2][17] = {};
     // device staging for specv_verify_sample_host
     void* stage = nullptr;
     size_t stage_bytes = 0;
@@ -65,16 +68,23 @@ struct Plan {
     int slice = 0;
 };
 
-Plan make_plan(const specv_ctx* h, int batch, int64_t V) {
+Plan make_plan(const specv_ctx* h, specv_dtype dt, int batch, int64_t V) {
     Plan p;
     if (V <= kWarpKernelMaxV) {
         p.warp = true;
         return p;
     }
-    int cmin = static_cast<int>((V + kMaxSlice - 1) / kMaxSlice);
+    const int cmin = static_cast<int>((V + kMaxSlice - 1) / kMaxSlice);
+    // the widest split whose clusters are all resident at once; if the batch
+    // does not fit in one wave at any size, the narrowest split
     int C = cmin;
-    // enough CTAs to cover the SMs several times over
-    while (C < 16 && static_cast<int64_t>(batch) * C < 4LL * h->sm_count) ++C;
+    const int* mc = h->max_clusters[dt == SPECV_BF16 ? 1 : 0];
+    for (int c = 16; c >= cmin; --c) {
+        if (mc[c] >= batch) {
+            C = c;
+            break;
+        }
+    }
     if (const char* env = getenv("SPECV_CLUSTER")) {
         const int forced = atoi(env);
         if (forced >= cmin && forced <= 16) C = forced;
@@ -112,6 +122,29 @@ cudaError_t launch_warp(const VerifyArgs& a, cudaStream_t stream) {
 }
 
 template <bool BF16>
+void query_clusters(int* out) {
+    for (int c = 1; c <= 16; ++c) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(c) * 256, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kClusterDynSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = c;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, verify_cluster_kernel<BF16>, &cfg) != cudaSuccess) {
+            n = 0;
+            cudaGetLastError();
+        }
+        out[c] = n;
+    }
+}
+
+template <bool BF16>
 cudaError_t set_attributes() {
     cudaError_t e = cudaFuncSetAttribute(verify_cluster_kernel<BF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -132,7 +165,7 @@ specv_status run(specv_ctx* h, specv_dtype dt, const VerifyArgs& a, void* stream
     if (a.B == 0) return SPECV_OK;
     DeviceGuard g(h->device);
     if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
-    const Plan p = make_plan(h, a.B, a.V);
+    const Plan p = make_plan(h, dt, a.B, a.V);
     VerifyArgs args = a;
     args.slice = p.slice;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -186,6 +219,8 @@ specv_status specv_create(specv_handle* out, int device, int max_batch, int max_
     h->max_batch = max_batch;
     h->max_k = max_k;
     h->vocab = vocab;
+    query_clusters<false>(h->max_clusters[0]);
+    query_clusters<true>(h->max_clusters[1]);
     *out = h;
     return SPECV_OK;
 }
@@ -295,7 +330,7 @@ specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, 
 
 int specv_plan_cluster(specv_handle h, specv_dtype logits_dtype, int batch, int k, int64_t V) {
     if (check_sizes(h, logits_dtype, batch, k, V) != SPECV_OK) return 0;
-    const Plan p = make_plan(h, batch, V);
+    const Plan p = make_plan(h, logits_dtype, batch, V);
     return p.warp ? 1 : p.cluster;
 }
 

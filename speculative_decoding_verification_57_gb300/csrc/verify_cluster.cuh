@@ -2,16 +2,21 @@
 // cluster of C CTAs per sequence, each CTA owning a contiguous V-slice of
 // all k+1 positions.
 //
-// Pass 1 streams the CTA's slice of every position once through a ring of
-// shared-memory tiles filled by 1-D bulk (TMA) copies and keeps, per
+// Each CTA has four consumer warps and one producer warp.  The producer
+// streams tiles into a ring of shared-memory stages with 1-D bulk (TMA)
+// copies; "full" and "empty" mbarriers hand the stages back and forth, so no
+// block-wide barrier sits in the streaming loops.
+//
+// Pass 1 streams the CTA's slice of every position once and keeps, per
 // position, an online maximum and sum of exp((l - max) / T) (sampled rows) or
 // the maximum and its lowest index (greedy rows).  The per-CTA partials meet
 // over distributed shared memory after a cluster barrier; every CTA then
 // evaluates the accept tests and the first rejection with one warp ballot,
-// identically.  Pass 2 revisits only the stop position j: it builds residual
-// weights max(0, p_j - q_j) (or the bonus weights p_k) chunk by chunk, the
-// CTA totals meet again over distributed shared memory, and the CTA whose
-// slice holds u * W finds the token with a block-wide prefix scan.
+// identically.  Pass 2 streams only the stop position j (target logits and,
+// after a rejection, the draft row q_j): it weighs every entry by
+// max(0, p_j - q_j) (or p_k for the bonus), keeps sums per 256-entry block,
+// and after a second exchange of CTA totals the CTA whose slice holds u * W
+// rescans one block with one warp to find the token.
 //
 // Sources (page title, section): "LLM Inference & Speculative Decoding: From
 // Roofline Physics to Lossless Acceleration", s.2 (acceptance rule, residual,
@@ -23,6 +28,7 @@
 // residual falls back to p).
 #pragma once
 #include <cfloat>
+#include <cstddef>
 #include <cstdint>
 
 #include "exp2dd.cuh"
@@ -30,14 +36,17 @@
 
 namespace specv {
 
-constexpr int kThreads = 128;
-constexpr int kWarps = kThreads / 32;
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kTileBytes = 8192;
 constexpr int kStages = 4;
 constexpr int kMaxK = 31;          // positions 0..k fit one warp
 constexpr int kMaxSlice = 16384;   // elements of one position held by one CTA
-constexpr int kChunk = 8;          // pass-2 elements per chunk
-constexpr int kMaxChunks = kMaxSlice / kChunk;
+constexpr int kChunk = 8;          // pass-2 entries per chunk
+constexpr int kLaneEntries = 32;   // pass-2 entries per lane and tile (four chunks)
+constexpr int kP2Elems = kLaneEntries * 32;  // pass-2 tile: 1024 entries, one warp
+constexpr int kMaxP2Tiles = kMaxSlice / kP2Elems;
 constexpr float kLargeP = 1e-5f;   // pass-2 entries with p above this use exp2dd
 constexpr uint32_t kWaitPolls = 1u << 22;
 constexpr float kLog2e = 1.44269504088896341f;
@@ -82,23 +91,33 @@ struct Partial {
     int flags;  // bit 0: a NaN was seen (greedy); bit 1: a wait timed out
 };
 
-struct ClusterSmem {
-    Partial wpart[kWarps][kMaxK + 1];
-    Partial part[kMaxK + 1];
-    int tstart[kMaxK + 2];      // first tile of each position
+struct alignas(16) ClusterSmem {
+    Partial wpart[kConsumerWarps][kMaxK + 1];
+    alignas(16) Partial allpart[16][kMaxK + 1];  // every CTA's partials, pushed by each CTA of the cluster
+    int tstart[kMaxK + 2];      // first pass-1 tile of each position
     int head[kMaxK + 1];        // unaligned leading elements of each position's slice
     int nbytes[kMaxK + 1];      // bytes of the 16-byte aligned interior
-    unsigned long long mbar[kStages];
-    double tot[4];              // pass-2 CTA totals: weights, sum of e, q over positive residuals, bad-q flag
-    double thr_w[kThreads];     // per-thread pass-2 sums (contiguous chunk blocks)
-    double thr_q[kThreads];
+    unsigned long long full[kStages];
+    unsigned long long empty[kStages];
+    float tile_hi[kMaxP2Tiles];  // pass-2 weights per tile of 1024 entries (pair), and q sums
+    float tile_lo[kMaxP2Tiles];
+    float tile_q[kMaxP2Tiles];
+    float lane_hi[kMaxP2Tiles][32];  // the same per 32-entry lane segment
+    float lane_lo[kMaxP2Tiles][32];
+    float lane_q[kMaxP2Tiles][32];
+    alignas(16) float alltot[16][8];  // every CTA's pass-2 totals: weights (pair), sum of e (pair), q over positive residuals, flags
+    float wred_hi[kConsumerWarps];
+    float wred_lo[kConsumerWarps];
     float2 exp2tab[128];
-    // row decisions, broadcast to the block
-    int j, status, mode, owner, last_pos;
-    float Mj, sj, thr;
-    float c_hi, c_lo;
-    double s_prec, delta, t_local;
+    int xs[kMaxK + 1];          // draft tokens, for whoever writes the outputs
+    int j, status, mode, owner, p2fast, ntiles2, timeout;
+    float Mj, sj, thr, c_hi, c_lo, uj;
+    float delta, sp_hi, sp_lo, t_hi, t_lo;
 };
+static_assert(sizeof(Partial) == 16, "Partial is pushed with one 16-byte store");
+static_assert(offsetof(ClusterSmem, allpart) % 16 == 0, "16-byte remote stores need 16-byte aligned targets");
+static_assert(offsetof(ClusterSmem, alltot) % 16 == 0, "16-byte remote stores need 16-byte aligned targets");
+static_assert(alignof(ClusterSmem) >= 16, "ClusterSmem must be 16-byte aligned");
 
 __device__ __forceinline__ float load_logit(const void* base, long long idx, bool bf16) {
     if (bf16) {
@@ -117,7 +136,7 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
         a = 0.0f;
         b2 = 0.0f;
     }
-    // NaN sums stay NaN through the products above
+    // NaN sums stay NaN
     if (s != s) a = s;
     if (s2 != s2) b2 = s2;
     m = M;
@@ -132,24 +151,253 @@ __device__ __forceinline__ void merge_arg(float& v, int& a, float v2, int a2) {
     }
 }
 
-// One element of the online softmax (used for the unaligned head/tail).
+// One element of the online softmax (the unaligned head/tail of a slice).
 __device__ __forceinline__ void online_add(float& m, float& s, float l, float c) {
     if (l > m) {
-        s = (m == -INFINITY) ? 0.0f : s * ex2((m - l) * c);
+        // s is 0 while m is -inf, unless a NaN was seen: s * 0 keeps it
+        s = (m == -INFINITY) ? s * 0.0f : s * ex2((m - l) * c);
         m = l;
     }
     if (m != -INFINITY || l != l) s += ex2((l - m) * c);
 }
 
+// Per-row constants of the stop-row weights.
+struct RowConst {
+    float M;       // row max
+    float s1;      // pass-1 sum of exp((l - M) / T)
+    float thr;     // entries with e above this take the double-float exponential
+    float ch, cl;  // log2(e) / T as a float pair
+};
+
+// SFU estimate of e = 2^((l - M) log2(e) / T), the exponent carried as a
+// float pair (xh, xl) and folded back in to first order.
+__device__ __forceinline__ float fast_e(float l, const RowConst& rc) {
+    const float dh = l - rc.M;
+    const float xh = dh * rc.ch;
+    const float xl = fmaf(dh, rc.cl, fmaf(dh, rc.ch, -xh));
+    const float ef = ex2(xh);
+    return fmaf(ef, xl * kLn2, ef);
+}
+
+// e with exp2dd, as a pair (the exact difference l - M for fp32 logits).
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyArgs a) {
+__device__ __forceinline__ df precise_e(float l, const RowConst& rc, const float2* tab) {
+    float dh = l - rc.M, dl = 0.0f;
+    if (!BF16) two_sum(l, -rc.M, dh, dl);
+    const float xh = dh * rc.ch;
+    const float xl = fmaf(dl, rc.ch, fmaf(dh, rc.cl, fmaf(dh, rc.ch, -xh)));
+    const float2 e = exp2dd(xh, xl, tab);
+    return df{e.x, e.y};
+}
+
+// e - s q as a pair (s q formed exactly with one fma).
+__device__ __forceinline__ df minus_sq(df e, df s, float q) {
+    const df p = df_mul_f(s, q);
+    float rh, rl;
+    two_sum(e.hi, -p.hi, rh, rl);
+    return df{rh, rl + (e.lo - p.lo)};
+}
+
+// The final weight of one entry, exactly (pair): e, or max(0, e - s q) with
+// the recomputed s in residual mode.
+template <bool BF16>
+__device__ __forceinline__ df exact_weight(float l, float qv, int md, const RowConst& rc, df s_prec,
+                                           const float2* tab) {
+    if (l == -INFINITY) return df_make(0.0f);
+    const df e = precise_e<BF16>(l, rc, tab);
+    if (md != MODE_RESIDUAL) return e;
+    const df r = minus_sq(e, s_prec, qv);
+    return (r.hi + r.lo > 0.0f) ? r : df_make(0.0f);
+}
+
+// Weight of one large entry with exp2dd: (w, q over a positive residual, e).
+template <bool BF16>
+__device__ __forceinline__ void large_weight(float l, float q, int md, const RowConst& rc, const float2* tab, df& w,
+                                             float& wq, df& e) {
+    e = precise_e<BF16>(l, rc, tab);
+    if (md == MODE_RESIDUAL) {
+        const df r = minus_sq(e, df_make(rc.s1), q);
+        const bool pos = r.hi + r.lo > 0.0f;
+        w = pos ? r : df_make(0.0f);
+        wq = pos ? q : 0.0f;
+    } else {
+        w = e;
+        wq = 0.0f;
+    }
+}
+
+// A lane's 32 consecutive stop-row entries, summed per 8-entry chunk so that
+// the sums can be walked in vocabulary order.  Weights are in e-units (the
+// row's sum of exponentials times p): residual mode r = max(0, e - s1 q),
+// bonus / fallback mode e.  Entries whose SFU estimate exceeds rc.thr are
+// "large": their weight is recomputed with exp2dd.
+struct Lane32 {
+    float s[4];      // weights of the small entries, per chunk (entry order)
+    float sq[4];     // q over positive residuals among them
+    df big[4];       // weights of the large entries, per chunk (entry order)
+    float bq[4];     // q over positive residuals among them
+    df e;            // sum of e over the lane's entries (residual mode)
+    uint32_t large;  // bit 8c+i: entry i of chunk c is large
+};
+
+__device__ __forceinline__ void lane32_init(Lane32& L) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        L.s[c] = 0.0f;
+        L.sq[c] = 0.0f;
+        L.big[c] = df_make(0.0f);
+        L.bq[c] = 0.0f;
+    }
+    L.e = df_make(0.0f);
+    L.large = 0;
+}
+
+// Small entries of chunk c (c is a run-time value: the chunks are visited in
+// a lane-rotated order to spread shared-memory banks; the sums are stored by
+// chunk).  nvalid: entries of the chunk inside the slice.  Branch-free.
+__device__ __forceinline__ void lane32_fast8(Lane32& L, int c, const float* lv, const float* qv, int nvalid, int md,
+                                             const RowConst& rc) {
+    float s = 0.0f, sq = 0.0f, es = 0.0f;
+    uint32_t bits = 0;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+        const float l = lv[i];
+        const bool live = (i < nvalid) && (l != -INFINITY);  // masked entries weigh nothing
+        float ef = fast_e(l, rc);
+        ef = live ? ef : 0.0f;
+        const bool big = ef > rc.thr;
+        bits |= (big ? 1u : 0u) << i;
+        if (md == MODE_RESIDUAL) {
+            const float r = fmaf(-rc.s1, qv[i], ef);
+            const bool take = !big && r > 0.0f;
+            s += take ? r : 0.0f;
+            sq += take ? qv[i] : 0.0f;
+            es += big ? 0.0f : ef;
+        } else {
+            s += big ? 0.0f : ef;
+        }
+    }
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {
+        if (k2 == c) {
+            L.s[k2] = s;
+            L.sq[k2] = sq;
+        }
+    }
+    L.large |= bits << (8 * c);
+    if (md == MODE_RESIDUAL) L.e = df_sum(L.e, df_make(es));
+}
+
+// Add one large entry's result to chunk c of the lane (entry order).
+__device__ __forceinline__ void lane32_add_large(Lane32& L, int c, df w, float wq, df e, int md) {
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {
+        if (k2 == c) {
+            L.big[k2] = df_sum(L.big[k2], w);
+            L.bq[k2] += wq;
+        }
+    }
+    if (md == MODE_RESIDUAL) L.e = df_sum(L.e, e);
+}
+
+// Chunk c's weight (pair) and q sum.
+__device__ __forceinline__ df lane32_chunk(const Lane32& L, int c, float& q) {
+    df w = df_make(0.0f);
+    q = 0.0f;
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2) {
+        if (k2 == c) {
+            w = df_sum(df_make(L.s[k2]), L.big[k2]);
+            q = L.sq[k2] + L.bq[k2];
+        }
+    }
+    return w;
+}
+
+// The lane's total weight and q sum, chunks in vocabulary order.
+__device__ __forceinline__ df lane32_total(const Lane32& L, float& q) {
+    df w = df_make(0.0f);
+    q = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        w = df_sum(w, df_sum(df_make(L.s[c]), L.big[c]));
+        q += L.sq[c] + L.bq[c];
+    }
+    return w;
+}
+
+// Up to 8 consecutive entries of a logits row / a q row from global memory
+// (vector loads when aligned and complete).
+template <bool BF16>
+__device__ __forceinline__ void load8_logits(const void* logits, long long idx, int cnt, float* lv) {
+    const unsigned char* lp = reinterpret_cast<const unsigned char*>(logits) + idx * (BF16 ? 2 : 4);
+    if (cnt == kChunk && (reinterpret_cast<uintptr_t>(lp) & 15) == 0) {
+        if (BF16) {
+            const uint4 w = ld_stream_v4(lp);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                lv[2 * q4] = bf16_lo(ws[q4]);
+                lv[2 * q4 + 1] = bf16_hi(ws[q4]);
+            }
+        } else {
+            const uint4 w0 = ld_stream_v4(lp), w1 = ld_stream_v4(lp + 16);
+            lv[0] = __uint_as_float(w0.x); lv[1] = __uint_as_float(w0.y);
+            lv[2] = __uint_as_float(w0.z); lv[3] = __uint_as_float(w0.w);
+            lv[4] = __uint_as_float(w1.x); lv[5] = __uint_as_float(w1.y);
+            lv[6] = __uint_as_float(w1.z); lv[7] = __uint_as_float(w1.w);
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kChunk; ++e) lv[e] = e < cnt ? load_logit(logits, idx + e, BF16) : -INFINITY;
+    }
+}
+
+__device__ __forceinline__ void load8_q(const float* qp, int cnt, float* qv) {
+    if (cnt == kChunk && (reinterpret_cast<uintptr_t>(qp) & 15) == 0) {
+        const uint4 w0 = ld_stream_v4(qp), w1 = ld_stream_v4(qp + 4);
+        qv[0] = __uint_as_float(w0.x); qv[1] = __uint_as_float(w0.y);
+        qv[2] = __uint_as_float(w0.z); qv[3] = __uint_as_float(w0.w);
+        qv[4] = __uint_as_float(w1.x); qv[5] = __uint_as_float(w1.y);
+        qv[6] = __uint_as_float(w1.z); qv[7] = __uint_as_float(w1.w);
+    } else {
+#pragma unroll
+        for (int e = 0; e < kChunk; ++e) qv[e] = e < cnt ? __ldg(qp + e) : 0.0f;
+    }
+}
+
+__device__ __forceinline__ bool q_invalid(const float* qv, int cnt) {
+    bool bad = false;
+#pragma unroll
+    for (int e = 0; e < kChunk; ++e) bad |= e < cnt && !(qv[e] >= 0.0f && qv[e] <= FLT_MAX);
+    return bad;
+}
+
+// Write a sampled row's outputs: the kept drafts, the drawn token, -1 after.
+__device__ __forceinline__ void write_sampled(const VerifyArgs& a, int b, int k, int j, int token, int st,
+                                              const int* xs) {
+    for (int i = 0; i <= k; ++i) {
+        int tok = -1;
+        if (i < j)
+            tok = xs[i];
+        else if (i == j)
+            tok = token;
+        a.out_tokens[static_cast<long long>(b) * (k + 1) + i] = tok;
+    }
+    a.num_accepted[b] = j;
+    if (a.row_status) a.row_status[b] = st;
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char dyn_smem[];
-    __shared__ ClusterSmem sh;
+    __shared__ __align__(16) ClusterSmem sh;
     constexpr int esz = BF16 ? 2 : 4;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
+    const bool producer = (warp == kConsumerWarps);
     const uint32_t rank = cluster_rank();
     const uint32_t C = cluster_size();
     const int b = blockIdx.x / C;
@@ -177,20 +425,22 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
             u1 = __ldg(a.u + ub + 1);
         }
     }
-
     if (tid <= k) {
         // geometry of this CTA's slice of position tid
         const long long e0 = (static_cast<long long>(b) * (k + 1) + tid) * V + v0;
         const uintptr_t addr = reinterpret_cast<uintptr_t>(lg + e0 * esz);
         int h = static_cast<int>(((16 - (addr & 15)) & 15) / esz);
         if (h > n) h = n;
-        const int nb = ((n - h) * esz) & ~15;
         sh.head[tid] = h;
-        sh.nbytes[tid] = nb;
+        sh.nbytes[tid] = ((n - h) * esz) & ~15;
     }
     if (tid < 128) sh.exp2tab[tid] = g_exp2_table[tid];
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&sh.mbar[s]), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&sh.full[s]), 1);
+            mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
+        }
+        sh.timeout = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
     }
@@ -204,71 +454,93 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
         sh.tstart[k + 1] = acc;
     }
     __syncthreads();
-    const int total_tiles = t_ok ? sh.tstart[k + 1] : 0;
+    const int total1 = t_ok ? sh.tstart[k + 1] : 0;
 
-    auto issue = [&](int tt) {
-        int i = 0;
-        while (sh.tstart[i + 1] <= tt) ++i;
-        const int off = (tt - sh.tstart[i]) * kTileBytes;
-        const int bytes = min(kTileBytes, sh.nbytes[i] - off);
-        const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + v0 + sh.head[i];
-        const int slot = tt % kStages;
-        const uint32_t bar = smem_u32(&sh.mbar[slot]);
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(bytes));
-        bulk_g2s(smem_u32(ring + slot * kTileBytes), lg + e0 * esz + off, static_cast<uint32_t>(bytes), bar);
+    // Ring protocol.  Stage use number `it` (counted identically by producer
+    // and consumers across both passes) occupies slot it % kStages; its full
+    // barrier completes phase (it / kStages) & 1 when the copies land, its
+    // empty barrier when the four consumer warps have released it.
+    auto prod_acquire = [&](int it) -> bool {
+        if (it < kStages) return true;
+        const int slot = it % kStages;
+        return mbar_wait_bounded(smem_u32(&sh.empty[slot]), ((it / kStages) & 1) ^ 1, kWaitPolls);
     };
-
-    int issued = 0;
-    if (tid == 0) {
-        for (; issued < min(kStages, total_tiles); ++issued) issue(issued);
-    }
-    // dependent scalar loads of the accept test (x_i has landed by now)
-    if (warp == 0 && lane < k && t_ok && !greedy && xi >= 0 && xi < V) {
-        const long long row = static_cast<long long>(b) * (k + 1) + lane;
-        Lx = load_logit(a.logits, row * V + xi, BF16);
-        qx = __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi);
-    }
+    auto cons_wait = [&](int it) -> bool {
+        const int slot = it % kStages;
+        return mbar_wait_bounded(smem_u32(&sh.full[slot]), (it / kStages) & 1, kWaitPolls);
+    };
+    auto cons_release = [&](int it) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.empty[it % kStages]));
+    };
+    int it_prod = 0, it_cons = 0;
 
     // ---------------------------------------------------------------- pass 1
-    bool timed_out = false;
-    int t = 0;
-    for (int i = 0; i <= k && t_ok; ++i) {
-        float m = -INFINITY, s = 0.0f;  // sampled state
-        int arg = 0x7fffffff;           // greedy state (m holds the best value)
-        bool nan_seen = false;
-        const long long row_e0 = (static_cast<long long>(b) * (k + 1) + i) * V + v0;
-        const int h = sh.head[i];
-        const int ntiles = sh.tstart[i + 1] - sh.tstart[i];
-        const int interior = sh.nbytes[i] / esz;
-
-        auto scalar_elem = [&](int rel) {
-            const float l = load_logit(a.logits, row_e0 + rel, BF16);
-            if (greedy) {
-                if (l != l) nan_seen = true;
-                if (l > m) {
-                    m = l;
-                    arg = static_cast<int>(v0 + rel);
+    if (producer) {
+        if (lane == 0) {
+            for (int tt = 0; tt < total1; ++tt, ++it_prod) {
+                if (sh.timeout || !prod_acquire(it_prod)) {
+                    atomicOr(&sh.timeout, 1);
+                    break;
                 }
-            } else {
-                online_add(m, s, l, c);
+                int i = 0;
+                while (sh.tstart[i + 1] <= tt) ++i;
+                const int off = (tt - sh.tstart[i]) * kTileBytes;
+                const int bytes = min(kTileBytes, sh.nbytes[i] - off);
+                const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + v0 + sh.head[i];
+                const int slot = it_prod % kStages;
+                const uint32_t bar = smem_u32(&sh.full[slot]);
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(bytes));
+                bulk_g2s(smem_u32(ring + slot * kTileBytes), lg + e0 * esz + off, static_cast<uint32_t>(bytes), bar);
             }
-        };
-        if (tid == 0)
-            for (int e = 0; e < h; ++e) scalar_elem(e);
+        }
+        it_prod = __shfl_sync(0xffffffffu, it_prod, 0);
+    } else {
+        int t = 0;
+        for (int i = 0; i <= k && t_ok; ++i) {
+            float m = -INFINITY, s = 0.0f;  // sampled state
+            int arg = 0x7fffffff;           // greedy state (m holds the best value)
+            bool nan_seen = false;
+            const long long row_e0 = (static_cast<long long>(b) * (k + 1) + i) * V + v0;
+            const int h = sh.head[i];
+            const int ntiles = sh.tstart[i + 1] - sh.tstart[i];
+            const int interior = sh.nbytes[i] / esz;
 
-        for (int lt = 0; lt < ntiles; ++lt, ++t) {
-            const int slot = t % kStages;
-            const uint32_t phase = (t / kStages) & 1;
-            const bool ok = timed_out ? false : mbar_wait_bounded(smem_u32(&sh.mbar[slot]), phase, kWaitPolls);
-            const int bytes = min(kTileBytes, sh.nbytes[i] - lt * kTileBytes);
-            const int nch = bytes >> 4;
-            const uint32_t tile = smem_u32(ring + slot * kTileBytes);
-            if (ok) {
-                constexpr int kPer = kTileBytes / 16 / kThreads;  // 16-byte chunks per thread
+            auto scalar_elem = [&](int rel) {
+                const float l = load_logit(a.logits, row_e0 + rel, BF16);
+                if (greedy) {
+                    if (l != l) nan_seen = true;
+                    if (l > m) {
+                        m = l;
+                        arg = static_cast<int>(v0 + rel);
+                    }
+                } else {
+                    online_add(m, s, l, c);
+                }
+            };
+            if (tid == 0)
+                for (int e = 0; e < h; ++e) scalar_elem(e);
+
+            for (int lt = 0; lt < ntiles; ++lt, ++t, ++it_cons) {
+                if (t == 2 && warp == 0 && lane < k && !greedy && xi >= 0 && xi < V) {
+                    // the accept test's scalars; x_i has long arrived
+                    const long long row = static_cast<long long>(b) * (k + 1) + lane;
+                    Lx = load_logit(a.logits, row * V + xi, BF16);
+                    qx = __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi);
+                }
+                const bool ok = !sh.timeout && cons_wait(it_cons);
+                const int bytes = min(kTileBytes, sh.nbytes[i] - lt * kTileBytes);
+                const int nch = bytes >> 4;
+                const uint32_t tile = smem_u32(ring + (it_cons % kStages) * kTileBytes);
+                if (!ok) {
+                    atomicOr(&sh.timeout, 1);
+                    continue;
+                }
+                constexpr int kPer = kTileBytes / 16 / kConsumers;  // 16-byte chunks per thread
                 uint4 w[kPer];
 #pragma unroll
                 for (int r = 0; r < kPer; ++r) {
-                    const int ch = tid + r * kThreads;
+                    const int ch = tid + r * kConsumers;
                     if (ch < nch) {
                         w[r] = ld_shared_v4(tile + ch * 16);
                     } else if (BF16) {
@@ -278,7 +550,7 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
                         w[r] = make_uint4(ni, ni, ni, ni);
                     }
                 }
-                // tile maximum of this thread's elements
+                cons_release(it_cons);  // the data is in registers
                 float lmax;
                 if (BF16) {
                     uint32_t mx = 0xff80ff80u, mn = 0xff80ff80u;
@@ -310,7 +582,7 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
                         bool found = false;
 #pragma unroll
                         for (int r = 0; r < kPer; ++r) {
-                            const int ch = tid + r * kThreads;
+                            const int ch = tid + r * kConsumers;
                             const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
@@ -350,7 +622,7 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
                     if (has_nan) s = __uint_as_float(0x7fc00000u);
                 } else {
                     if (lmax > m) {
-                        s = (m == -INFINITY) ? 0.0f : s * ex2((m - lmax) * c);
+                        s = (m == -INFINITY) ? s * 0.0f : s * ex2((m - lmax) * c);
                         m = lmax;
                     }
                     const f2 mm = pack2(m, m), cc = pack2(c, c);
@@ -369,7 +641,8 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
                         } else {
 #pragma unroll
                             for (int q4 = 0; q4 < 4; q4 += 2) {
-                                const f2 d = mul2(sub2(pack2(__uint_as_float(ws[q4]), __uint_as_float(ws[q4 + 1])), mm), cc);
+                                const f2 d =
+                                    mul2(sub2(pack2(__uint_as_float(ws[q4]), __uint_as_float(ws[q4 + 1])), mm), cc);
                                 float d0, d1;
                                 unpack2(d, d0, d1);
                                 acc = add2(acc, pack2(ex2(d0), ex2(d1)));
@@ -381,41 +654,38 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
                     s += a0 + a1;
                 }
             }
-            // the slot is free once every thread is past it; a timeout
-            // anywhere in the block stops the stream for the whole block
-            if (__syncthreads_or(!ok)) timed_out = true;
-            if (tid == 0 && !timed_out && issued < total_tiles) issue(issued++);
-        }
-        if (tid == 0)
-            for (int e = h + interior; e < n; ++e) scalar_elem(e);
+            if (tid == 0)
+                for (int e = h + interior; e < n; ++e) scalar_elem(e);
 
-        // warp reduction of this position's partial
-        if (greedy) {
-            for (int off = 16; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                const int a2 = __shfl_xor_sync(0xffffffffu, arg, off);
-                merge_arg(m, arg, m2, a2);
+            // warp reduction of this position's partial
+            if (greedy) {
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+                    const int a2 = __shfl_xor_sync(0xffffffffu, arg, off);
+                    merge_arg(m, arg, m2, a2);
+                }
+                nan_seen = __any_sync(0xffffffffu, nan_seen);
+            } else {
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+                    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+                    merge_ms(m, s, m2, s2, c);
+                }
             }
-            nan_seen = __any_sync(0xffffffffu, nan_seen);
-        } else {
-            for (int off = 16; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-                merge_ms(m, s, m2, s2, c);
-            }
+            if (lane == 0) sh.wpart[warp][i] = Partial{m, s, arg, nan_seen ? 1 : 0};
         }
-        if (lane == 0) sh.wpart[warp][i] = Partial{m, s, arg, nan_seen ? 1 : 0};
-    }
-    if (timed_out && tid == 0) {
-        // let the copies still in flight (at most one per stage) land before
-        // the buffers are reused or the block exits
-        for (int tt = max(0, issued - kStages); tt < issued; ++tt)
-            mbar_wait_bounded(smem_u32(&sh.mbar[tt % kStages]), (tt / kStages) & 1, kWaitPolls);
+        // rows too short to reach the third tile load the scalars here
+        if (t_ok && total1 <= 2 && warp == 0 && lane < k && !greedy && xi >= 0 && xi < V) {
+            const long long row = static_cast<long long>(b) * (k + 1) + lane;
+            Lx = load_logit(a.logits, row * V + xi, BF16);
+            qx = __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi);
+        }
     }
     __syncthreads();
+    const bool timed_out = sh.timeout != 0;
     if (tid <= k && t_ok) {
         Partial p = sh.wpart[0][tid];
-        for (int w = 1; w < kWarps; ++w) {
+        for (int w = 1; w < kConsumerWarps; ++w) {
             const Partial o = sh.wpart[w][tid];
             if (greedy) {
                 merge_arg(p.m, p.arg, o.m, o.arg);
@@ -425,7 +695,11 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
             }
         }
         if (timed_out) p.flags |= 2;
-        sh.part[tid] = p;
+        // push this CTA's partial of position tid into every CTA of the cluster
+        const uint32_t local = smem_u32(&sh.allpart[rank][tid]);
+        for (uint32_t r = 0; r < C; ++r)
+            st_cluster_v4(map_rank(local, r), __float_as_uint(p.m), __float_as_uint(p.s), static_cast<uint32_t>(p.arg),
+                          static_cast<uint32_t>(p.flags));
     }
     cluster_sync();  // #1: every CTA's partials are visible
 
@@ -434,17 +708,13 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
         float M = -INFINITY, S = 0.0f;
         int A = 0x7fffffff, flags = 0;
         if (lane <= k && t_ok) {
-            const uint32_t local = smem_u32(&sh.part[lane]);
             for (uint32_t r = 0; r < C; ++r) {
-                const uint32_t ra = map_rank(local, r);
-                const float m2 = ld_cluster_f32(ra);
-                const float s2 = ld_cluster_f32(ra + 4);
-                const int a2 = ld_cluster_s32(ra + 8);
-                flags |= ld_cluster_s32(ra + 12);
+                const Partial pr = sh.allpart[r][lane];
+                flags |= pr.flags;
                 if (greedy)
-                    merge_arg(M, A, m2, a2);
+                    merge_arg(M, A, pr.m, pr.arg);
                 else
-                    merge_ms(M, S, m2, s2, c);
+                    merge_ms(M, S, pr.m, pr.s, c);
             }
             if (greedy && A == 0x7fffffff) A = 0;  // every value is -inf: index 0
         }
@@ -466,17 +736,14 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
                     if (!err) {
                         // p_i(x_i) with the double-float exponential (a masked
                         // entry, logit -inf, has p = 0)
-                        const double cd = 1.4426950408889634 / static_cast<double>(T);
-                        const float ch = static_cast<float>(cd);
-                        const float cl = static_cast<float>(cd - static_cast<double>(ch));
-                        if (Lx != -INFINITY) {
-                            float dh = Lx - M, dl = 0.0f;
-                            if (!BF16) two_sum(Lx, -M, dh, dl);  // fp32 logits: keep the rounding error
-                            const float xh = dh * ch;
-                            const float xl = fmaf(dh, cl, fmaf(dh, ch, -xh)) + dl * ch;
-                            const float2 e = exp2dd(xh, xl, sh.exp2tab);
-                            p = (e.x + e.y) / S;
-                        }
+                        const df c2 = log2e_over(T);
+                        RowConst rc;
+                        rc.M = M;
+                        rc.s1 = S;
+                        rc.thr = 0.0f;
+                        rc.ch = c2.hi;
+                        rc.cl = c2.lo;
+                        p = df_val(exact_weight<BF16>(Lx, 0.0f, MODE_BONUS, rc, df_make(0.0f), sh.exp2tab)) / S;
                         const float rho = fminf(1.0f, p / fmaxf(qx, 1e-12f));
                         stop = !(u0 < rho);
                     } else {
@@ -497,13 +764,16 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
         const float Mj = __shfl_sync(0xffffffffu, M, j);
         const float Sj = __shfl_sync(0xffffffffu, S, j);
         const int Aj = __shfl_sync(0xffffffffu, A, j);
+        const float ujj = __shfl_sync(0xffffffffu, u1, j);
         if (lane == 0) {
+            sh.uj = ujj;
             sh.j = j;
             sh.status = st;
             sh.Mj = Mj;
             sh.sj = Sj;
             sh.mode = (j < k) ? MODE_RESIDUAL : MODE_BONUS;
         }
+        if (lane <= k) sh.xs[lane] = xi;
         // rank 0 writes debug values and, for greedy or failed rows, the outputs
         if (rank == 0) {
             if (lane <= k && t_ok) {
@@ -529,10 +799,6 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
                 }
             }
         }
-        if (lane <= k) {
-            // keep the draft tokens for whoever writes the sampled outputs
-            sh.wpart[0][lane].arg = xi;
-        }
     }
     __syncthreads();
     const bool sample = t_ok && !greedy && !(sh.status & ST_ERRMASK);
@@ -542,222 +808,244 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
     }
 
     // ---------------------------------------------------------------- pass 2
-    if (tid == 0) {
-        const double cd = 1.4426950408889634 / static_cast<double>(T);
-        sh.c_hi = static_cast<float>(cd);
-        sh.c_lo = static_cast<float>(cd - static_cast<double>(sh.c_hi));
-        sh.thr = kLargeP * sh.sj;
-        sh.last_pos = -1;
-    }
-    __syncthreads();
     const int j = sh.j;
-    const float Mj = sh.Mj, sj = sh.sj, thr = sh.thr, ch = sh.c_hi, cl = sh.c_lo;
     const long long lrow = (static_cast<long long>(b) * (k + 1) + j) * V;
     const float* qrow = a.q + (static_cast<long long>(b) * k + (j < k ? j : 0)) * V;
-    const int nch = (n + kChunk - 1) / kChunk;
-    float* ch_hi = reinterpret_cast<float*>(ring);
-    float* ch_lo = ch_hi + kMaxChunks;
-    float* ch_q = ch_lo + kMaxChunks;
+    if (tid == 0) {
+        const df c2 = log2e_over(T);
+        sh.c_hi = c2.hi;
+        sh.c_lo = c2.lo;
+        sh.thr = kLargeP * sh.sj;
+        // bulk copies need 16-byte aligned starts and sizes: both rows
+        // aligned at the slice start, and whole groups of 8 entries
+        const bool la = (reinterpret_cast<uintptr_t>(lg + (lrow + v0) * esz) & 15) == 0;
+        const bool qa = (reinterpret_cast<uintptr_t>(qrow + v0) & 15) == 0;
+        sh.p2fast = la && (j == k || qa) && (n % kChunk) == 0;
+        sh.ntiles2 = (n + kP2Elems - 1) / kP2Elems;
+    }
+    __syncthreads();
+    RowConst rc;
+    rc.M = sh.Mj;
+    rc.s1 = sh.sj;
+    rc.thr = sh.thr;
+    rc.ch = sh.c_hi;
+    rc.cl = sh.c_lo;
+    const bool p2fast = sh.p2fast != 0;
+    const int ntiles2 = sh.ntiles2;
     int mode = sh.mode;
 
-    // weights of one chunk: returns its (hi, lo) and its q sum over positive
-    // residuals; adds e to the thread's (eh, el) sum (residual mode)
-    auto chunk_weights = [&](int cidx, int md, float& whi, float& wlo, float& wq, float& teh, float& tel,
-                             bool& qbad) {
-        const long long e0 = v0 + static_cast<long long>(cidx) * kChunk;
-        const int cnt = min(kChunk, n - cidx * kChunk);
-        float lv[kChunk], qv[kChunk];
-        const unsigned char* lp = lg + (lrow + e0) * esz;
-        if (cnt == kChunk && (reinterpret_cast<uintptr_t>(lp) & 15) == 0) {
-            if (BF16) {
-                const uint4 w = ld_stream_v4(lp);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    lv[2 * q4] = bf16_lo(ws[q4]);
-                    lv[2 * q4 + 1] = bf16_hi(ws[q4]);
-                }
-            } else {
-                const uint4 w0 = ld_stream_v4(lp), w1 = ld_stream_v4(lp + 16);
-                lv[0] = __uint_as_float(w0.x); lv[1] = __uint_as_float(w0.y);
-                lv[2] = __uint_as_float(w0.z); lv[3] = __uint_as_float(w0.w);
-                lv[4] = __uint_as_float(w1.x); lv[5] = __uint_as_float(w1.y);
-                lv[6] = __uint_as_float(w1.z); lv[7] = __uint_as_float(w1.w);
-            }
+    // one stop-row entry by tile-local index, from the staged tile or from global memory
+    auto fetch1 = [&](bool staged, uint32_t base, int e0, int idx, float& l, float& q) {
+        if (staged) {
+            l = BF16 ? __uint_as_float(static_cast<uint32_t>(ld_shared_u16(base + kP2Elems * 4 + idx * 2)) << 16)
+                     : ld_shared_f32(base + kP2Elems * 4 + idx * 4);
+            q = mode == MODE_RESIDUAL ? ld_shared_f32(base + idx * 4) : 0.0f;
         } else {
-#pragma unroll
-            for (int e = 0; e < kChunk; ++e) lv[e] = e < cnt ? load_logit(a.logits, lrow + e0 + e, BF16) : -INFINITY;
+            l = load_logit(a.logits, lrow + v0 + e0 + idx, BF16);
+            q = mode == MODE_RESIDUAL ? __ldg(qrow + v0 + e0 + idx) : 0.0f;
         }
-        if (md == MODE_RESIDUAL) {
-            const float* qp = qrow + e0;
-            if (cnt == kChunk && (reinterpret_cast<uintptr_t>(qp) & 15) == 0) {
-                const uint4 w0 = ld_stream_v4(qp), w1 = ld_stream_v4(qp + 4);
-                qv[0] = __uint_as_float(w0.x); qv[1] = __uint_as_float(w0.y);
-                qv[2] = __uint_as_float(w0.z); qv[3] = __uint_as_float(w0.w);
-                qv[4] = __uint_as_float(w1.x); qv[5] = __uint_as_float(w1.y);
-                qv[6] = __uint_as_float(w1.z); qv[7] = __uint_as_float(w1.w);
-            } else {
-#pragma unroll
-                for (int e = 0; e < kChunk; ++e) qv[e] = e < cnt ? __ldg(qp + e) : 0.0f;
-            }
-#pragma unroll
-            for (int e = 0; e < kChunk; ++e) qbad |= !(qv[e] >= 0.0f && qv[e] <= FLT_MAX);
-        }
-        float rs = 0.0f, qs = 0.0f, es = 0.0f;
-        float lh = 0.0f, ll = 0.0f;
-#pragma unroll
-        for (int e = 0; e < kChunk; ++e) {
-            const float l = lv[e];
-            if (e >= cnt || l == -INFINITY) continue;  // masked entries weigh nothing
-            const float dh = l - Mj;
-            const float xh = dh * ch;
-            float xl = fmaf(dh, cl, fmaf(dh, ch, -xh));
-            float ef = ex2(xh);
-            ef = fmaf(ef, xl * kLn2, ef);
-            if (ef > thr) {
-                if (!BF16) {
-                    float d2, dl;
-                    two_sum(l, -Mj, d2, dl);
-                    xl = fmaf(dl, ch, xl);
-                }
-                const float2 ed = exp2dd(xh, xl, sh.exp2tab);
-                if (md == MODE_RESIDUAL) {
-                    const float qq = qv[e];
-                    const float ph = sj * qq;
-                    const float pl = fmaf(sj, qq, -ph);
-                    float rh, rl;
-                    two_sum(ed.x, -ph, rh, rl);
-                    rl = rl + (ed.y - pl);
-                    if (rh + rl > 0.0f) {
-                        df_add(lh, ll, rh, rl);
-                        qs += qq;
-                    }
-                    df_add(teh, tel, ed.x, ed.y);
-                } else {
-                    df_add(lh, ll, ed.x, ed.y);
-                }
-            } else {
-                if (md == MODE_RESIDUAL) {
-                    const float r = fmaf(-sj, qv[e], ef);
-                    if (r > 0.0f) {
-                        rs += r;
-                        qs += qv[e];
-                    }
-                    es += ef;
-                } else {
-                    rs += ef;
-                }
-            }
-        }
-        float hi, lo;
-        two_sum(rs, lh, hi, lo);
-        whi = hi;
-        wlo = lo + ll;
-        wq = qs;
-        if (md == MODE_RESIDUAL) df_add(teh, tel, es, 0.0f);
     };
 
     for (;;) {
-        // sweep: chunk weights of this CTA's slice of row j
-        float teh = 0.0f, tel = 0.0f;
+        df te = df_make(0.0f);  // this thread's sum of e (residual mode)
         bool qbad = false;
-        for (int cidx = tid; cidx < nch; cidx += kThreads) {
-            float whi, wlo, wq;
-            chunk_weights(cidx, mode, whi, wlo, wq, teh, tel, qbad);
-            ch_hi[cidx] = whi;
-            ch_lo[cidx] = wlo;
-            ch_q[cidx] = wq;
-        }
-        __syncthreads();
-        // per-thread sums over contiguous chunk blocks (vocabulary order)
-        const int cpt = (nch + kThreads - 1) / kThreads;
-        const int c_begin = min(nch, tid * cpt), c_end = min(nch, c_begin + cpt);
-        float sh_hi = 0.0f, sh_lo = 0.0f, sq = 0.0f;
-        for (int cc = c_begin; cc < c_end; ++cc) {
-            df_add(sh_hi, sh_lo, ch_hi[cc], ch_lo[cc]);
-            sq += ch_q[cc];
-        }
-        double w_d = static_cast<double>(sh_hi) + static_cast<double>(sh_lo);
-        double q_d = static_cast<double>(sq);
-        double e_d = static_cast<double>(teh) + static_cast<double>(tel);
-        sh.thr_w[tid] = w_d;
-        sh.thr_q[tid] = q_d;
-        for (int off = 16; off > 0; off >>= 1) {
-            w_d += __shfl_xor_sync(0xffffffffu, w_d, off);
-            q_d += __shfl_xor_sync(0xffffffffu, q_d, off);
-            e_d += __shfl_xor_sync(0xffffffffu, e_d, off);
-        }
-        __shared__ double wsum[kWarps][3];
-        const int any_qbad = __syncthreads_or(qbad ? 1 : 0);
-        if (lane == 0) {
-            wsum[warp][0] = w_d;
-            wsum[warp][1] = e_d;
-            wsum[warp][2] = q_d;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            double t0 = 0.0, t1 = 0.0, t2 = 0.0;
-            for (int w = 0; w < kWarps; ++w) {
-                t0 += wsum[w][0];
-                t1 += wsum[w][1];
-                t2 += wsum[w][2];
+        if (producer) {
+            if (p2fast && lane == 0) {
+                for (int t2 = 0; t2 < ntiles2; ++t2, ++it_prod) {
+                    if (sh.timeout || !prod_acquire(it_prod)) {
+                        atomicOr(&sh.timeout, 1);
+                        break;
+                    }
+                    const int e0 = t2 * kP2Elems;
+                    const int cnt = min(kP2Elems, n - e0);
+                    const int slot = it_prod % kStages;
+                    const uint32_t bar = smem_u32(&sh.full[slot]);
+                    const uint32_t dst = smem_u32(ring + slot * kTileBytes);
+                    const uint32_t lbytes = static_cast<uint32_t>(cnt * esz);
+                    const uint32_t qbytes = mode == MODE_RESIDUAL ? static_cast<uint32_t>(cnt * 4) : 0u;
+                    mbar_arrive_expect_tx(bar, lbytes + qbytes);
+                    bulk_g2s(dst + kP2Elems * 4, lg + (lrow + v0 + e0) * esz, lbytes, bar);
+                    if (qbytes) bulk_g2s(dst, qrow + v0 + e0, qbytes, bar);
+                }
             }
-            sh.tot[0] = t0;
-            sh.tot[1] = t1;
-            sh.tot[2] = t2;
-            sh.tot[3] = any_qbad ? 1.0 : 0.0;
+            it_prod = __shfl_sync(0xffffffffu, it_prod, 0);
+        } else {
+            // one warp per tile of 1024 entries; lane l owns entries [32l, 32l+32)
+            const int it0 = it_cons;
+            for (int t2 = warp; t2 < ntiles2; t2 += kConsumerWarps) {
+                const int it = it0 + t2;
+                const int e0 = t2 * kP2Elems;
+                const int cnt = min(kP2Elems, n - e0);
+                const int my0 = lane * kLaneEntries;
+                bool ok = true;
+                uint32_t base = 0;
+                if (p2fast) {
+                    ok = __all_sync(0xffffffffu, !sh.timeout && cons_wait(it));
+                    base = smem_u32(ring + (it % kStages) * kTileBytes);
+                    if (!ok) atomicOr(&sh.timeout, 1);
+                }
+                Lane32 L;
+                lane32_init(L);
+                if (ok) {
+#pragma unroll 2
+                    for (int i = 0; i < 4; ++i) {
+                        const int c = (i + lane) & 3;  // rotated: spreads the lanes over the banks
+                        const int off = my0 + c * kChunk;
+                        const int nv = max(0, min(kChunk, cnt - off));
+                        float lv[kChunk], qv[kChunk];
+#pragma unroll
+                        for (int e = 0; e < kChunk; ++e) {
+                            lv[e] = -INFINITY;
+                            qv[e] = 0.0f;
+                        }
+                        if (nv > 0) {
+                            if (p2fast) {
+                                if (BF16) {
+                                    const uint4 w = ld_shared_v4(base + kP2Elems * 4 + off * 2);
+                                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                                    for (int q4 = 0; q4 < 4; ++q4) {
+                                        lv[2 * q4] = bf16_lo(ws[q4]);
+                                        lv[2 * q4 + 1] = bf16_hi(ws[q4]);
+                                    }
+                                } else {
+                                    const uint4 w0 = ld_shared_v4(base + kP2Elems * 4 + off * 4);
+                                    const uint4 w1 = ld_shared_v4(base + kP2Elems * 4 + off * 4 + 16);
+                                    lv[0] = __uint_as_float(w0.x); lv[1] = __uint_as_float(w0.y);
+                                    lv[2] = __uint_as_float(w0.z); lv[3] = __uint_as_float(w0.w);
+                                    lv[4] = __uint_as_float(w1.x); lv[5] = __uint_as_float(w1.y);
+                                    lv[6] = __uint_as_float(w1.z); lv[7] = __uint_as_float(w1.w);
+                                }
+                                if (mode == MODE_RESIDUAL) {
+                                    const uint4 w0 = ld_shared_v4(base + off * 4);
+                                    const uint4 w1 = ld_shared_v4(base + off * 4 + 16);
+                                    qv[0] = __uint_as_float(w0.x); qv[1] = __uint_as_float(w0.y);
+                                    qv[2] = __uint_as_float(w0.z); qv[3] = __uint_as_float(w0.w);
+                                    qv[4] = __uint_as_float(w1.x); qv[5] = __uint_as_float(w1.y);
+                                    qv[6] = __uint_as_float(w1.z); qv[7] = __uint_as_float(w1.w);
+                                }
+                            } else {
+                                // unaligned rows: the same tiles, read straight from global memory
+                                load8_logits<BF16>(a.logits, lrow + v0 + e0 + off, nv, lv);
+                                if (mode == MODE_RESIDUAL) load8_q(qrow + v0 + e0 + off, nv, qv);
+                            }
+                        }
+                        if (mode == MODE_RESIDUAL) qbad |= q_invalid(qv, nv);
+                        lane32_fast8(L, c, lv, qv, nv, mode, rc);
+                    }
+                    // large entries, each lane its own in entry order (the warp
+                    // runs as many rounds as its busiest lane has entries)
+                    for (uint32_t m = L.large; m; m &= m - 1) {
+                        const int bit = __ffs(m) - 1;
+                        float l, q;
+                        fetch1(p2fast, base, e0, my0 + bit, l, q);
+                        df w, e;
+                        float wq;
+                        large_weight<BF16>(l, q, mode, rc, sh.exp2tab, w, wq, e);
+                        lane32_add_large(L, bit >> 3, w, wq, e, mode);
+                    }
+                    if (p2fast) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cnt(smem_u32(&sh.empty[it % kStages]), kConsumerWarps);
+                    }
+                }
+                float lq;
+                const df lw = lane32_total(L, lq);
+                sh.lane_hi[t2][lane] = lw.hi;
+                sh.lane_lo[t2][lane] = lw.lo;
+                sh.lane_q[t2][lane] = lq;
+                te = df_sum(te, L.e);
+                const df tw = df_warp_total(lw);
+                float tq = lq;
+                for (int off = 16; off > 0; off >>= 1) tq += __shfl_down_sync(0xffffffffu, tq, off);
+                if (lane == 0) {
+                    sh.tile_hi[t2] = tw.hi;
+                    sh.tile_lo[t2] = tw.lo;
+                    sh.tile_q[t2] = tq;
+                }
+            }
+            it_cons = it0 + ntiles2;
+        }
+        // CTA totals: weights, e (residual mode), q over positive residuals
+        const df tw = df_warp_total(te);
+        const int any_qbad = __syncthreads_or(qbad ? 1 : 0);
+        if (lane == 0 && !producer) {
+            sh.wred_hi[warp] = tw.hi;
+            sh.wred_lo[warp] = tw.lo;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const bool in = lane < ntiles2;
+            const df Wc = df_warp_total(in ? df{sh.tile_hi[lane], sh.tile_lo[lane]} : df_make(0.0f));
+            float vq = in ? sh.tile_q[lane] : 0.0f;
+            for (int off = 16; off > 0; off >>= 1) vq += __shfl_down_sync(0xffffffffu, vq, off);
+            const df Ec = df_warp_total(lane < kConsumerWarps ? df{sh.wred_hi[lane], sh.wred_lo[lane]} : df_make(0.0f));
+            // push this CTA's totals into every CTA of the cluster (lane r -> rank r)
+            const uint32_t flags2 = static_cast<uint32_t>((any_qbad ? 1 : 0) | (sh.timeout ? 2 : 0));
+            const df Wb = df_shfl(Wc, 0), Eb = df_shfl(Ec, 0);
+            const float qb = __shfl_sync(0xffffffffu, vq, 0);
+            if (lane < static_cast<int>(C)) {
+                const uint32_t ra = map_rank(smem_u32(&sh.alltot[rank][0]), lane);
+                st_cluster_v4(ra, __float_as_uint(Wb.hi), __float_as_uint(Wb.lo), __float_as_uint(Eb.hi),
+                              __float_as_uint(Eb.lo));
+                st_cluster_v2(ra + 16, __float_as_uint(qb), flags2);
+            }
         }
         cluster_sync();  // #2: CTA totals visible
-        if (tid == 0) {
-            const uint32_t local = smem_u32(&sh.tot[0]);
-            double wr[16], qr[16];
-            double s_prec = 0.0, qflag = 0.0;
-            for (uint32_t r = 0; r < C; ++r) {
-                const uint32_t ra = map_rank(local, r);
-                wr[r] = ld_cluster_f64(ra);
-                s_prec += ld_cluster_f64(ra + 8);
-                qr[r] = ld_cluster_f64(ra + 16);
-                qflag += ld_cluster_f64(ra + 24);
+        if (warp == 0) {
+            // lane r holds rank r's totals
+            const bool has = lane < static_cast<int>(C);
+            df wr = df_make(0.0f), er = df_make(0.0f);
+            float qr = 0.0f;
+            int fl = 0;
+            if (has) {
+                wr = df{sh.alltot[lane][0], sh.alltot[lane][1]};
+                er = df{sh.alltot[lane][2], sh.alltot[lane][3]};
+                qr = sh.alltot[lane][4];
+                fl = static_cast<int>(__float_as_uint(sh.alltot[lane][5]));
             }
-            double delta = 0.0;
-            if (mode == MODE_RESIDUAL) delta = s_prec - static_cast<double>(sj);
-            double W = 0.0;
-            for (uint32_t r = 0; r < C; ++r) {
-                wr[r] -= delta * qr[r];
-                W += wr[r];
-            }
-            sh.delta = delta;
-            sh.s_prec = (mode == MODE_RESIDUAL) ? s_prec : 0.0;
-            if (mode == MODE_RESIDUAL && qflag > 0.0) {
-                // a draft probability of the residual row is NaN, negative or infinite
-                sh.owner = -2;
-                if (rank == 0) {
-                    for (int i = 0; i <= k; ++i) a.out_tokens[static_cast<long long>(b) * (k + 1) + i] = -1;
+            const df s_prec = df_shfl(df_warp_total(er), 0);
+            const bool any_q = __any_sync(0xffffffffu, (fl & 1) != 0);
+            const bool any_to = __any_sync(0xffffffffu, (fl & 2) != 0);
+            const float delta = mode == MODE_RESIDUAL ? df_val(df_sum(s_prec, df_make(-rc.s1))) : 0.0f;
+            wr = df_sum(wr, df_make(-delta * qr));
+            const df Wt = df_shfl(df_warp_total(wr), 0);
+            int bad = 0;
+            if (any_to)
+                bad = ST_TIMEOUT;
+            else if (mode == MODE_RESIDUAL && any_q)
+                bad = ST_QBAD;  // a draft probability of the residual row is NaN, negative or infinite
+            if (bad) {
+                if (lane == 0) sh.owner = -2;
+                if (rank == 0 && lane <= k) a.out_tokens[static_cast<long long>(b) * (k + 1) + lane] = -1;
+                if (rank == 0 && lane == 0) {
                     a.num_accepted[b] = 0;
-                    if (a.row_status) a.row_status[b] = sh.status | ST_QBAD;
+                    if (a.row_status) a.row_status[b] = sh.status | bad;
                 }
-            } else if (mode == MODE_RESIDUAL && !(W > 0.0)) {
-                sh.mode = MODE_FALLBACK;
-                sh.owner = -1;
+            } else if (mode == MODE_RESIDUAL && !(Wt.hi + Wt.lo > 0.0f)) {
+                if (lane == 0) {
+                    sh.mode = MODE_FALLBACK;
+                    sh.owner = -1;
+                }
             } else {
-                const float uj = a.u[(static_cast<long long>(b) * (k + 1) + j) * 2 + 1];
-                const double target = static_cast<double>(uj) * W;
-                double pre = 0.0;
-                int owner = -1, last = -1;
-                for (uint32_t r = 0; r < C; ++r) {
-                    if (wr[r] > 0.0) last = static_cast<int>(r);
-                    if (owner < 0 && target < pre + wr[r]) {
-                        owner = static_cast<int>(r);
-                        sh.t_local = target - pre;
-                    }
-                    if (owner < 0) pre += wr[r];
+                const df target = df_mul_f(Wt, sh.uj);
+                const df incl = df_warp_incl_scan(wr, lane);
+                const df excl = df_sum(incl, df_neg(wr));
+                const bool positive = has && (wr.hi + wr.lo > 0.0f);
+                const unsigned hit =
+                    __ballot_sync(0xffffffffu, positive && !df_less(target, excl) && df_less(target, incl));
+                const unsigned pos = __ballot_sync(0xffffffffu, positive);
+                const int owner = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : 0);
+                const df t_loc = df_sum(target, df_neg(df_shfl(excl, owner)));
+                if (lane == 0) {
+                    sh.owner = owner;
+                    sh.t_hi = hit ? t_loc.hi : INFINITY;
+                    sh.t_lo = hit ? t_loc.lo : 0.0f;
+                    sh.delta = delta;
+                    sh.sp_hi = s_prec.hi;
+                    sh.sp_lo = s_prec.lo;
+                    if (rank == 0 && a.dbg_resid && mode == MODE_RESIDUAL) a.dbg_resid[b] = df_val(Wt) / df_val(s_prec);
                 }
-                if (owner < 0) {
-                    owner = last;
-                    sh.t_local = INFINITY;
-                }
-                sh.owner = owner;
-                if (rank == 0 && a.dbg_resid && mode == MODE_RESIDUAL) a.dbg_resid[b] = static_cast<float>(W / s_prec);
             }
         }
         __syncthreads();
@@ -770,83 +1058,56 @@ __global__ void __launch_bounds__(kThreads) verify_cluster_kernel(const VerifyAr
     }
 
     // ---------------------------------------------------------------- search
-    if (static_cast<int>(rank) == sh.owner) {
-        const double delta = sh.delta;
-        const double tl = sh.t_local;
-        // inclusive scan of the corrected per-thread sums (fixed order)
-        double wt = sh.thr_w[tid] - delta * sh.thr_q[tid];
-        double incl = wt;
-        for (int off = 1; off < 32; off <<= 1) {
-            const double o = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += o;
+    if (static_cast<int>(rank) == sh.owner && warp == 0) {
+        const float delta = sh.delta;
+        const df s_prec = df{sh.sp_hi, sh.sp_lo};
+        df t = df{sh.t_hi, sh.t_lo};
+        int st = sh.status;
+        if (mode == MODE_FALLBACK) st |= ST_ZERO_RESIDUAL;
+        // level 1: the tile (lane t holds tile t)
+        const df vt = lane < ntiles2 ? df_sum(df{sh.tile_hi[lane], sh.tile_lo[lane]}, df_make(-delta * sh.tile_q[lane]))
+                                     : df_make(0.0f);
+        df ti = df_warp_incl_scan(vt, lane);
+        df te2 = df_sum(ti, df_neg(vt));
+        bool pz = vt.hi + vt.lo > 0.0f;
+        unsigned hit = __ballot_sync(0xffffffffu, pz && !df_less(t, te2) && df_less(t, ti));
+        int tile;
+        if (hit) {
+            tile = __ffs(hit) - 1;
+        } else {
+            const unsigned pos = __ballot_sync(0xffffffffu, pz);
+            tile = pos ? 31 - __clz(pos) : 0;  // only through rounding at the top edge
+            t = df_make(INFINITY);
         }
-        __shared__ double wtot[kWarps];
-        if (lane == 31) wtot[warp] = incl;
-        __syncthreads();
-        double before_warp = 0.0;
-        for (int w = 0; w < warp; ++w) before_warp += wtot[w];
-        incl += before_warp;
-        const double excl = incl - wt;
-        if (wt > 0.0) atomicMax(&sh.last_pos, tid);
-        __syncthreads();
-        bool mine = (wt > 0.0) && (tl >= excl) && (tl < incl);
-        // no thread holds the target only through rounding at the top edge:
-        // the last thread with positive weight takes it
-        const int owner_found = __syncthreads_or(mine ? 1 : 0);
-        if (!owner_found && tid == sh.last_pos) mine = true;
-        if (mine) {
-            const int cpt = (nch + kThreads - 1) / kThreads;
-            const int c_begin = min(nch, tid * cpt), c_end = min(nch, c_begin + cpt);
-            double acc = excl;
-            int cstar = -1, clast = -1;
-            for (int cc = c_begin; cc < c_end; ++cc) {
-                const double w = static_cast<double>(ch_hi[cc]) + static_cast<double>(ch_lo[cc]) -
-                                 delta * static_cast<double>(ch_q[cc]);
-                if (w > 0.0) clast = cc;
-                if (tl < acc + w) {
-                    cstar = cc;
-                    break;
-                }
-                acc += w;
-            }
-            if (cstar < 0) {
-                cstar = clast >= 0 ? clast : c_begin;
-                acc = -INFINITY;  // take the chunk's last positive element
-            }
-            // exact walk through the chunk's entries
-            const long long e0 = v0 + static_cast<long long>(cstar) * kChunk;
-            const int cnt = min(kChunk, n - cstar * kChunk);
-            int token = -1, lastpos = -1;
-            for (int e = 0; e < cnt; ++e) {
-                const float l = load_logit(a.logits, lrow + e0 + e, BF16);
-                if (l == -INFINITY) continue;
-                float dh = l - Mj, dl = 0.0f;
-                if (!BF16) two_sum(l, -Mj, dh, dl);
-                const float xh = dh * ch;
-                const float xl = fmaf(dl, ch, fmaf(dh, cl, fmaf(dh, ch, -xh)));
-                const float2 ed = exp2dd(xh, xl, sh.exp2tab);
-                double w = static_cast<double>(ed.x) + static_cast<double>(ed.y);
-                if (mode == MODE_RESIDUAL) {
-                    w -= sh.s_prec * static_cast<double>(__ldg(qrow + e0 + e));
-                    if (w < 0.0) w = 0.0;
-                }
-                if (w > 0.0) lastpos = static_cast<int>(e0 + e);
-                acc += w;
-                if (token < 0 && w > 0.0 && tl < acc) token = static_cast<int>(e0 + e);
-            }
-            if (token < 0) token = lastpos;
-            int st = sh.status;
-            if (mode == MODE_FALLBACK) st |= ST_ZERO_RESIDUAL;
-            for (int i = 0; i <= k; ++i) {
-                int tok = -1;
-                if (i < j)
-                    tok = sh.wpart[0][i].arg;
-                else if (i == j)
-                    tok = token;
-                a.out_tokens[static_cast<long long>(b) * (k + 1) + i] = tok;
-            }
-            a.num_accepted[b] = j;
-            if (a.row_status) a.row_status[b] = st;
+        const df base1 = df_shfl(te2, tile);
+        // level 2: the lane's 32 entries within the tile
+        const df vl = df_sum(df{sh.lane_hi[tile][lane], sh.lane_lo[tile][lane]}, df_make(-delta * sh.lane_q[tile][lane]));
+        const df li = df_sum(base1, df_warp_incl_scan(vl, lane));
+        const df le = df_sum(li, df_neg(vl));
+        pz = vl.hi + vl.lo > 0.0f;
+        hit = __ballot_sync(0xffffffffu, pz && !df_less(t, le) && df_less(t, li));
+        int who;
+        if (hit) {
+            who = __ffs(hit) - 1;
+        } else {
+            const unsigned pos = __ballot_sync(0xffffffffu, pz);
+            who = pos ? 31 - __clz(pos) : 0;
+            t = df_make(INFINITY);
+        }
+        {
+            // the segment's 32 entries, one per lane, with their exact weights
+            const int e0 = tile * kP2Elems;
+            const int cnt = min(kP2Elems, n - e0);
+            const int idx = who * kLaneEntries + lane;
+            float l = -INFINITY, q = 0.0f;
+            if (idx < cnt) fetch1(false, 0, e0, idx, l, q);
+            const df we = exact_weight<BF16>(l, q, mode, rc, s_prec, sh.exp2tab);
+            const bool p = we.hi + we.lo > 0.0f;
+            const df ci = df_sum(df_shfl(le, who), df_warp_incl_scan(we, lane));
+            const unsigned ehit = __ballot_sync(0xffffffffu, p && df_less(t, ci));
+            const unsigned epos = __ballot_sync(0xffffffffu, p);
+            const int wl = ehit ? (__ffs(ehit) - 1) : (epos ? 31 - __clz(epos) : 0);
+            if (lane == 0) write_sampled(a, b, k, j, static_cast<int>(v0 + e0 + who * kLaneEntries + wl), st, sh.xs);
         }
     }
     cluster_sync();  // #3: no CTA leaves while a peer may still read its totals

@@ -1,7 +1,7 @@
 // verify_warp.cuh -- verify kernel for small vocabularies: one warp per
 // sequence, lanes striding over V.  Same rule, same status bits and same
 // inverse-CDF convention as the split-vocabulary kernel; here the whole stop
-// row is weighted with the double-float exponential and summed in float64,
+// row is weighted with the double-float exponential and summed as float pairs,
 // which costs little at small V.
 #pragma once
 #include <cfloat>
@@ -15,15 +15,6 @@ namespace specv {
 
 constexpr int kWarpKernelMaxV = 2048;
 constexpr int kWarpsPerBlock = 4;
-
-__device__ __forceinline__ float2 row_exp2dd(float l, float M, float ch, float cl, bool bf16, const float2* tab) {
-    if (l == -INFINITY) return make_float2(0.0f, 0.0f);  // a masked entry
-    float dh = l - M, dl = 0.0f;
-    if (!bf16) two_sum(l, -M, dh, dl);
-    const float xh = dh * ch;
-    const float xl = fmaf(dl, ch, fmaf(dh, cl, fmaf(dh, ch, -xh)));
-    return exp2dd(xh, xl, tab);
-}
 
 template <bool BF16>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const VerifyArgs a) {
@@ -39,8 +30,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
     const bool greedy = (T == 0.0f);
     const bool t_ok = greedy || (T >= FLT_MIN && T <= FLT_MAX);
     const float c = (greedy || !t_ok) ? 0.0f : kLog2e / T;
-    const double cd = (greedy || !t_ok) ? 0.0 : 1.4426950408889634 / static_cast<double>(T);
-    const float ch = static_cast<float>(cd), cl = static_cast<float>(cd - static_cast<double>(ch));
+    const df c2 = (greedy || !t_ok) ? df_make(0.0f) : log2e_over(T);
     const long long base = static_cast<long long>(b) * (k + 1) * V;
 
     int xi = -1;
@@ -111,8 +101,13 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
                 }
                 if (!err) {
                     const float Lx = load_logit(a.logits, base + lane * V + xi, BF16);
-                    const float2 e = row_exp2dd(Lx, Mi, ch, cl, BF16, tab);
-                    p = (e.x + e.y) / Si;
+                    RowConst rc;
+                    rc.M = Mi;
+                    rc.s1 = Si;
+                    rc.thr = 0.0f;
+                    rc.ch = c2.hi;
+                    rc.cl = c2.lo;
+                    p = df_val(exact_weight<BF16>(Lx, 0.0f, MODE_BONUS, rc, df_make(0.0f), tab)) / Si;
                     const float rho = fminf(1.0f, p / fmaxf(qx, 1e-12f));
                     stop = !(u0 < rho);
                 } else {
@@ -146,66 +141,64 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
     const bool bad = (st & ST_ERRMASK) != 0;
     if (!bad && greedy) token = Aj;
     if (!bad && !greedy) {
-        // pass 2 on row j in float64: weights r = max(0, e - s q) (residual,
-        // s recomputed exactly), or e (bonus, or empty residual)
+        // pass 2 on row j: every entry with exp2dd, sums as float pairs;
+        // weights r = max(0, e - s q) (residual, s recomputed exactly), or e
+        // (bonus, or empty residual)
         const long long row = base + j * V;
         const float* qrow = a.q + (static_cast<long long>(b) * k + (j < k ? j : 0)) * V;
         int mode = (j < k) ? MODE_RESIDUAL : MODE_BONUS;
-        double s_prec = 0.0;
+        RowConst rc;
+        rc.M = Mj;
+        rc.s1 = 0.0f;
+        rc.thr = 0.0f;
+        rc.ch = c2.hi;
+        rc.cl = c2.lo;
+        df s_prec = df_make(0.0f);
         if (mode == MODE_RESIDUAL) {
-            for (long long v = lane; v < V; v += 32) {
-                const float2 e = row_exp2dd(load_logit(a.logits, row + v, BF16), Mj, ch, cl, BF16, tab);
-                s_prec += static_cast<double>(e.x) + static_cast<double>(e.y);
-            }
-            for (int off = 16; off > 0; off >>= 1) s_prec += __shfl_xor_sync(0xffffffffu, s_prec, off);
+            for (long long v = lane; v < V; v += 32)
+                s_prec = df_sum(s_prec, exact_weight<BF16>(load_logit(a.logits, row + v, BF16), 0.0f, MODE_BONUS, rc,
+                                                           df_make(0.0f), tab));
+            s_prec = df_shfl(df_warp_total(s_prec), 0);
         }
-        auto weight = [&](long long v) -> double {
-            const float2 e = row_exp2dd(load_logit(a.logits, row + v, BF16), Mj, ch, cl, BF16, tab);
-            double w = static_cast<double>(e.x) + static_cast<double>(e.y);
-            if (mode == MODE_RESIDUAL) {
-                w -= s_prec * static_cast<double>(__ldg(qrow + v));
-                if (w < 0.0) w = 0.0;
-            }
-            return w;
+        auto weight = [&](long long v) -> df {
+            const float qq = mode == MODE_RESIDUAL ? __ldg(qrow + v) : 0.0f;
+            return exact_weight<BF16>(load_logit(a.logits, row + v, BF16), qq, mode, rc, s_prec, tab);
         };
         bool qbad = false;
-        double W = 0.0;
+        df W = df_make(0.0f);
         for (long long v = lane; v < V; v += 32) {
-            W += weight(v);
+            W = df_sum(W, weight(v));
             if (mode == MODE_RESIDUAL) {
                 const float qq = __ldg(qrow + v);
                 qbad |= !(qq >= 0.0f && qq <= FLT_MAX);
             }
         }
-        for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+        W = df_shfl(df_warp_total(W), 0);
         if (__any_sync(0xffffffffu, qbad)) st |= ST_QBAD;
         if (mode == MODE_RESIDUAL && !(st & ST_ERRMASK)) {
-            if (lane == 0 && a.dbg_resid) a.dbg_resid[b] = static_cast<float>(W / s_prec);
-            if (!(W > 0.0)) {
+            if (lane == 0 && a.dbg_resid) a.dbg_resid[b] = df_val(W) / df_val(s_prec);
+            if (!(W.hi + W.lo > 0.0f)) {
                 mode = MODE_FALLBACK;
                 st |= ST_ZERO_RESIDUAL;
-                W = 0.0;
-                for (long long v = lane; v < V; v += 32) W += weight(v);
-                for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+                W = df_make(0.0f);
+                for (long long v = lane; v < V; v += 32) W = df_sum(W, weight(v));
+                W = df_shfl(df_warp_total(W), 0);
             }
         }
         if (!(st & ST_ERRMASK)) {
-            const double target = static_cast<double>(uj) * W;
-            double acc = 0.0;
+            const df target = df_mul_f(W, uj);
+            df acc = df_make(0.0f);
             int lastpos = -1;
             for (long long v0 = 0; v0 < V && token < 0; v0 += 32) {
                 const long long v = v0 + lane;
-                const double w = v < V ? weight(v) : 0.0;
-                double incl = w;
-                for (int off = 1; off < 32; off <<= 1) {
-                    const double o = __shfl_up_sync(0xffffffffu, incl, off);
-                    if (lane >= off) incl += o;
-                }
-                const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0);
-                if (pos) lastpos = static_cast<int>(v0 + 31 - __clz(pos));
-                const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0 && target < acc + incl);
+                const df w = v < V ? weight(v) : df_make(0.0f);
+                const bool pos = w.hi + w.lo > 0.0f;
+                const df incl = df_sum(acc, df_warp_incl_scan(w, lane));
+                const unsigned posm = __ballot_sync(0xffffffffu, pos);
+                if (posm) lastpos = static_cast<int>(v0 + 31 - __clz(posm));
+                const unsigned hit = __ballot_sync(0xffffffffu, pos && df_less(target, incl));
                 if (hit) token = static_cast<int>(v0 + __ffs(hit) - 1);
-                acc += __shfl_sync(0xffffffffu, incl, 31);
+                acc = df_shfl(incl, 31);
             }
             if (token < 0) token = lastpos;
         }
