@@ -89,7 +89,7 @@ def kernel_source_hash():
 def measured_traffic():
     """DRAM traffic per launch of the verify kernel from the committed ncu
     summary, if it was taken on the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", "ncu_verify_cluster_c3.json")
+    path = os.path.join(ROOT, "profiles", "verify_cluster_kernel_B64_k5_V128256_bf16.json")
     try:
         with open(path) as f:
             d = json.load(f)
