@@ -109,6 +109,8 @@ struct alignas(16) ClusterSmem {
     float wred_hi[kConsumerWarps];
     float wred_lo[kConsumerWarps];
     float2 exp2tab[128];
+    alignas(16) uint32_t lpad[4];  // one masked piece of logits (-inf)
+    alignas(16) float qpad[4];     // and of q (zero)
     int xs[kMaxK + 1];          // draft tokens, for whoever writes the outputs
     int j, status, mode, owner, p2fast, ntiles2, timeout;
     float Mj, sj, thr, c_hi, c_lo, uj;
@@ -169,21 +171,12 @@ struct RowConst {
     float ch, cl;  // log2(e) / T as a float pair
 };
 
-// SFU estimate of e = 2^((l - M) log2(e) / T), the exponent carried as a
-// float pair (xh, xl) and folded back in to first order.
-__device__ __forceinline__ float fast_e(float l, const RowConst& rc) {
-    const float dh = l - rc.M;
-    const float xh = dh * rc.ch;
-    const float xl = fmaf(dh, rc.cl, fmaf(dh, rc.ch, -xh));
-    const float ef = ex2(xh);
-    return fmaf(ef, xl * kLn2, ef);
-}
-
-// e with exp2dd, as a pair (the exact difference l - M for fp32 logits).
+// e with exp2dd, as a pair.  The difference l - M is split exactly (two-sum):
+// a logit close to zero next to a large maximum does not fit one float.
 template <bool BF16>
 __device__ __forceinline__ df precise_e(float l, const RowConst& rc, const float2* tab) {
-    float dh = l - rc.M, dl = 0.0f;
-    if (!BF16) two_sum(l, -rc.M, dh, dl);
+    float dh, dl;
+    two_sum(l, -rc.M, dh, dl);
     const float xh = dh * rc.ch;
     const float xl = fmaf(dl, rc.ch, fmaf(dh, rc.cl, fmaf(dh, rc.ch, -xh)));
     const float2 e = exp2dd(xh, xl, tab);
@@ -210,167 +203,125 @@ __device__ __forceinline__ df exact_weight(float l, float qv, int md, const RowC
     return (r.hi + r.lo > 0.0f) ? r : df_make(0.0f);
 }
 
-// Weight of one large entry with exp2dd: (w, q over a positive residual, e).
-template <bool BF16>
-__device__ __forceinline__ void large_weight(float l, float q, int md, const RowConst& rc, const float2* tab, df& w,
-                                             float& wq, df& e) {
-    e = precise_e<BF16>(l, rc, tab);
-    if (md == MODE_RESIDUAL) {
-        const df r = minus_sq(e, df_make(rc.s1), q);
-        const bool pos = r.hi + r.lo > 0.0f;
-        w = pos ? r : df_make(0.0f);
-        wq = pos ? q : 0.0f;
-    } else {
-        w = e;
-        wq = 0.0f;
-    }
-}
-
-// A lane's 32 consecutive stop-row entries, summed per 8-entry chunk so that
-// the sums can be walked in vocabulary order.  Weights are in e-units (the
-// row's sum of exponentials times p): residual mode r = max(0, e - s1 q),
-// bonus / fallback mode e.  Entries whose SFU estimate exceeds rc.thr are
-// "large": their weight is recomputed with exp2dd.
-struct Lane32 {
-    float s[4];      // weights of the small entries, per chunk (entry order)
-    float sq[4];     // q over positive residuals among them
-    df big[4];       // weights of the large entries, per chunk (entry order)
-    float bq[4];     // q over positive residuals among them
-    df e;            // sum of e over the lane's entries (residual mode)
-    uint32_t large;  // bit 8c+i: entry i of chunk c is large
+// ------------------------------------------------------------------ stop-row sweep
+// Constants of the stop-row sweep, packed for the f32x2 instructions.
+struct SweepConst {
+    f2 MM;      // (M, M): the row maximum
+    f2 CH;      // high part of log2(e) / T
+    f2 NCH;     // its negation
+    f2 CL;      // low part of log2(e) / T
+    f2 LN2;     // ln 2
+    f2 NS1;     // -s1, the pass-1 sum of exponentials
+    float thr;  // entries whose estimate of e exceeds this are "large"
 };
 
-__device__ __forceinline__ void lane32_init(Lane32& L) {
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        L.s[c] = 0.0f;
-        L.sq[c] = 0.0f;
-        L.big[c] = df_make(0.0f);
-        L.bq[c] = 0.0f;
-    }
-    L.e = df_make(0.0f);
-    L.large = 0;
+// SFU estimate of e = 2^((l - M) log2(e) / T) for two entries.  The exponent
+// is a float pair: xh = (l - M) ch rounded, and xl = the product's rounding
+// error plus (l - M) cl, folded back in to first order.  A masked entry
+// (l = -inf) comes out NaN; the sweep gives it weight zero.
+__device__ __forceinline__ f2 fast_e2(f2 L, const SweepConst& K) {
+    const f2 D = sub2(L, K.MM);
+    const f2 N = mul2(D, K.NCH);                    // -xh
+    const f2 XL = fma2(D, K.CL, fma2(D, K.CH, N));  // xl
+    float n0, n1;
+    unpack2(N, n0, n1);
+    const f2 E = pack2(ex2(-n0), ex2(-n1));
+    return fma2(E, mul2(XL, K.LN2), E);
 }
 
-// Small entries of chunk c (c is a run-time value: the chunks are visited in
-// a lane-rotated order to spread shared-memory banks; the sums are stored by
-// chunk).  nvalid: entries of the chunk inside the slice.  Branch-free.
-__device__ __forceinline__ void lane32_fast8(Lane32& L, int c, const float* lv, const float* qv, int nvalid, int md,
-                                             const RowConst& rc) {
-    float s = 0.0f, sq = 0.0f, es = 0.0f;
-    uint32_t bits = 0;
-#pragma unroll
-    for (int i = 0; i < kChunk; ++i) {
-        const float l = lv[i];
-        const bool live = (i < nvalid) && (l != -INFINITY);  // masked entries weigh nothing
-        float ef = fast_e(l, rc);
-        ef = live ? ef : 0.0f;
-        const bool big = ef > rc.thr;
-        bits |= (big ? 1u : 0u) << i;
-        if (md == MODE_RESIDUAL) {
-            const float r = fmaf(-rc.s1, qv[i], ef);
-            const bool take = !big && r > 0.0f;
-            s += take ? r : 0.0f;
-            sq += take ? qv[i] : 0.0f;
-            es += big ? 0.0f : ef;
-        } else {
-            s += big ? 0.0f : ef;
-        }
-    }
-#pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {
-        if (k2 == c) {
-            L.s[k2] = s;
-            L.sq[k2] = sq;
-        }
-    }
-    L.large |= bits << (8 * c);
-    if (md == MODE_RESIDUAL) L.e = df_sum(L.e, df_make(es));
+// (hi, lo) pairs of two sums advanced together: H + L += X, lane by lane.
+__device__ __forceinline__ void df2_add(f2& H, f2& L, f2 X) {
+    const f2 S = add2(H, X);
+    const f2 BB = sub2(S, H);
+    const f2 E = add2(sub2(H, sub2(S, BB)), sub2(X, BB));
+    H = S;
+    L = add2(L, E);
 }
 
-// Add one large entry's result to chunk c of the lane (entry order).
-__device__ __forceinline__ void lane32_add_large(Lane32& L, int c, df w, float wq, df e, int md) {
-#pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {
-        if (k2 == c) {
-            L.big[k2] = df_sum(L.big[k2], w);
-            L.bq[k2] += wq;
-        }
-    }
-    if (md == MODE_RESIDUAL) L.e = df_sum(L.e, e);
+// One lane's sums over its 32 consecutive stop-row entries of a tile.
+// Weights are in e-units (the row's sum of exponentials times p): residual
+// mode r = max(0, e - s1 q), bonus / fallback mode e.  Small entries are
+// summed in floats, eight at a time, and folded into the pairs; large entries
+// (estimate above thr) are left out here and added exactly afterwards.
+struct LaneAcc {
+    f2 wh, wl;       // (weights, sum of e) as (hi, lo) pairs, packed
+    float q;         // q over entries with a positive residual
+    f2 qa;           // every q: a NaN or an infinity surfaces here
+    uint32_t qor;    // OR of the q bit patterns: a set sign bit marks a possible negative
+    uint32_t large;  // bit i: entry i of the lane's 32 is large
+};
+
+__device__ __forceinline__ void lane_init(LaneAcc& A) {
+    A.wh = pack2(0.0f, 0.0f);
+    A.wl = pack2(0.0f, 0.0f);
+    A.q = 0.0f;
+    A.qa = pack2(0.0f, 0.0f);
+    A.qor = 0;
+    A.large = 0;
 }
 
-// Chunk c's weight (pair) and q sum.
-__device__ __forceinline__ df lane32_chunk(const Lane32& L, int c, float& q) {
-    df w = df_make(0.0f);
-    q = 0.0f;
+// The lane's 32 entries in eight pieces of four, visited in the lane-rotated
+// order (p + rot) mod 8 so that the warp's 8- and 16-byte shared loads fall
+// in distinct banks.  ls / qs: this lane's logits and q in shared memory;
+// pieces at or past nvl / 4 read lpad / qpad (a masked logit, q = 0).
+template <bool BF16, bool RESID>
+__device__ __forceinline__ void sweep_lane(LaneAcc& A, const unsigned char* ls, const float* qs, const void* lpad,
+                                           const float* qpad, int rot, int nvl, const SweepConst& K) {
+    f2 sw = pack2(0.0f, 0.0f), se = pack2(0.0f, 0.0f), sq = pack2(0.0f, 0.0f);
 #pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {
-        if (k2 == c) {
-            w = df_sum(df_make(L.s[k2]), L.big[k2]);
-            q = L.sq[k2] + L.bq[k2];
-        }
-    }
-    return w;
-}
-
-// The lane's total weight and q sum, chunks in vocabulary order.
-__device__ __forceinline__ df lane32_total(const Lane32& L, float& q) {
-    df w = df_make(0.0f);
-    q = 0.0f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        w = df_sum(w, df_sum(df_make(L.s[c]), L.big[c]));
-        q += L.sq[c] + L.bq[c];
-    }
-    return w;
-}
-
-// Up to 8 consecutive entries of a logits row / a q row from global memory
-// (vector loads when aligned and complete).
-template <bool BF16>
-__device__ __forceinline__ void load8_logits(const void* logits, long long idx, int cnt, float* lv) {
-    const unsigned char* lp = reinterpret_cast<const unsigned char*>(logits) + idx * (BF16 ? 2 : 4);
-    if (cnt == kChunk && (reinterpret_cast<uintptr_t>(lp) & 15) == 0) {
+    for (int st = 0; st < 8; ++st) {
+        const int p = (st + rot) & 7;
+        const bool valid = 4 * p < nvl;
+        f2 L0, L1;
         if (BF16) {
-            const uint4 w = ld_stream_v4(lp);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                lv[2 * q4] = bf16_lo(ws[q4]);
-                lv[2 * q4 + 1] = bf16_hi(ws[q4]);
-            }
+            const uint2 w = *reinterpret_cast<const uint2*>(valid ? static_cast<const void*>(ls + 8 * p) : lpad);
+            L0 = pack2(bf16_lo(w.x), bf16_hi(w.x));
+            L1 = pack2(bf16_lo(w.y), bf16_hi(w.y));
         } else {
-            const uint4 w0 = ld_stream_v4(lp), w1 = ld_stream_v4(lp + 16);
-            lv[0] = __uint_as_float(w0.x); lv[1] = __uint_as_float(w0.y);
-            lv[2] = __uint_as_float(w0.z); lv[3] = __uint_as_float(w0.w);
-            lv[4] = __uint_as_float(w1.x); lv[5] = __uint_as_float(w1.y);
-            lv[6] = __uint_as_float(w1.z); lv[7] = __uint_as_float(w1.w);
+            const float4 w = *reinterpret_cast<const float4*>(valid ? static_cast<const void*>(ls + 16 * p) : lpad);
+            L0 = pack2(w.x, w.y);
+            L1 = pack2(w.z, w.w);
         }
-    } else {
+        float e[4];
+        unpack2(fast_e2(L0, K), e[0], e[1]);
+        unpack2(fast_e2(L1, K), e[2], e[3]);
+        uint32_t bits = 0;
 #pragma unroll
-        for (int e = 0; e < kChunk; ++e) lv[e] = e < cnt ? load_logit(logits, idx + e, BF16) : -INFINITY;
+        for (int i = 0; i < 4; ++i) {
+            bits |= (e[i] > K.thr ? 1u : 0u) << i;
+            e[i] = (e[i] <= K.thr) ? e[i] : 0.0f;  // large entries and NaN (masked) weigh nothing here
+        }
+        A.large |= bits << (4 * p);
+        const f2 ES0 = pack2(e[0], e[1]), ES1 = pack2(e[2], e[3]);
+        if (RESID) {
+            const float4 qv = *reinterpret_cast<const float4*>(valid ? qs + 4 * p : qpad);
+            const f2 Q0 = pack2(qv.x, qv.y), Q1 = pack2(qv.z, qv.w);
+            float r[4];
+            unpack2(fma2(K.NS1, Q0, ES0), r[0], r[1]);
+            unpack2(fma2(K.NS1, Q1, ES1), r[2], r[3]);
+            sw = add2(sw, pack2(fmaxf(r[0], 0.0f), fmaxf(r[1], 0.0f)));
+            sw = add2(sw, pack2(fmaxf(r[2], 0.0f), fmaxf(r[3], 0.0f)));
+            sq = add2(sq, pack2(r[0] > 0.0f ? qv.x : 0.0f, r[1] > 0.0f ? qv.y : 0.0f));
+            sq = add2(sq, pack2(r[2] > 0.0f ? qv.z : 0.0f, r[3] > 0.0f ? qv.w : 0.0f));
+            se = add2(se, add2(ES0, ES1));
+            A.qa = add2(A.qa, add2(Q0, Q1));
+            A.qor |= __float_as_uint(qv.x) | __float_as_uint(qv.y) | __float_as_uint(qv.z) | __float_as_uint(qv.w);
+        } else {
+            sw = add2(sw, add2(ES0, ES1));
+        }
+        if (st & 1) {
+            // fold the eight entries of the last two pieces into the pairs
+            float a0, a1, b0, b1;
+            unpack2(sw, a0, a1);
+            unpack2(se, b0, b1);
+            df2_add(A.wh, A.wl, pack2(a0 + a1, b0 + b1));
+            sw = pack2(0.0f, 0.0f);
+            se = pack2(0.0f, 0.0f);
+        }
     }
-}
-
-__device__ __forceinline__ void load8_q(const float* qp, int cnt, float* qv) {
-    if (cnt == kChunk && (reinterpret_cast<uintptr_t>(qp) & 15) == 0) {
-        const uint4 w0 = ld_stream_v4(qp), w1 = ld_stream_v4(qp + 4);
-        qv[0] = __uint_as_float(w0.x); qv[1] = __uint_as_float(w0.y);
-        qv[2] = __uint_as_float(w0.z); qv[3] = __uint_as_float(w0.w);
-        qv[4] = __uint_as_float(w1.x); qv[5] = __uint_as_float(w1.y);
-        qv[6] = __uint_as_float(w1.z); qv[7] = __uint_as_float(w1.w);
-    } else {
-#pragma unroll
-        for (int e = 0; e < kChunk; ++e) qv[e] = e < cnt ? __ldg(qp + e) : 0.0f;
-    }
-}
-
-__device__ __forceinline__ bool q_invalid(const float* qv, int cnt) {
-    bool bad = false;
-#pragma unroll
-    for (int e = 0; e < kChunk; ++e) bad |= e < cnt && !(qv[e] >= 0.0f && qv[e] <= FLT_MAX);
-    return bad;
+    float q0, q1;
+    unpack2(sq, q0, q1);
+    A.q += q0 + q1;
 }
 
 // Write a sampled row's outputs: the kept drafts, the drawn token, -1 after.
@@ -435,6 +386,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         sh.nbytes[tid] = ((n - h) * esz) & ~15;
     }
     if (tid < 128) sh.exp2tab[tid] = g_exp2_table[tid];
+    if (tid < 4) {
+        sh.lpad[tid] = BF16 ? 0xff80ff80u : 0xff800000u;
+        sh.qpad[tid] = 0.0f;
+    }
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
@@ -520,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             };
             if (tid == 0)
                 for (int e = 0; e < h; ++e) scalar_elem(e);
+            __syncwarp();  // reconverge before the tile loop's warp-wide steps
 
             for (int lt = 0; lt < ntiles; ++lt, ++t, ++it_cons) {
                 if (t == 2 && warp == 0 && lane < k && !greedy && xi >= 0 && xi < V) {
@@ -656,6 +612,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             }
             if (tid == 0)
                 for (int e = h + interior; e < n; ++e) scalar_elem(e);
+            __syncwarp();  // a diverged warp makes every shuffle below slow
 
             // warp reduction of this position's partial
             if (greedy) {
@@ -718,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             }
             if (greedy && A == 0x7fffffff) A = 0;  // every value is -inf: index 0
         }
+        __syncwarp();
         int err = 0;
         bool stop = false;
         float p = 0.0f;
@@ -754,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 }
             }
         }
+        __syncwarp();
         const unsigned mask = __ballot_sync(0xffffffffu, lane <= k && stop);
         const int j = t_ok ? (__ffs(mask) - 1) : 0;
         int st = t_ok ? __shfl_sync(0xffffffffu, err, j) : ST_TEMP;
@@ -834,17 +793,19 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     const int ntiles2 = sh.ntiles2;
     int mode = sh.mode;
 
-    // one stop-row entry by tile-local index, from the staged tile or from global memory
-    auto fetch1 = [&](bool staged, uint32_t base, int e0, int idx, float& l, float& q) {
-        if (staged) {
-            l = BF16 ? __uint_as_float(static_cast<uint32_t>(ld_shared_u16(base + kP2Elems * 4 + idx * 2)) << 16)
-                     : ld_shared_f32(base + kP2Elems * 4 + idx * 4);
-            q = mode == MODE_RESIDUAL ? ld_shared_f32(base + idx * 4) : 0.0f;
-        } else {
-            l = load_logit(a.logits, lrow + v0 + e0 + idx, BF16);
-            q = mode == MODE_RESIDUAL ? __ldg(qrow + v0 + e0 + idx) : 0.0f;
-        }
+    // one stop-row entry by tile-local index, from global memory (the search)
+    auto fetch1 = [&](int e0, int idx, float& l, float& q) {
+        l = load_logit(a.logits, lrow + v0 + e0 + idx, BF16);
+        q = mode == MODE_RESIDUAL ? __ldg(qrow + v0 + e0 + idx) : 0.0f;
     };
+    SweepConst K;
+    K.MM = pack2(rc.M, rc.M);
+    K.CH = pack2(rc.ch, rc.ch);
+    K.NCH = pack2(-rc.ch, -rc.ch);
+    K.CL = pack2(rc.cl, rc.cl);
+    K.LN2 = pack2(kLn2, kLn2);
+    K.NS1 = pack2(-rc.s1, -rc.s1);
+    K.thr = rc.thr;
 
     for (;;) {
         df te = df_make(0.0f);  // this thread's sum of e (residual mode)
@@ -872,97 +833,97 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         } else {
             // one warp per tile of 1024 entries; lane l owns entries [32l, 32l+32)
             const int it0 = it_cons;
+            const int rot = (lane + (lane >> 3)) & 7;
             for (int t2 = warp; t2 < ntiles2; t2 += kConsumerWarps) {
                 const int it = it0 + t2;
                 const int e0 = t2 * kP2Elems;
                 const int cnt = min(kP2Elems, n - e0);
                 const int my0 = lane * kLaneEntries;
+                unsigned char* stage = ring + (it % kStages) * kTileBytes;
                 bool ok = true;
-                uint32_t base = 0;
                 if (p2fast) {
                     ok = __all_sync(0xffffffffu, !sh.timeout && cons_wait(it));
-                    base = smem_u32(ring + (it % kStages) * kTileBytes);
-                    if (!ok) atomicOr(&sh.timeout, 1);
-                }
-                Lane32 L;
-                lane32_init(L);
-                if (ok) {
-#pragma unroll 2
-                    for (int i = 0; i < 4; ++i) {
-                        const int c = (i + lane) & 3;  // rotated: spreads the lanes over the banks
-                        const int off = my0 + c * kChunk;
-                        const int nv = max(0, min(kChunk, cnt - off));
-                        float lv[kChunk], qv[kChunk];
-#pragma unroll
-                        for (int e = 0; e < kChunk; ++e) {
-                            lv[e] = -INFINITY;
-                            qv[e] = 0.0f;
-                        }
-                        if (nv > 0) {
-                            if (p2fast) {
-                                if (BF16) {
-                                    const uint4 w = ld_shared_v4(base + kP2Elems * 4 + off * 2);
-                                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                                    for (int q4 = 0; q4 < 4; ++q4) {
-                                        lv[2 * q4] = bf16_lo(ws[q4]);
-                                        lv[2 * q4 + 1] = bf16_hi(ws[q4]);
-                                    }
-                                } else {
-                                    const uint4 w0 = ld_shared_v4(base + kP2Elems * 4 + off * 4);
-                                    const uint4 w1 = ld_shared_v4(base + kP2Elems * 4 + off * 4 + 16);
-                                    lv[0] = __uint_as_float(w0.x); lv[1] = __uint_as_float(w0.y);
-                                    lv[2] = __uint_as_float(w0.z); lv[3] = __uint_as_float(w0.w);
-                                    lv[4] = __uint_as_float(w1.x); lv[5] = __uint_as_float(w1.y);
-                                    lv[6] = __uint_as_float(w1.z); lv[7] = __uint_as_float(w1.w);
-                                }
-                                if (mode == MODE_RESIDUAL) {
-                                    const uint4 w0 = ld_shared_v4(base + off * 4);
-                                    const uint4 w1 = ld_shared_v4(base + off * 4 + 16);
-                                    qv[0] = __uint_as_float(w0.x); qv[1] = __uint_as_float(w0.y);
-                                    qv[2] = __uint_as_float(w0.z); qv[3] = __uint_as_float(w0.w);
-                                    qv[4] = __uint_as_float(w1.x); qv[5] = __uint_as_float(w1.y);
-                                    qv[6] = __uint_as_float(w1.z); qv[7] = __uint_as_float(w1.w);
-                                }
-                            } else {
-                                // unaligned rows: the same tiles, read straight from global memory
-                                load8_logits<BF16>(a.logits, lrow + v0 + e0 + off, nv, lv);
-                                if (mode == MODE_RESIDUAL) load8_q(qrow + v0 + e0 + off, nv, qv);
-                            }
-                        }
-                        if (mode == MODE_RESIDUAL) qbad |= q_invalid(qv, nv);
-                        lane32_fast8(L, c, lv, qv, nv, mode, rc);
+                    if (!ok && lane == 0) atomicOr(&sh.timeout, 1);
+                } else {
+                    // unaligned rows: the warp stages its own tile with plain loads
+                    // (slot it % kStages is this warp's alone, its tiles being
+                    // t2 = warp mod 4); entries past the slice are masked
+                    for (int idx = lane; idx < kP2Elems; idx += 32) {
+                        const bool in = idx < cnt;
+                        const long long g = lrow + v0 + e0 + idx;
+                        if (BF16)
+                            reinterpret_cast<uint16_t*>(stage + kP2Elems * 4)[idx] =
+                                in ? __ldg(reinterpret_cast<const unsigned short*>(a.logits) + g) : uint16_t(0xff80u);
+                        else
+                            reinterpret_cast<float*>(stage + kP2Elems * 4)[idx] =
+                                in ? __ldg(reinterpret_cast<const float*>(a.logits) + g) : -INFINITY;
+                        if (mode == MODE_RESIDUAL)
+                            reinterpret_cast<float*>(stage)[idx] = in ? __ldg(qrow + v0 + e0 + idx) : 0.0f;
                     }
+                }
+                __syncwarp();
+                LaneAcc A;
+                lane_init(A);
+                df bw = df_make(0.0f), be = df_make(0.0f);  // large entries: weights, e
+                if (ok) {
+                    const unsigned char* ls = stage + kP2Elems * 4 + my0 * esz;
+                    const float* qs = reinterpret_cast<const float*>(stage) + my0;
+                    const int nvl = p2fast ? max(0, min(kLaneEntries, cnt - my0)) : kLaneEntries;
+                    if (mode == MODE_RESIDUAL)
+                        sweep_lane<BF16, true>(A, ls, qs, sh.lpad, sh.qpad, rot, nvl, K);
+                    else
+                        sweep_lane<BF16, false>(A, ls, qs, sh.lpad, sh.qpad, rot, nvl, K);
                     // large entries, each lane its own in entry order (the warp
                     // runs as many rounds as its busiest lane has entries)
-                    for (uint32_t m = L.large; m; m &= m - 1) {
+                    for (uint32_t m = A.large; m; m &= m - 1) {
                         const int bit = __ffs(m) - 1;
-                        float l, q;
-                        fetch1(p2fast, base, e0, my0 + bit, l, q);
-                        df w, e;
-                        float wq;
-                        large_weight<BF16>(l, q, mode, rc, sh.exp2tab, w, wq, e);
-                        lane32_add_large(L, bit >> 3, w, wq, e, mode);
+                        const float l = BF16 ? bf16_lo(reinterpret_cast<const uint16_t*>(ls)[bit])
+                                             : reinterpret_cast<const float*>(ls)[bit];
+                        const df e = precise_e<BF16>(l, rc, sh.exp2tab);
+                        if (mode == MODE_RESIDUAL) {
+                            const float q = qs[bit];
+                            const df r = minus_sq(e, df_make(rc.s1), q);
+                            const bool pos = r.hi + r.lo > 0.0f;
+                            bw = df_sum(bw, pos ? r : df_make(0.0f));
+                            A.q += pos ? q : 0.0f;
+                            be = df_sum(be, e);
+                        } else {
+                            bw = df_sum(bw, e);
+                        }
                     }
-                    if (p2fast) {
+                    __syncwarp();
+                    if (mode == MODE_RESIDUAL) {
+                        // a NaN or infinite sum, or a set sign bit (-0 is a
+                        // valid q), sends the lane through an exact check
+                        float qa0, qa1;
+                        unpack2(A.qa, qa0, qa1);
+                        if ((A.qor & 0x80000000u) || !(fabsf(qa0 + qa1) <= FLT_MAX)) {
+                            for (int i = 0; i < nvl; ++i) {
+                                const float q = qs[i];
+                                qbad |= !(q >= 0.0f && q <= FLT_MAX);
+                            }
+                        }
                         __syncwarp();
-                        if (lane == 0) mbar_arrive_cnt(smem_u32(&sh.empty[it % kStages]), kConsumerWarps);
                     }
+                    if (p2fast && lane == 0) mbar_arrive_cnt(smem_u32(&sh.empty[it % kStages]), kConsumerWarps);
                 }
-                float lq;
-                const df lw = lane32_total(L, lq);
+                float wh, eh, wlo, elo;
+                unpack2(A.wh, wh, eh);
+                unpack2(A.wl, wlo, elo);
+                const df lw = df_sum(df{wh, wlo}, bw);
                 sh.lane_hi[t2][lane] = lw.hi;
                 sh.lane_lo[t2][lane] = lw.lo;
-                sh.lane_q[t2][lane] = lq;
-                te = df_sum(te, L.e);
+                sh.lane_q[t2][lane] = A.q;
+                te = df_sum(te, df_sum(df{eh, elo}, be));
                 const df tw = df_warp_total(lw);
-                float tq = lq;
+                float tq = A.q;
                 for (int off = 16; off > 0; off >>= 1) tq += __shfl_down_sync(0xffffffffu, tq, off);
                 if (lane == 0) {
                     sh.tile_hi[t2] = tw.hi;
                     sh.tile_lo[t2] = tw.lo;
                     sh.tile_q[t2] = tq;
                 }
+                __syncwarp();
             }
             it_cons = it0 + ntiles2;
         }
@@ -1004,6 +965,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 qr = sh.alltot[lane][4];
                 fl = static_cast<int>(__float_as_uint(sh.alltot[lane][5]));
             }
+            __syncwarp();  // a diverged warp makes every shuffle below slow
             const df s_prec = df_shfl(df_warp_total(er), 0);
             const bool any_q = __any_sync(0xffffffffu, (fl & 1) != 0);
             const bool any_to = __any_sync(0xffffffffu, (fl & 2) != 0);
@@ -1100,8 +1062,9 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             const int cnt = min(kP2Elems, n - e0);
             const int idx = who * kLaneEntries + lane;
             float l = -INFINITY, q = 0.0f;
-            if (idx < cnt) fetch1(false, 0, e0, idx, l, q);
+            if (idx < cnt) fetch1(e0, idx, l, q);
             const df we = exact_weight<BF16>(l, q, mode, rc, s_prec, sh.exp2tab);
+            __syncwarp();
             const bool p = we.hi + we.lo > 0.0f;
             const df ci = df_sum(df_shfl(le, who), df_warp_incl_scan(we, lane));
             const unsigned ehit = __ballot_sync(0xffffffffu, p && df_less(t, ci));

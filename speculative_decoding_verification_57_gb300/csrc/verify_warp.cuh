@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
             nanf = nan_seen ? 1 : 0;
         }
     }
+    __syncwarp();
     // accept tests, one lane per position
     int err = 0;
     bool stop = false;
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
             }
         }
     }
+    __syncwarp();
     const unsigned mask = __ballot_sync(0xffffffffu, lane <= k && stop);
     const int j = t_ok ? __ffs(mask) - 1 : 0;
     int st = t_ok ? __shfl_sync(0xffffffffu, err, j) : ST_TEMP;
