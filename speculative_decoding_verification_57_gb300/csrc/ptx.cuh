@@ -132,6 +132,9 @@ __device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_
     asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
+// Named barrier 1 over the first 128 threads of the CTA (the consumer warps).
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // ------------------------------------------------------------------ loads
 __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;

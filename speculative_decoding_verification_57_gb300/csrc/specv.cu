@@ -60,7 +60,6 @@ struct DeviceGuard {
     }
 };
 
-constexpr size_t kClusterDynSmem = static_cast<size_t>(kStages) * kTileBytes;
 
 struct Plan {
     bool warp = false;
@@ -102,7 +101,7 @@ cudaError_t launch_cluster(const VerifyArgs& a, const Plan& p, cudaStream_t stre
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.B) * p.cluster, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kClusterDynSmem;
+    cfg.dynamicSmemBytes = cluster_dyn_smem(p.cluster, a.pk);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -122,12 +121,12 @@ cudaError_t launch_warp(const VerifyArgs& a, cudaStream_t stream) {
 }
 
 template <bool BF16>
-void query_clusters(int* out) {
+void query_clusters(int* out, int pk) {
     for (int c = 1; c <= 16; ++c) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(c) * 256, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kClusterDynSmem;
+        cfg.dynamicSmemBytes = cluster_dyn_smem(c, pk);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = c;
@@ -149,7 +148,7 @@ cudaError_t set_attributes() {
     cudaError_t e = cudaFuncSetAttribute(verify_cluster_kernel<BF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(verify_cluster_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kClusterDynSmem));
+                                static_cast<int>(cluster_dyn_smem(16, kMaxK + 1)));
 }
 
 specv_status check_sizes(const specv_ctx* h, specv_dtype dt, int batch, int k, int64_t V) {
@@ -168,6 +167,7 @@ specv_status run(specv_ctx* h, specv_dtype dt, const VerifyArgs& a, void* stream
     const Plan p = make_plan(h, dt, a.B, a.V);
     VerifyArgs args = a;
     args.slice = p.slice;
+    args.pk = h->max_k + 1;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (p.warp)
@@ -219,8 +219,8 @@ specv_status specv_create(specv_handle* out, int device, int max_batch, int max_
     h->max_batch = max_batch;
     h->max_k = max_k;
     h->vocab = vocab;
-    query_clusters<false>(h->max_clusters[0]);
-    query_clusters<true>(h->max_clusters[1]);
+    query_clusters<false>(h->max_clusters[0], max_k + 1);
+    query_clusters<true>(h->max_clusters[1], max_k + 1);
     *out = h;
     return SPECV_OK;
 }

@@ -40,7 +40,9 @@ constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;  // + one producer warp
 constexpr int kTileBytes = 8192;
-constexpr int kStages = 4;
+constexpr int kStages = 5;         // pass-1 ring: stages of kTileBytes
+constexpr int kRingBytes = kStages * kTileBytes;
+constexpr int kStages2 = 8;        // pass-2 ring: at most this many slots of one tile each
 constexpr int kMaxK = 31;          // positions 0..k fit one warp
 constexpr int kMaxSlice = 16384;   // elements of one position held by one CTA
 constexpr int kChunk = 8;          // pass-2 entries per chunk
@@ -82,6 +84,7 @@ struct VerifyArgs {
     int B;
     int k;
     int slice;               // elements per CTA, a multiple of 64
+    int pk;                  // positions per partial array in shared memory (>= k + 1)
 };
 
 struct Partial {
@@ -91,14 +94,21 @@ struct Partial {
     int flags;  // bit 0: a NaN was seen (greedy); bit 1: a wait timed out
 };
 
+// Dynamic shared memory: the ring (kRingBytes), then the per-warp partials
+// [kConsumerWarps][pk], then every cluster CTA's partials [C][pk] (pushed by
+// each CTA of the cluster).
+inline size_t cluster_dyn_smem(int C, int pk) {
+    return static_cast<size_t>(kRingBytes) + static_cast<size_t>(kConsumerWarps + C) * pk * sizeof(Partial);
+}
+
 struct alignas(16) ClusterSmem {
-    Partial wpart[kConsumerWarps][kMaxK + 1];
-    alignas(16) Partial allpart[16][kMaxK + 1];  // every CTA's partials, pushed by each CTA of the cluster
     int tstart[kMaxK + 2];      // first pass-1 tile of each position
     int head[kMaxK + 1];        // unaligned leading elements of each position's slice
     int nbytes[kMaxK + 1];      // bytes of the 16-byte aligned interior
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
+    unsigned long long full2[kStages2];
+    unsigned long long empty2[kStages2];
     float tile_hi[kMaxP2Tiles];  // pass-2 weights per tile of 1024 entries (pair), and q sums
     float tile_lo[kMaxP2Tiles];
     float tile_q[kMaxP2Tiles];
@@ -112,12 +122,12 @@ struct alignas(16) ClusterSmem {
     alignas(16) uint32_t lpad[4];  // one masked piece of logits (-inf)
     alignas(16) float qpad[4];     // and of q (zero)
     int xs[kMaxK + 1];          // draft tokens, for whoever writes the outputs
-    int j, status, mode, owner, p2fast, ntiles2, timeout;
+    int j, status, mode, owner, p2fast, ntiles2, timeout, stride2, nslots2, loff2;
     float Mj, sj, thr, c_hi, c_lo, uj;
     float delta, sp_hi, sp_lo, t_hi, t_lo;
 };
 static_assert(sizeof(Partial) == 16, "Partial is pushed with one 16-byte store");
-static_assert(offsetof(ClusterSmem, allpart) % 16 == 0, "16-byte remote stores need 16-byte aligned targets");
+static_assert(kRingBytes % 16 == 0 && sizeof(Partial) % 16 == 0, "partials follow the ring 16-byte aligned");
 static_assert(offsetof(ClusterSmem, alltot) % 16 == 0, "16-byte remote stores need 16-byte aligned targets");
 static_assert(alignof(ClusterSmem) >= 16, "ClusterSmem must be 16-byte aligned");
 
@@ -358,6 +368,9 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     const int n = static_cast<int>(max(0LL, min(static_cast<long long>(a.slice), V - v0)));
     const unsigned char* lg = reinterpret_cast<const unsigned char*>(a.logits);
     unsigned char* ring = dyn_smem;
+    const int pk = a.pk;
+    Partial* wpart = reinterpret_cast<Partial*>(dyn_smem + kRingBytes);  // [kConsumerWarps][pk]
+    Partial* allpart = wpart + kConsumerWarps * pk;                       // [C][pk]
 
     // ---------------------------------------------------------------- row setup
     const float T = a.temp ? __ldg(a.temp + b) : 0.0f;
@@ -394,6 +407,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
             mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
+        }
+        for (int s = 0; s < kStages2; ++s) {
+            mbar_init(smem_u32(&sh.full2[s]), 1);
+            mbar_init(smem_u32(&sh.empty2[s]), 1);
         }
         sh.timeout = 0;
         fence_mbar_init();
@@ -629,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                     merge_ms(m, s, m2, s2, c);
                 }
             }
-            if (lane == 0) sh.wpart[warp][i] = Partial{m, s, arg, nan_seen ? 1 : 0};
+            if (lane == 0) wpart[warp * pk + i] = Partial{m, s, arg, nan_seen ? 1 : 0};
         }
         // rows too short to reach the third tile load the scalars here
         if (t_ok && total1 <= 2 && warp == 0 && lane < k && !greedy && xi >= 0 && xi < V) {
@@ -641,9 +658,9 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     __syncthreads();
     const bool timed_out = sh.timeout != 0;
     if (tid <= k && t_ok) {
-        Partial p = sh.wpart[0][tid];
+        Partial p = wpart[tid];
         for (int w = 1; w < kConsumerWarps; ++w) {
-            const Partial o = sh.wpart[w][tid];
+            const Partial o = wpart[w * pk + tid];
             if (greedy) {
                 merge_arg(p.m, p.arg, o.m, o.arg);
                 p.flags |= o.flags;
@@ -653,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         }
         if (timed_out) p.flags |= 2;
         // push this CTA's partial of position tid into every CTA of the cluster
-        const uint32_t local = smem_u32(&sh.allpart[rank][tid]);
+        const uint32_t local = smem_u32(&allpart[rank * pk + tid]);
         for (uint32_t r = 0; r < C; ++r)
             st_cluster_v4(map_rank(local, r), __float_as_uint(p.m), __float_as_uint(p.s), static_cast<uint32_t>(p.arg),
                           static_cast<uint32_t>(p.flags));
@@ -666,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         int A = 0x7fffffff, flags = 0;
         if (lane <= k && t_ok) {
             for (uint32_t r = 0; r < C; ++r) {
-                const Partial pr = sh.allpart[r][lane];
+                const Partial pr = allpart[r * pk + lane];
                 flags |= pr.flags;
                 if (greedy)
                     merge_arg(M, A, pr.m, pr.arg);
@@ -781,6 +798,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         const bool qa = (reinterpret_cast<uintptr_t>(qrow + v0) & 15) == 0;
         sh.p2fast = la && (j == k || qa) && (n % kChunk) == 0;
         sh.ntiles2 = (n + kP2Elems - 1) / kP2Elems;
+        // pass-2 slots: [q (residual rows)][logits], one tile each
+        sh.loff2 = (j < k) ? kP2Elems * 4 : 0;
+        sh.stride2 = sh.loff2 + kP2Elems * esz;
+        sh.nslots2 = min(kStages2, kRingBytes / sh.stride2);  // at least 5: the consumers step 4 tiles at a time
     }
     __syncthreads();
     RowConst rc;
@@ -791,6 +812,8 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     rc.cl = sh.c_lo;
     const bool p2fast = sh.p2fast != 0;
     const int ntiles2 = sh.ntiles2;
+    const int loff2 = sh.loff2, stride2 = sh.stride2, S2 = sh.nslots2;
+    int g2 = 0;  // pass-2 tiles issued / consumed so far (both sweeps): tile g uses slot g % S2
     int mode = sh.mode;
 
     // one stop-row entry by tile-local index, from global memory (the search)
@@ -812,51 +835,66 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         bool qbad = false;
         if (producer) {
             if (p2fast && lane == 0) {
-                for (int t2 = 0; t2 < ntiles2; ++t2, ++it_prod) {
-                    if (sh.timeout || !prod_acquire(it_prod)) {
+                // the ring's last generic-proxy reads (pass 1) are ordered
+                // before these async-proxy writes by the block barrier above
+                fence_proxy_async_smem();
+                int slot = g2 % S2, phase = (g2 / S2) & 1;  // tile g: slot g % S2, phase (g / S2) & 1
+                for (int t2 = 0; t2 < ntiles2; ++t2) {
+                    const int g = g2 + t2;
+                    if (sh.timeout ||
+                        (g >= S2 && !mbar_wait_bounded(smem_u32(&sh.empty2[slot]), phase ^ 1, kWaitPolls))) {
                         atomicOr(&sh.timeout, 1);
                         break;
                     }
                     const int e0 = t2 * kP2Elems;
                     const int cnt = min(kP2Elems, n - e0);
-                    const int slot = it_prod % kStages;
-                    const uint32_t bar = smem_u32(&sh.full[slot]);
-                    const uint32_t dst = smem_u32(ring + slot * kTileBytes);
+                    const uint32_t bar = smem_u32(&sh.full2[slot]);
+                    const uint32_t dst = smem_u32(ring + slot * stride2);
                     const uint32_t lbytes = static_cast<uint32_t>(cnt * esz);
                     const uint32_t qbytes = mode == MODE_RESIDUAL ? static_cast<uint32_t>(cnt * 4) : 0u;
                     mbar_arrive_expect_tx(bar, lbytes + qbytes);
-                    bulk_g2s(dst + kP2Elems * 4, lg + (lrow + v0 + e0) * esz, lbytes, bar);
+                    bulk_g2s(dst + loff2, lg + (lrow + v0 + e0) * esz, lbytes, bar);
                     if (qbytes) bulk_g2s(dst, qrow + v0 + e0, qbytes, bar);
+                    if (++slot == S2) {
+                        slot = 0;
+                        phase ^= 1;
+                    }
                 }
             }
-            it_prod = __shfl_sync(0xffffffffu, it_prod, 0);
+            __syncwarp();
         } else {
             // one warp per tile of 1024 entries; lane l owns entries [32l, 32l+32)
-            const int it0 = it_cons;
             const int rot = (lane + (lane >> 3)) & 7;
+            int slot = (g2 + warp) % S2, phase = ((g2 + warp) / S2) & 1;  // advanced by 4 tiles a step (S2 > 4)
             for (int t2 = warp; t2 < ntiles2; t2 += kConsumerWarps) {
-                const int it = it0 + t2;
                 const int e0 = t2 * kP2Elems;
                 const int cnt = min(kP2Elems, n - e0);
                 const int my0 = lane * kLaneEntries;
-                unsigned char* stage = ring + (it % kStages) * kTileBytes;
+                unsigned char* stage = ring + (p2fast ? slot : warp) * stride2;
+                const int my_slot = slot;
+                slot += kConsumerWarps;
+                const int my_phase = phase;
+                if (slot >= S2) {
+                    slot -= S2;
+                    phase ^= 1;
+                }
                 bool ok = true;
                 if (p2fast) {
-                    ok = __all_sync(0xffffffffu, !sh.timeout && cons_wait(it));
+                    ok = __all_sync(0xffffffffu, !sh.timeout &&
+                                                     mbar_wait_bounded(smem_u32(&sh.full2[my_slot]), my_phase, kWaitPolls));
                     if (!ok && lane == 0) atomicOr(&sh.timeout, 1);
                 } else {
-                    // unaligned rows: the warp stages its own tile with plain loads
-                    // (slot it % kStages is this warp's alone, its tiles being
-                    // t2 = warp mod 4); entries past the slice are masked
+                    // unaligned rows: the warp stages its own tiles in slot
+                    // `warp` with plain loads; entries past the slice are masked
                     for (int idx = lane; idx < kP2Elems; idx += 32) {
                         const bool in = idx < cnt;
-                        const long long g = lrow + v0 + e0 + idx;
+                        const long long gi = lrow + v0 + e0 + idx;
                         if (BF16)
-                            reinterpret_cast<uint16_t*>(stage + kP2Elems * 4)[idx] =
-                                in ? __ldg(reinterpret_cast<const unsigned short*>(a.logits) + g) : uint16_t(0xff80u);
+                            reinterpret_cast<uint16_t*>(stage + loff2)[idx] =
+                                in ? __ldg(reinterpret_cast<const unsigned short*>(a.logits) + gi) : uint16_t(0xff80u);
                         else
-                            reinterpret_cast<float*>(stage + kP2Elems * 4)[idx] =
-                                in ? __ldg(reinterpret_cast<const float*>(a.logits) + g) : -INFINITY;
+                            reinterpret_cast<float*>(stage + loff2)[idx] =
+                                in ? __ldg(reinterpret_cast<const float*>(a.logits) + gi) : -INFINITY;
                         if (mode == MODE_RESIDUAL)
                             reinterpret_cast<float*>(stage)[idx] = in ? __ldg(qrow + v0 + e0 + idx) : 0.0f;
                     }
@@ -866,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 lane_init(A);
                 df bw = df_make(0.0f), be = df_make(0.0f);  // large entries: weights, e
                 if (ok) {
-                    const unsigned char* ls = stage + kP2Elems * 4 + my0 * esz;
+                    const unsigned char* ls = stage + loff2 + my0 * esz;
                     const float* qs = reinterpret_cast<const float*>(stage) + my0;
                     const int nvl = p2fast ? max(0, min(kLaneEntries, cnt - my0)) : kLaneEntries;
                     if (mode == MODE_RESIDUAL)
@@ -905,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                         }
                         __syncwarp();
                     }
-                    if (p2fast && lane == 0) mbar_arrive_cnt(smem_u32(&sh.empty[it % kStages]), kConsumerWarps);
+                    if (p2fast && lane == 0) mbar_arrive(smem_u32(&sh.empty2[my_slot]));
                 }
                 float wh, eh, wlo, elo;
                 unpack2(A.wh, wh, eh);
@@ -925,7 +963,6 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 }
                 __syncwarp();
             }
-            it_cons = it0 + ntiles2;
         }
         // CTA totals: weights, e (residual mode), q over positive residuals
         const df tw = df_warp_total(te);
@@ -1013,6 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         __syncthreads();
         if (sh.mode == MODE_FALLBACK && mode == MODE_RESIDUAL) {
             mode = MODE_FALLBACK;
+            g2 += ntiles2;
             cluster_sync();  // peers are done reading this CTA's totals
             continue;
         }
