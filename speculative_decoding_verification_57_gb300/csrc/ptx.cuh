@@ -51,13 +51,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
     return ok != 0;
 }
 
-// Bounded wait on an mbarrier phase: gives up after `limit` polls (each
-// poll may itself suspend the thread for a short, hardware-chosen time) and
-// returns false, so that a lost completion ends the kernel with an error
-// status instead of a hang.
+// Nanoseconds of the global timer.
+__device__ __forceinline__ unsigned long long gtimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// No wait in these kernels takes more than this (a correct call runs for
+// microseconds); past it a wait gives up and the row reports a timeout.
+constexpr unsigned long long kWaitNs = 200ull * 1000 * 1000;
+
+// Bounded wait on an mbarrier phase: gives up after `limit` polls or kWaitNs
+// of wall-clock time, whichever comes first (each poll may itself suspend the
+// thread for about a microsecond), and returns false, so that a lost
+// completion ends the kernel with an error status instead of a hang.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t phase, uint32_t limit) {
-    for (uint32_t it = 0; it < limit; ++it)
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0; it < limit; ++it) {
         if (mbar_try_wait(bar, phase)) return true;
+        if ((it & 255) == 255) {
+            const unsigned long long t = gtimer();
+            if (t0 == 0)
+                t0 = t;
+            else if (t - t0 > kWaitNs)
+                return false;
+        }
+    }
     return false;
 }
 
