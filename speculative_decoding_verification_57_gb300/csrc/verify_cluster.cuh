@@ -389,21 +389,27 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             u1 = __ldg(a.u + ub + 1);
         }
     }
-    if (tid <= k) {
-        // geometry of this CTA's slice of position tid
-        const long long e0 = (static_cast<long long>(b) * (k + 1) + tid) * V + v0;
-        const uintptr_t addr = reinterpret_cast<uintptr_t>(lg + e0 * esz);
-        int h = static_cast<int>(((16 - (addr & 15)) & 15) / esz);
-        if (h > n) h = n;
-        sh.head[tid] = h;
-        sh.nbytes[tid] = ((n - h) * esz) & ~15;
-    }
     if (tid < 128) sh.exp2tab[tid] = g_exp2_table[tid];
     if (tid < 4) {
         sh.lpad[tid] = BF16 ? 0xff80ff80u : 0xff800000u;
         sh.qpad[tid] = 0.0f;
     }
-    if (tid == 0) {
+    // One pass-1 tile: tile tt of the CTA's slices, position by position.
+    auto issue_p1 = [&](int tt, int it) {
+        int i = 0;
+        while (sh.tstart[i + 1] <= tt) ++i;
+        const int off = (tt - sh.tstart[i]) * kTileBytes;
+        const int bytes = min(kTileBytes, sh.nbytes[i] - off);
+        const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + v0 + sh.head[i];
+        const int slot = it % kStages;
+        const uint32_t bar = smem_u32(&sh.full[slot]);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(bytes));
+        bulk_g2s(smem_u32(ring + slot * kTileBytes), lg + e0 * esz + off, static_cast<uint32_t>(bytes), bar);
+    };
+    int it_prod = 0, it_cons = 0;
+    if (producer && lane == 0) {
+        // the producer sets up the ring and the slice geometry, and starts the
+        // first copies before the block's first barrier
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
             mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
@@ -415,15 +421,21 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         sh.timeout = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
-    }
-    __syncthreads();
-    if (tid == 0) {
         int acc = 0;
         for (int i = 0; i <= k; ++i) {
+            const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + v0;
+            const uintptr_t addr = reinterpret_cast<uintptr_t>(lg + e0 * esz);
+            int h = static_cast<int>(((16 - (addr & 15)) & 15) / esz);
+            if (h > n) h = n;
+            const int nb = ((n - h) * esz) & ~15;
+            sh.head[i] = h;
+            sh.nbytes[i] = nb;
             sh.tstart[i] = acc;
-            acc += (sh.nbytes[i] + kTileBytes - 1) / kTileBytes;
+            acc += (nb + kTileBytes - 1) / kTileBytes;
         }
         sh.tstart[k + 1] = acc;
+        if (t_ok)
+            for (; it_prod < min(kStages, acc); ++it_prod) issue_p1(it_prod, it_prod);
     }
     __syncthreads();
     const int total1 = t_ok ? sh.tstart[k + 1] : 0;
@@ -445,25 +457,16 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&sh.empty[it % kStages]));
     };
-    int it_prod = 0, it_cons = 0;
 
     // ---------------------------------------------------------------- pass 1
     if (producer) {
         if (lane == 0) {
-            for (int tt = 0; tt < total1; ++tt, ++it_prod) {
+            for (int tt = it_prod; tt < total1; ++tt, ++it_prod) {
                 if (sh.timeout || !prod_acquire(it_prod)) {
                     atomicOr(&sh.timeout, 1);
                     break;
                 }
-                int i = 0;
-                while (sh.tstart[i + 1] <= tt) ++i;
-                const int off = (tt - sh.tstart[i]) * kTileBytes;
-                const int bytes = min(kTileBytes, sh.nbytes[i] - off);
-                const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + v0 + sh.head[i];
-                const int slot = it_prod % kStages;
-                const uint32_t bar = smem_u32(&sh.full[slot]);
-                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(bytes));
-                bulk_g2s(smem_u32(ring + slot * kTileBytes), lg + e0 * esz + off, static_cast<uint32_t>(bytes), bar);
+                issue_p1(tt, it_prod);
             }
         }
         it_prod = __shfl_sync(0xffffffffu, it_prod, 0);
