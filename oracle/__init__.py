@@ -86,8 +86,9 @@ def verify(logits, q, x, u, T, *, debug=False, boundary_eps=1e-6, nthreads=1, li
     """Run the oracle over a batch.
 
     logits [B,k+1,V] float32 or uint16 (bf16 bits); q [B,k,V] float32 or
-    None; x [B,k] int32; u [B,k+1,2] float32 or None; T [B] float32 or None
-    (None: every row greedy).  Returns a dict of numpy arrays:
+    None (one-hot drafts: q is the point mass at each draft token); x [B,k]
+    int32; u [B,k+1,2] float32 or None; T [B] float32 or None (None: every
+    row greedy).  Returns a dict of numpy arrays:
     num_accepted, out_tokens, row_status, boundary (0 or 1 + 2*i + slot of
     the uniform found within ``boundary_eps`` of a decision edge) and, with
     ``debug``, p_at_draft, q_at_draft, row_max, row_sumexp, residual_mass.

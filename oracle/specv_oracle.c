@@ -150,6 +150,23 @@ int specv_oracle_residual(const double *p, const float *q, int64_t V, double *r_
     return st;
 }
 
+/* The residual for a one-hot draft, q = the point mass at the draft token x
+ * ([C] "One guess (lookup)": keep x with probability p(x), otherwise sample
+ * from p with x removed; "N-gram and prompt lookup": q is one-hot).  It is
+ * the same definition r(v) = max(0, p(v) - q(v)) with q(x) = 1 and q(v) = 0
+ * elsewhere: r(v) = p(v) for v != x and r(x) = max(0, p(x) - 1) = 0.        */
+int specv_oracle_residual_onehot(const double *p, int64_t V, int64_t x, double *r_out, double *S_out) {
+    double S = 0.0;
+    for (int64_t v = 0; v < V; ++v) {
+        double r = p[v] - (v == x ? 1.0 : 0.0);
+        if (r < 0.0) r = 0.0;
+        r_out[v] = r;
+        S += r;
+    }
+    *S_out = S;
+    return 0;
+}
+
 /* Inverse-CDF sampling over non-negative weights w[0..V): lay the weights
  * end to end in vocabulary order and take the slot that u * W lands in
  * ([C] "First: what an output distribution is", sampling; [D] sample()).
@@ -253,7 +270,7 @@ static void fill_debug(const job_t *J, int64_t b, int greedy, double T) {
         double p = 0.0, q = 0.0;
         if (!greedy && x >= 0 && x < J->V) {
             p = exp((logit_at(J->dtype, row, x) - M) / T) / s;
-            q = (double)J->q[(b * k + i) * J->V + x];
+            q = J->q ? (double)J->q[(b * k + i) * J->V + x] : 1.0; /* one-hot draft: q(x) = 1 */
         }
         if (J->p_at_draft) J->p_at_draft[b * k + i] = p;
         if (J->q_at_draft) J->q_at_draft[b * k + i] = q;
@@ -303,7 +320,7 @@ static void verify_sampled_row(const job_t *J, int64_t b, double T, double *buf_
         st |= specv_oracle_softmax_stats(J->dtype, row_ptr(J, b, i), V, T, &M, &s, NULL);
         double q = 0.0;
         if (x >= 0 && x < V) {
-            q = (double)J->q[(b * k + i) * V + x];
+            q = J->q ? (double)J->q[(b * k + i) * V + x] : 1.0; /* one-hot draft: q(x) = 1 */
             if (!(q >= 0.0 && q <= (double)FLT_MAX)) st |= ST_Q_INVALID;
         }
         if (st) {
@@ -341,7 +358,8 @@ static void verify_sampled_row(const job_t *J, int64_t b, double T, double *buf_
     } else {
         for (int64_t v = 0; v < V; ++v) buf_p[v] = buf_w[v] / s;
         double S;
-        int qst = specv_oracle_residual(buf_p, J->q + (b * k + j) * V, V, buf_w, &S);
+        int qst = J->q ? specv_oracle_residual(buf_p, J->q + (b * k + j) * V, V, buf_w, &S)
+                       : specv_oracle_residual_onehot(buf_p, V, (int64_t)J->x[b * k + j], buf_w, &S);
         if (qst) {
             finish_error(J, b, qst);
             return;
@@ -409,7 +427,7 @@ int specv_oracle_verify(int dtype, const void *logits, const float *q, const int
                         double boundary_eps, int nthreads) {
     if (B < 0 || k < 1 || V < 1 || (dtype != 0 && dtype != 1)) return -1;
     if (!logits || !x || !num_accepted || !out_tokens || !row_status) return -1;
-    if (T && (!q || !u)) return -1;
+    if (T && !u) return -1; /* q may be NULL: one-hot drafts */
     job_t J = {dtype, logits, q, x, u, T, B, k, V, num_accepted, out_tokens, row_status,
                p_at_draft, q_at_draft, row_max, row_sumexp, residual_mass, boundary, boundary_eps};
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);

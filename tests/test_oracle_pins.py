@@ -285,6 +285,46 @@ def test_one_hot_draft():
     assert np.all(r["out_tokens"][r["num_accepted"] == 0, 0] != x0)
 
 
+def test_one_hot_draft_without_q():
+    """q = None means one-hot drafts ("Speculative decoding." lesson, "N-gram
+    and prompt lookup": q is one-hot, so acceptance is just p(x)).  It must
+    equal the explicit one-hot q in every output, and on one draft token it
+    keeps x with probability p(x), otherwise samples p with x removed."""
+    rng = np.random.default_rng(17)
+    V, B = 10, 60_000
+    p = random_simplex(rng, V)
+    x0 = int(np.argsort(p)[-2])  # not the mode: the residual keeps the mode
+    q = np.zeros(V)
+    q[x0] = 1.0
+    w = W.make_from_distributions(p, q, B=B, k=1, seed=18)
+    assert np.all(w.x == x0)
+    r_null = oracle.verify(w.logits, None, w.x, w.u, w.T, debug=True, nthreads=8)
+    r_hot = oracle.verify(w.logits, w.q, w.x, w.u, w.T, debug=True, nthreads=8)
+    for key in r_hot:
+        np.testing.assert_array_equal(r_null[key], r_hot[key], err_msg=key)
+    keep = (r_null["num_accepted"] == 1).mean()
+    assert abs(keep - p[x0]) < 4 * math.sqrt(p[x0] * (1 - p[x0]) / B)
+    fix = r_null["out_tokens"][r_null["num_accepted"] == 0, 0]
+    assert np.all(fix != x0)
+    expect = p.copy()
+    expect[x0] = 0.0
+    expect /= expect.sum()
+    freq = np.bincount(fix, minlength=V) / len(fix)
+    assert 0.5 * np.abs(freq - expect).sum() < 0.01
+    # residual mass 1 - p(x) on the rejected rows
+    rej = r_null["num_accepted"] == 0
+    np.testing.assert_allclose(r_null["residual_mass"][rej], 1.0 - p[x0], rtol=1e-6)
+    # many draft tokens and positions: still identical to the explicit form
+    w2 = W.make_random(name="onehot", B=64, k=4, V=300, dtype="bf16", seed=19, logit_sigma=2.0, draft_sigma=1.0,
+                       temperature=0.9)
+    hot = np.zeros_like(w2.q)
+    np.put_along_axis(hot, w2.x[:, :, None], 1.0, axis=2)
+    a = oracle.verify(w2.logits, None, w2.x, w2.u, w2.T, debug=True)
+    b = oracle.verify(w2.logits, hot, w2.x, w2.u, w2.T, debug=True)
+    for key in a:
+        np.testing.assert_array_equal(a[key], b[key], err_msg=key)
+
+
 def test_greedy_rows_match_textbook_argmax():
     rng = np.random.default_rng(9)
     B, k, V = 400, 4, 37
