@@ -42,6 +42,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--graph-calls", type=int, default=100)
+    p.add_argument("--variant", choices=["sample", "onehot"], default="sample",
+                   help="onehot: the same workload verified as one-hot drafts (q = None)")
     return p.parse_args(argv)
 
 
@@ -64,18 +66,20 @@ def reduce_max(value, world_size, device=None):
     return float(t.item())
 
 
-def algorithmic_bytes(w, num_accepted, row_status):
+def algorithmic_bytes(w, num_accepted, row_status, onehot=False):
     """Bytes the verify step must move for one call: every logit once, the
     draft-probability row at each rejected sampled position, the gathered
     q(x), x and accept uniforms, the draw uniform and temperature, and the
-    outputs (num_accepted, out_tokens, row_status)."""
+    outputs (num_accepted, out_tokens, row_status).  One-hot drafts read no
+    q at all."""
     import numpy as np
 
     B, k, V = w.B, w.k, w.V
     esz = 2 if w.dtype == "bf16" else 4
     ok = (row_status & 0x2F) == 0
     rejected = ok & (w.T != 0) & (num_accepted < k)
-    return (B * (k + 1) * V * esz + int(rejected.sum()) * V * 4 + B * k * 12 + B * 12 + B * (k + 2) * 4)
+    qrow = 0 if onehot else int(rejected.sum()) * V * 4
+    return (B * (k + 1) * V * esz + qrow + B * k * (8 if onehot else 12) + B * 12 + B * (k + 2) * 4)
 
 
 def kernel_source_hash():
@@ -174,7 +178,7 @@ def time_oracle(w, budget_s, max_rows=None):
 
     rows = w.B if max_rows is None else min(w.B, max_rows)
     sl = slice(0, rows)
-    args = (w.logits[sl], w.q[sl], w.x[sl], w.u[sl], w.T[sl])
+    args = (w.logits[sl], None if w.q is None else w.q[sl], w.x[sl], w.u[sl], w.T[sl])
     cores = host_cores()
     oracle.verify(*args, nthreads=cores)  # warm (page in)
     n, t0 = 0, time.perf_counter()
@@ -244,12 +248,15 @@ def run_ours(args):
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
     w = W.make_config(CONFIG_INDEX, seed=57000 + CONFIG_INDEX + 1000 * rank)
+    onehot = args.variant == "onehot"
+    if onehot:
+        w = W.Workload(w.name, w.dtype, w.logits, None, w.x, w.u, w.T)
     B, k, V = w.B, w.k, w.V
     h = sv.specv_create(local, max_batch=B, max_k=k, vocab=V)
     L0 = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16)
     sets = []
     for s in range(N_SETS):
-        sets.append(dict(L=L0.to(dev), q=torch.from_numpy(w.q).to(dev), x=torch.from_numpy(w.x).to(dev),
+        sets.append(dict(L=L0.to(dev), q=None if onehot else torch.from_numpy(w.q).to(dev), x=torch.from_numpy(w.x).to(dev),
                          u=torch.from_numpy(w.u).to(dev), T=torch.from_numpy(w.T).to(dev)))
     outs = [dict(num_accepted=torch.empty(B, dtype=torch.int32, device=dev),
                  out_tokens=torch.empty((B, k + 1), dtype=torch.int32, device=dev),
@@ -267,7 +274,7 @@ def run_ours(args):
     got = {kk: v.cpu().numpy() for kk, v in outs[0].items()}
     if np.any(got["row_status"] & sv.ST_ERROR_MASK):
         raise RuntimeError("verify reported data errors on the benchmark inputs")
-    alg = algorithmic_bytes(w, got["num_accepted"], got["row_status"])
+    alg = algorithmic_bytes(w, got["num_accepted"], got["row_status"], onehot)
 
     # capture G calls (cycling through the sets) into a CUDA graph
     G = max(1, min(args.graph_calls, args.steps))
@@ -339,7 +346,7 @@ def run_ours(args):
     value = B * args.steps * ws / (ms_max / 1e3)
 
     # end to end through the host-buffer entry point (pinned memory in/out)
-    pin = dict(L=L0.pin_memory(), q=torch.from_numpy(w.q).pin_memory(), x=torch.from_numpy(w.x).pin_memory(),
+    pin = dict(L=L0.pin_memory(), q=None if onehot else torch.from_numpy(w.q).pin_memory(), x=torch.from_numpy(w.x).pin_memory(),
                u=torch.from_numpy(w.u).pin_memory(), T=torch.from_numpy(w.T).pin_memory())
     host_out = dict(num_accepted=torch.empty(B, dtype=torch.int32).pin_memory(),
                     out_tokens=torch.empty((B, k + 1), dtype=torch.int32).pin_memory(),
@@ -352,7 +359,7 @@ def run_ours(args):
     for _ in range(args.e2e_steps):
         sv.specv_verify_sample_host(h, pin["L"], pin["q"], pin["x"], pin["u"], pin["T"], out=host_out, stream=stream)
     e2e_s = reduce_max(time.perf_counter() - t0, ws, dev)
-    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     assert np.array_equal(host_out["num_accepted"].numpy(), got["num_accepted"])
 
@@ -380,9 +387,11 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": WORKLOAD, "B": B, "k": k, "V": V, "logits": "bf16", "T": 1.0,
+            "workload": WORKLOAD + (", one-hot drafts (q = None)" if onehot else ""), "B": B, "k": k, "V": V,
+            "logits": "bf16", "T": 1.0,
             "global_batch": B * ws, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-            "l2": f"rotating {N_SETS} input sets ({N_SETS * (w.logits.nbytes + w.q.nbytes) / 1e9:.2f} GB) > 2x L2",
+            "l2": f"rotating {N_SETS} input sets "
+                  f"({N_SETS * (w.logits.nbytes + (0 if onehot else w.q.nbytes)) / 1e9:.2f} GB) > 2x L2",
             "launch": f"{launch_mode}, {specv_cluster_desc(sv, h, B, k, V)}",
         },
         "logits_per_s": B * (k + 1) * V * args.steps * ws / (ms_max / 1e3),

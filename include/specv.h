@@ -34,7 +34,14 @@
  * Layouts (all row-major, contiguous, device memory unless stated):
  *   target_logits [B, k+1, V]  bf16 (SPECV_BF16) or fp32 (SPECV_F32)
  *   draft_probs   [B, k, V]    fp32, the distribution the drafts were drawn
- *                              from, used as given (never re-tempered)
+ *                              from, used as given (never re-tempered); or
+ *                              NULL for one-hot drafts (prompt lookup, n-gram
+ *                              or greedy drafting: q is the point mass at the
+ *                              draft token, so a draft is kept with
+ *                              probability p(x) and a rejection samples p with
+ *                              x removed -- "Speculative decoding." lesson,
+ *                              "One guess (lookup)", "N-gram and prompt
+ *                              lookup"; no page gives a separate call for it)
  *   draft_tokens  [B, k]       int32
  *   uniforms      [B, k+1, 2]  fp32 in [0,1); [b,i,0] drives the accept test
  *                              at i < k, [b,j,1] the residual/bonus draw at
@@ -96,11 +103,12 @@ typedef enum { SPECV_F32 = 0, SPECV_BF16 = 1 } specv_dtype;
  * rows row_sumexp, p_at_draft, q_at_draft and residual_mass are 0. */
 typedef struct {
     float *p_at_draft;    /* [B, k]   p_i(x_i) (0 if x_i is out of range) */
-    float *q_at_draft;    /* [B, k]   q_i(x_i) as read (0 if out of range) */
+    float *q_at_draft;    /* [B, k]   q_i(x_i) as read, 1 for one-hot drafts (0 if out of range) */
     float *row_max;       /* [B, k+1] max_v logits[b,i,v] */
     float *row_sumexp;    /* [B, k+1] sum_v exp((logits[b,i,v] - row_max) / T) */
     float *residual_mass; /* [B]      sum_v max(0, p_j(v) - q_j(v)) at a rejected
-                                      position, else 0 */
+                                      position (1 - p_j(x_j) for one-hot drafts),
+                                      else 0 */
 } specv_debug;
 
 /* Create a handle on CUDA device `device` for batches up to max_batch rows,

@@ -117,7 +117,8 @@ def _stream_ptr(stream):
 
 def specv_verify_sample(h: Handle, logits, q, x, u, T, *, debug=False, out=None, stream=None):
     """Verify a batch (asynchronous on ``stream``, default: torch's current
-    stream).  logits [B,k+1,V] bf16/fp32, q [B,k,V] fp32, x [B,k] int32,
+    stream).  logits [B,k+1,V] bf16/fp32, q [B,k,V] fp32 or None (one-hot
+    drafts: q is the point mass at each draft token), x [B,k] int32,
     u [B,k+1,2] fp32, T [B] fp32 (0 = greedy row), all CUDA tensors.
     Returns a dict of CUDA tensors: num_accepted [B], out_tokens [B,k+1],
     row_status [B] and, with ``debug``, p_at_draft, q_at_draft, row_max,
@@ -127,7 +128,7 @@ def specv_verify_sample(h: Handle, logits, q, x, u, T, *, debug=False, out=None,
     k = k1 - 1
     dt = _logits_dtype(logits)
     _dev(logits, logits.dtype, "logits")
-    pq = _dev(q, torch.float32, "q", (B, k, V))
+    pq = None if q is None else _dev(q, torch.float32, "q", (B, k, V))
     px = _dev(x, torch.int32, "x", (B, k))
     pu = _dev(u, torch.float32, "u", (B, k + 1, 2))
     pt = _dev(T, torch.float32, "T", (B,))
@@ -189,6 +190,8 @@ def specv_verify_sample_host(h: Handle, logits, q, x, u, T, *, out=None, stream=
     k = k1 - 1
     dt = _logits_dtype(logits)
     for t, name in ((logits, "logits"), (q, "q"), (x, "x"), (u, "u"), (T, "T")):
+        if t is None and name == "q":
+            continue  # one-hot drafts
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CPU tensor")
     if out is None:
@@ -199,7 +202,7 @@ def specv_verify_sample_host(h: Handle, logits, q, x, u, T, *, out=None, stream=
             "row_status": torch.empty(B, dtype=torch.int32, pin_memory=pin),
         }
     st = _lib.load().specv_verify_sample_host(
-        h.ptr, dt, ctypes.c_void_p(logits.data_ptr()), ctypes.c_void_p(q.data_ptr()),
+        h.ptr, dt, ctypes.c_void_p(logits.data_ptr()), ctypes.c_void_p(None if q is None else q.data_ptr()),
         ctypes.c_void_p(x.data_ptr()), ctypes.c_void_p(u.data_ptr()), ctypes.c_void_p(T.data_ptr()), B, k, V,
         ctypes.c_void_p(out["num_accepted"].data_ptr()), ctypes.c_void_p(out["out_tokens"].data_ptr()),
         ctypes.c_void_p(out["row_status"].data_ptr()), _stream_ptr(stream))

@@ -231,7 +231,7 @@ specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const
                                  int32_t* out_tokens, int32_t* row_status, const specv_debug* dbg, void* stream) {
     specv_status st = check_sizes(h, logits_dtype, batch, k, V);
     if (st != SPECV_OK) return st;
-    if (batch > 0 && (!target_logits || !draft_probs || !draft_tokens || !uniforms || !temperature ||
+    if (batch > 0 && (!target_logits || !draft_tokens || !uniforms || !temperature ||
                       !num_accepted || !out_tokens))
         return SPECV_ERR_INVALID_ARGUMENT;
     VerifyArgs a = {};
@@ -283,15 +283,15 @@ specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, 
     specv_status st = check_sizes(h, logits_dtype, batch, k, V);
     if (st != SPECV_OK) return st;
     if (batch == 0) return SPECV_OK;
-    if (!target_logits || !draft_probs || !draft_tokens || !uniforms || !temperature || !num_accepted ||
-        !out_tokens)
+    if (!target_logits || !draft_tokens || !uniforms || !temperature || !num_accepted || !out_tokens)
         return SPECV_ERR_INVALID_ARGUMENT;
     const size_t esz = logits_dtype == SPECV_BF16 ? 2 : 4;
     const size_t B = static_cast<size_t>(batch), K = static_cast<size_t>(k), VV = static_cast<size_t>(V);
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t nL = B * (K + 1) * VV * esz, nQ = B * K * VV * 4, nX = B * K * 4, nU = B * (K + 1) * 2 * 4,
                  nT = B * 4, nA = B * 4, nO = B * (K + 1) * 4, nS = B * 4;
-    const size_t need = al(nL) + al(nQ) + al(nX) + al(nU) + al(nT) + al(nA) + al(nO) + al(nS);
+    const size_t nQc = draft_probs ? nQ : 0;  // one-hot drafts: no q to copy
+    const size_t need = al(nL) + al(nQc) + al(nX) + al(nU) + al(nT) + al(nA) + al(nO) + al(nS);
     DeviceGuard g(h->device);
     if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
     if (h->stage_bytes < need) {
@@ -304,7 +304,7 @@ specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, 
     unsigned char* p = static_cast<unsigned char*>(h->stage);
     unsigned char* dL = p;
     unsigned char* dQ = dL + al(nL);
-    unsigned char* dX = dQ + al(nQ);
+    unsigned char* dX = dQ + al(nQc);
     unsigned char* dU = dX + al(nX);
     unsigned char* dT = dU + al(nU);
     unsigned char* dA = dT + al(nT);
@@ -312,11 +312,11 @@ specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, 
     unsigned char* dS = dO + al(nO);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     SPECV_CUDA(cudaMemcpyAsync(dL, target_logits, nL, cudaMemcpyHostToDevice, s));
-    SPECV_CUDA(cudaMemcpyAsync(dQ, draft_probs, nQ, cudaMemcpyHostToDevice, s));
+    if (nQc) SPECV_CUDA(cudaMemcpyAsync(dQ, draft_probs, nQc, cudaMemcpyHostToDevice, s));
     SPECV_CUDA(cudaMemcpyAsync(dX, draft_tokens, nX, cudaMemcpyHostToDevice, s));
     SPECV_CUDA(cudaMemcpyAsync(dU, uniforms, nU, cudaMemcpyHostToDevice, s));
     SPECV_CUDA(cudaMemcpyAsync(dT, temperature, nT, cudaMemcpyHostToDevice, s));
-    st = specv_verify_sample(h, logits_dtype, dL, reinterpret_cast<const float*>(dQ),
+    st = specv_verify_sample(h, logits_dtype, dL, draft_probs ? reinterpret_cast<const float*>(dQ) : nullptr,
                              reinterpret_cast<const int32_t*>(dX), reinterpret_cast<const float*>(dU),
                              reinterpret_cast<const float*>(dT), batch, k, V, reinterpret_cast<int32_t*>(dA),
                              reinterpret_cast<int32_t*>(dO), reinterpret_cast<int32_t*>(dS), nullptr, stream);

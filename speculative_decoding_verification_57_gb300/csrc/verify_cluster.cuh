@@ -64,11 +64,13 @@ enum : int {
     ST_ERRMASK = 1 | 2 | 4 | 8 | 32 | 64,
 };
 
-enum : int { MODE_RESIDUAL = 0, MODE_BONUS = 1, MODE_FALLBACK = 2 };
+// Stop-row weights: residual max(0, e - s q); bonus e; fallback e (zero
+// residual mass); one-hot e except at the draft token (q = point mass there).
+enum : int { MODE_RESIDUAL = 0, MODE_BONUS = 1, MODE_FALLBACK = 2, MODE_ONEHOT = 3 };
 
 struct VerifyArgs {
     const void* logits;      // [B, k+1, V] bf16 or fp32
-    const float* q;          // [B, k, V] (nullable when every row is greedy)
+    const float* q;          // [B, k, V]; null: one-hot drafts (and for all-greedy calls)
     const int32_t* x;        // [B, k]
     const float* u;          // [B, k+1, 2] (nullable when every row is greedy)
     const float* temp;       // [B] (nullable: every row greedy)
@@ -502,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                     // the accept test's scalars; x_i has long arrived
                     const long long row = static_cast<long long>(b) * (k + 1) + lane;
                     Lx = load_logit(a.logits, row * V + xi, BF16);
-                    qx = __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi);
+                    qx = a.q ? __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi) : 1.0f;
                 }
                 const bool ok = !sh.timeout && cons_wait(it_cons);
                 const int bytes = min(kTileBytes, sh.nbytes[i] - lt * kTileBytes);
@@ -655,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         if (t_ok && total1 <= 2 && warp == 0 && lane < k && !greedy && xi >= 0 && xi < V) {
             const long long row = static_cast<long long>(b) * (k + 1) + lane;
             Lx = load_logit(a.logits, row * V + xi, BF16);
-            qx = __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi);
+            qx = a.q ? __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi) : 1.0f;
         }
     }
     __syncthreads();
@@ -750,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             sh.status = st;
             sh.Mj = Mj;
             sh.sj = Sj;
-            sh.mode = (j < k) ? MODE_RESIDUAL : MODE_BONUS;
+            sh.mode = (j < k) ? (a.q ? MODE_RESIDUAL : MODE_ONEHOT) : MODE_BONUS;
         }
         if (lane <= k) sh.xs[lane] = xi;
         // rank 0 writes debug values and, for greedy or failed rows, the outputs
@@ -789,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     // ---------------------------------------------------------------- pass 2
     const int j = sh.j;
     const long long lrow = (static_cast<long long>(b) * (k + 1) + j) * V;
-    const float* qrow = a.q + (static_cast<long long>(b) * k + (j < k ? j : 0)) * V;
+    const float* qrow = a.q ? a.q + (static_cast<long long>(b) * k + (j < k ? j : 0)) * V : nullptr;
     if (tid == 0) {
         const df c2 = log2e_over(T);
         sh.c_hi = c2.hi;
@@ -798,11 +800,11 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         // bulk copies need 16-byte aligned starts and sizes: both rows
         // aligned at the slice start, and whole groups of 8 entries
         const bool la = (reinterpret_cast<uintptr_t>(lg + (lrow + v0) * esz) & 15) == 0;
-        const bool qa = (reinterpret_cast<uintptr_t>(qrow + v0) & 15) == 0;
-        sh.p2fast = la && (j == k || qa) && (n % kChunk) == 0;
+        const bool qa = qrow && (reinterpret_cast<uintptr_t>(qrow + v0) & 15) == 0;
+        sh.p2fast = la && (sh.mode != MODE_RESIDUAL || qa) && (n % kChunk) == 0;
         sh.ntiles2 = (n + kP2Elems - 1) / kP2Elems;
         // pass-2 slots: [q (residual rows)][logits], one tile each
-        sh.loff2 = (j < k) ? kP2Elems * 4 : 0;
+        sh.loff2 = (sh.mode == MODE_RESIDUAL) ? kP2Elems * 4 : 0;
         sh.stride2 = sh.loff2 + kP2Elems * esz;
         sh.nslots2 = min(kStages2, kRingBytes / sh.stride2);  // at least 5: the consumers step 4 tiles at a time
     }
@@ -822,6 +824,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     // one stop-row entry by tile-local index, from global memory (the search)
     auto fetch1 = [&](int e0, int idx, float& l, float& q) {
         l = load_logit(a.logits, lrow + v0 + e0 + idx, BF16);
+        if (mode == MODE_ONEHOT && v0 + e0 + idx == sh.xs[j]) l = -INFINITY;  // the draft token: q = 1
         q = mode == MODE_RESIDUAL ? __ldg(qrow + v0 + e0 + idx) : 0.0f;
     };
     SweepConst K;
@@ -900,6 +903,17 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                                 in ? __ldg(reinterpret_cast<const float*>(a.logits) + gi) : -INFINITY;
                         if (mode == MODE_RESIDUAL)
                             reinterpret_cast<float*>(stage)[idx] = in ? __ldg(qrow + v0 + e0 + idx) : 0.0f;
+                    }
+                }
+                if (mode == MODE_ONEHOT && ok && lane == 0) {
+                    // one-hot drafts: the draft token's entry weighs nothing (q = 1 there)
+                    const long long rel = static_cast<long long>(sh.xs[j]) - v0 - e0;  // j < k here
+                    if (rel >= 0 && rel < cnt) {
+                        if (BF16)
+                            reinterpret_cast<uint16_t*>(stage + loff2)[rel] = uint16_t(0xff80u);
+                        else
+                            reinterpret_cast<float*>(stage + loff2)[rel] = -INFINITY;
+                        fence_proxy_async_smem();  // before the slot's next bulk copy
                     }
                 }
                 __syncwarp();
@@ -1024,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                     a.num_accepted[b] = 0;
                     if (a.row_status) a.row_status[b] = sh.status | bad;
                 }
-            } else if (mode == MODE_RESIDUAL && !(Wt.hi + Wt.lo > 0.0f)) {
+            } else if ((mode == MODE_RESIDUAL || mode == MODE_ONEHOT) && !(Wt.hi + Wt.lo > 0.0f)) {
                 if (lane == 0) {
                     sh.mode = MODE_FALLBACK;
                     sh.owner = -1;
@@ -1047,6 +1061,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                     sh.sp_hi = s_prec.hi;
                     sh.sp_lo = s_prec.lo;
                     if (rank == 0 && a.dbg_resid && mode == MODE_RESIDUAL) a.dbg_resid[b] = df_val(Wt) / df_val(s_prec);
+                    if (rank == 0 && a.dbg_resid && mode == MODE_ONEHOT) a.dbg_resid[b] = df_val(Wt) / rc.s1;
                 }
             }
         }

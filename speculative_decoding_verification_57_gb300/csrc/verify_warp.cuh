@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
                 if (xi < 0 || xi >= V) err |= ST_TOKEN;
                 if (!(u0 >= 0.0f && u0 < 1.0f)) err |= ST_UNIFORM;
                 if (xi >= 0 && xi < V) {
-                    qx = __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi);
+                    qx = a.q ? __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi) : 1.0f;
                     if (!(qx >= 0.0f && qx <= FLT_MAX)) err |= ST_QBAD;
                 }
                 if (!err) {
@@ -147,8 +147,9 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
         // weights r = max(0, e - s q) (residual, s recomputed exactly), or e
         // (bonus, or empty residual)
         const long long row = base + j * V;
-        const float* qrow = a.q + (static_cast<long long>(b) * k + (j < k ? j : 0)) * V;
-        int mode = (j < k) ? MODE_RESIDUAL : MODE_BONUS;
+        const float* qrow = a.q ? a.q + (static_cast<long long>(b) * k + (j < k ? j : 0)) * V : nullptr;
+        int mode = (j < k) ? (a.q ? MODE_RESIDUAL : MODE_ONEHOT) : MODE_BONUS;
+        const int xj = __shfl_sync(0xffffffffu, xi, j < k ? j : 0);  // one-hot drafts: left out of the residual
         RowConst rc;
         rc.M = Mj;
         rc.s1 = 0.0f;
@@ -164,7 +165,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
         }
         auto weight = [&](long long v) -> df {
             const float qq = mode == MODE_RESIDUAL ? __ldg(qrow + v) : 0.0f;
-            return exact_weight<BF16>(load_logit(a.logits, row + v, BF16), qq, mode, rc, s_prec, tab);
+            const float l = (mode == MODE_ONEHOT && v == xj) ? -INFINITY : load_logit(a.logits, row + v, BF16);
+            return exact_weight<BF16>(l, qq, mode, rc, s_prec, tab);
         };
         bool qbad = false;
         df W = df_make(0.0f);
@@ -177,8 +179,10 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
         }
         W = df_shfl(df_warp_total(W), 0);
         if (__any_sync(0xffffffffu, qbad)) st |= ST_QBAD;
-        if (mode == MODE_RESIDUAL && !(st & ST_ERRMASK)) {
-            if (lane == 0 && a.dbg_resid) a.dbg_resid[b] = df_val(W) / df_val(s_prec);
+        if ((mode == MODE_RESIDUAL || mode == MODE_ONEHOT) && !(st & ST_ERRMASK)) {
+            const float Sj = __shfl_sync(0xffffffffu, Si, j);
+            if (lane == 0 && a.dbg_resid)
+                a.dbg_resid[b] = df_val(W) / (mode == MODE_RESIDUAL ? df_val(s_prec) : Sj);
             if (!(W.hi + W.lo > 0.0f)) {
                 mode = MODE_FALLBACK;
                 st |= ST_ZERO_RESIDUAL;

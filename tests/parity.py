@@ -21,8 +21,8 @@ def to_device(w, dev):
         L = torch.from_numpy(w.logits.view(np.int16)).to(dev).view(torch.bfloat16)
     else:
         L = torch.from_numpy(w.logits).to(dev)
-    return (L, torch.from_numpy(w.q).to(dev), torch.from_numpy(w.x).to(dev), torch.from_numpy(w.u).to(dev),
-            torch.from_numpy(w.T).to(dev))
+    q = None if w.q is None else torch.from_numpy(w.q).to(dev)  # None: one-hot drafts
+    return (L, q, torch.from_numpy(w.x).to(dev), torch.from_numpy(w.u).to(dev), torch.from_numpy(w.T).to(dev))
 
 
 def run_gpu(h, w, dev="cuda:0", debug=False):
@@ -58,7 +58,7 @@ def compare(w, got, ref=None, *, check_debug=False):
         idx = int(ref["boundary"][b]) - 1
         i, slot = idx // 2, idx % 2
         alts = set()
-        sub = (w.logits[b:b + 1], w.q[b:b + 1], w.x[b:b + 1], w.T[b:b + 1])
+        sub = (w.logits[b:b + 1], None if w.q is None else w.q[b:b + 1], w.x[b:b + 1], w.T[b:b + 1])
         for d in NUDGES:
             for sgn in (-1.0, 1.0):
                 uu = w.u[b:b + 1].copy()

@@ -252,6 +252,31 @@ def test_bench_workload_many_uniforms(h):
     assert mism <= 1e-4 * rows + 0.5
 
 
+@pytest.mark.parametrize("V,k,B,dtype", [(128256, 5, 64, "bf16"), (32000, 4, 8, "bf16"), (40003, 3, 6, "f32"),
+                                        (1500, 4, 16, "f32"), (700, 6, 9, "bf16")])
+def test_one_hot_drafts(h, V, k, B, dtype):
+    """q = None: one-hot drafts (prompt lookup, greedy drafting).  Accept
+    with p(x); a rejection samples p with x removed ("Speculative decoding."
+    lesson, "One guess (lookup)", "N-gram and prompt lookup")."""
+    w = W.make_random(name="onehot", B=B, k=k, V=V, dtype=dtype, seed=V + k, logit_sigma=2.5, draft_sigma=0.5,
+                      temperature=0.9, spike=5.0, spike_mode="position", greedy_rows=1)
+    w = W.Workload(w.name, w.dtype, w.logits, None, w.x, w.u, w.T)
+    got = run_gpu(h, w, debug=True)
+    st = _acc(compare(w, got, check_debug=True))
+    assert (got["row_status"] == 0).any()
+    print("one-hot", V, st)
+
+
+def test_one_hot_many_uniforms(h):
+    """The benchmark logits with one-hot drafts over 20 uniform sets."""
+    base = W.make_config(3)
+    rng = np.random.default_rng(5)
+    for r in range(20):
+        w = W.Workload(base.name, base.dtype, base.logits, None, base.x,
+                       rng.random(base.u.shape, dtype=np.float32), base.T)
+        _acc(compare(w, run_gpu(h, w)))
+
+
 def test_zz_summary():
     """Disagreements at flagged boundaries over every parity case above."""
     print("parity totals", TOTALS)

@@ -79,7 +79,7 @@ MUTANTS = {
         "            token = specv_oracle_inverse_cdf(buf_p, V, (double)u1, &lo, &hi);\n        } else {",
     ),
     # residual without the max(0, .)
-    "no_clamp": ("        if (r < 0.0) r = 0.0;\n", ""),
+    "no_clamp": ("        double r = p[v] - qv;\n        if (r < 0.0) r = 0.0;\n", "        double r = p[v] - qv;\n"),
     # acceptance ratio upside down
     "ratio_inverted": ("double rho = p / (q > 1e-12 ? q : 1e-12);", "double rho = q / (p > 1e-12 ? p : 1e-12);"),
     # accept test at position i reads the target row of position i+1
@@ -94,8 +94,8 @@ MUTANTS = {
     ),
     # residual built from the draft row of the next position
     "residual_next_q": (
-        "J->q + (b * k + j) * V, V, buf_w, &S);",
-        "J->q + (b * k + (j + 1) % k) * V, V, buf_w, &S);",
+        "specv_oracle_residual(buf_p, J->q + (b * k + j) * V, V, buf_w, &S)",
+        "specv_oracle_residual(buf_p, J->q + (b * k + (j + 1) % k) * V, V, buf_w, &S)",
     ),
     # inverse CDF compares u with the unnormalised running sum
     "unnormalised_cdf": ("    double target = u * W;\n", "    double target = u;\n"),
