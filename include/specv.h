@@ -144,6 +144,34 @@ specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, 
                                       int k, int64_t V, int32_t *num_accepted, int32_t *out_tokens,
                                       int32_t *row_status, void *stream);
 
+/* Paged KV-cache bookkeeping after a verification ("LLM Inference &
+ * Speculative Decoding: From Roofline Physics to Lossless Acceleration", s.6,
+ * PagedKVCacheManager.rollback_to), all pointers device memory:
+ *   num_accepted [B]               int32, as returned by a verify call
+ *   seq_lens     [B]               int32 in/out: positions held in the cache,
+ *                                  the last k of them the drafts; becomes
+ *                                  seq_len - (k - num_accepted)
+ *   block_tables [B, max_blocks]   int32 in/out: physical block of each
+ *                                  logical block; popped entries become -1
+ *   num_blocks   [B]               int32 in/out: blocks in use; becomes
+ *                                  ceil(new seq_len / block_size)
+ *   free_list    [free_capacity]   int32: freed blocks are appended
+ *   free_count   [1]               int32 in/out: entries used in free_list
+ *   row_status   [B]               int32 out (nullable): 0; 128 if the row's
+ *                                  num_accepted is outside [0, k], its new
+ *                                  length would be negative or num_blocks is
+ *                                  outside [0, max_blocks] (the row is left
+ *                                  as it is); 256 on every row if the free
+ *                                  list has no room for all freed blocks
+ *                                  (then nothing changes)
+ * The result equals rolling the rows back one at a time in batch order,
+ * each row's blocks popped last-first.  Asynchronous on `stream`; argument
+ * errors are returned before launch. */
+specv_status specv_rollback(specv_handle h, const int32_t *num_accepted, int batch, int k, int32_t *seq_lens,
+                            int32_t *block_tables, int max_blocks, int32_t *num_blocks, int block_size,
+                            int32_t *free_list, int64_t free_capacity, int32_t *free_count, int32_t *row_status,
+                            void *stream);
+
 /* Number of CTAs per sequence (thread-block cluster size, 1..16) that the
  * next call with these sizes would use; 0 if the sizes are invalid. */
 int specv_plan_cluster(specv_handle h, specv_dtype logits_dtype, int batch, int k, int64_t V);

@@ -53,6 +53,9 @@ def _declare(lib):
     lib.specv_oracle_residual.argtypes = [vp, vp, ctypes.c_int64, vp, dp]
     lib.specv_oracle_inverse_cdf.restype = ctypes.c_int64
     lib.specv_oracle_inverse_cdf.argtypes = [vp, ctypes.c_int64, ctypes.c_double, dp, dp]
+    lib.specv_oracle_rollback.restype = ctypes.c_int
+    lib.specv_oracle_rollback.argtypes = [vp, ctypes.c_int64, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int,
+                                          vp, ctypes.c_int64, vp, vp]
     return lib
 
 
@@ -168,3 +171,26 @@ def inverse_cdf(w, u, *, lib=None):
     lo, hi = ctypes.c_double(), ctypes.c_double()
     t = lib.specv_oracle_inverse_cdf(_ptr(w), w.shape[0], float(u), ctypes.byref(lo), ctypes.byref(hi))
     return t, lo.value, hi.value
+
+
+def rollback(num_accepted, k, seq_lens, block_tables, num_blocks, block_size, free_list, free_count, *, lib=None):
+    """Paged KV rollback after verification, on copies of the inputs.
+    num_accepted [B], seq_lens [B], block_tables [B, max_blocks],
+    num_blocks [B] int32; free_list [capacity] int32 and free_count (int):
+    the free list and its fill.  Returns a dict: seq_lens, block_tables,
+    num_blocks, free_list, free_count, row_status."""
+    lib = lib or load()
+    na = np.ascontiguousarray(num_accepted, dtype=np.int32)
+    sl = np.array(seq_lens, dtype=np.int32, copy=True)
+    bt = np.array(block_tables, dtype=np.int32, copy=True)
+    nb = np.array(num_blocks, dtype=np.int32, copy=True)
+    fl = np.array(free_list, dtype=np.int32, copy=True)
+    fc = np.array([free_count], dtype=np.int32)
+    st = np.zeros(len(na), np.int32)
+    B, mb = bt.shape
+    rc = lib.specv_oracle_rollback(_ptr(na), B, int(k), _ptr(sl), _ptr(bt), mb, _ptr(nb), int(block_size),
+                                   _ptr(fl), len(fl), _ptr(fc), _ptr(st))
+    if rc != 0:
+        raise ValueError(f"specv_oracle_rollback: bad arguments ({rc})")
+    return {"seq_lens": sl, "block_tables": bt, "num_blocks": nb, "free_list": fl, "free_count": int(fc[0]),
+            "row_status": st}

@@ -460,3 +460,57 @@ int specv_oracle_verify(int dtype, const void *logits, const float *q, const int
     free(th);
     return err ? -2 : 0;
 }
+
+/* ---------------------------------------------------------------- rollback
+ * Paged KV-cache bookkeeping after verification, row by row in batch order
+ * ([A] s.6 "PagedKVCacheManager", rollback_to): a row whose cache holds
+ * seq_len positions, the last k of them the drafts, keeps
+ *   target_len = seq_len - (k - num_accepted)
+ * positions; its block table keeps ceil(target_len / block_size) blocks
+ * (0 for an empty sequence) and the rest are popped from the end, each one
+ * appended to the free list as it is popped.  A row whose num_accepted is
+ * outside [0, k], whose target length would be negative, or whose block
+ * count is out of [0, max_blocks] is left as it is and gets status 128.
+ * If the free list cannot take every freed block, nothing changes and every
+ * row gets status 256.  Popped table entries are set to -1.             */
+int specv_oracle_rollback(const int32_t *num_accepted, int64_t B, int k, int32_t *seq_lens,
+                          int32_t *block_tables, int max_blocks, int32_t *num_blocks, int block_size,
+                          int32_t *free_list, int64_t free_capacity, int32_t *free_count,
+                          int32_t *row_status) {
+    if (B < 0 || k < 0 || max_blocks < 0 || block_size < 1 || !num_accepted || !seq_lens ||
+        !block_tables || !num_blocks || !free_count || (!free_list && free_capacity > 0))
+        return -1;
+    /* the free list's room is checked against the whole batch first */
+    int64_t total = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        int32_t n = num_accepted[b], len = seq_lens[b], nb = num_blocks[b];
+        if (n < 0 || n > k || len - (k - n) < 0 || nb < 0 || nb > max_blocks) continue;
+        int64_t target = (int64_t)len - (k - n);
+        int64_t needed = target > 0 ? (target + block_size - 1) / block_size : 0;
+        if (nb > needed) total += nb - needed;
+    }
+    if ((int64_t)*free_count + total > free_capacity) {
+        if (row_status)
+            for (int64_t b = 0; b < B; ++b) row_status[b] = 256;
+        return 0;
+    }
+    for (int64_t b = 0; b < B; ++b) {
+        int32_t n = num_accepted[b], len = seq_lens[b];
+        int32_t *table = block_tables + b * max_blocks;
+        if (n < 0 || n > k || len - (k - n) < 0 || num_blocks[b] < 0 || num_blocks[b] > max_blocks) {
+            if (row_status) row_status[b] = 128;
+            continue;
+        }
+        int64_t target = (int64_t)len - (k - n);
+        int64_t needed = target > 0 ? (target + block_size - 1) / block_size : 0;
+        while (num_blocks[b] > needed) {
+            int32_t freed = table[num_blocks[b] - 1]; /* pop */
+            table[num_blocks[b] - 1] = -1;
+            num_blocks[b] -= 1;
+            free_list[(*free_count)++] = freed; /* append */
+        }
+        seq_lens[b] = (int32_t)target;
+        if (row_status) row_status[b] = 0;
+    }
+    return 0;
+}

@@ -210,6 +210,28 @@ def specv_verify_sample_host(h: Handle, logits, q, x, u, T, *, out=None, stream=
     return out
 
 
+def specv_rollback(h: Handle, num_accepted, k, seq_lens, block_tables, num_blocks, block_size, free_list,
+                   free_count, *, row_status=None, stream=None):
+    """Paged KV-cache rollback after verification, in place on CUDA int32
+    tensors: num_accepted [B], seq_lens [B], block_tables [B, max_blocks],
+    num_blocks [B], free_list [capacity], free_count [1]; row_status [B]
+    (optional) receives 0 / 128 (invalid row) / 256 (no room)."""
+    torch = _torch()
+    B = num_accepted.shape[0]
+    mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    ptrs = []
+    for t, name, shape in ((num_accepted, "num_accepted", (B,)), (seq_lens, "seq_lens", (B,)),
+                           (block_tables, "block_tables", (B, mb)), (num_blocks, "num_blocks", (B,)),
+                           (free_list, "free_list", None), (free_count, "free_count", (1,))):
+        ptrs.append(_dev(t, torch.int32, name, shape))
+    prs = None if row_status is None else _dev(row_status, torch.int32, "row_status", (B,))
+    st = _lib.load().specv_rollback(
+        h.ptr, ctypes.c_void_p(ptrs[0]), B, int(k), ctypes.c_void_p(ptrs[1]), ctypes.c_void_p(ptrs[2]), mb,
+        ctypes.c_void_p(ptrs[3]), int(block_size), ctypes.c_void_p(ptrs[4]), free_list.numel(),
+        ctypes.c_void_p(ptrs[5]), ctypes.c_void_p(prs), _stream_ptr(stream))
+    _check(st, "specv_rollback")
+
+
 def specv_plan_cluster(h: Handle, logits_dtype, B, k, V) -> int:
     return int(_lib.load().specv_plan_cluster(h.ptr, logits_dtype, B, k, V))
 

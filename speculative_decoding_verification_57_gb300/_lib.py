@@ -60,6 +60,8 @@ def load(build_if_missing=True):
     lib.specv_verify_greedy.argtypes = [vp, i32, vp, vp, i32, i32, i64, vp, vp, vp, vp]
     lib.specv_verify_sample_host.restype = i32
     lib.specv_verify_sample_host.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp]
+    lib.specv_rollback.restype = i32
+    lib.specv_rollback.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, i32, vp, i64, vp, vp, vp]
     lib.specv_plan_cluster.restype = i32
     lib.specv_plan_cluster.argtypes = [vp, i32, i32, i32, i64]
     lib.specv_launch_count.restype = i64

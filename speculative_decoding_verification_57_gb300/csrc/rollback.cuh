@@ -1,0 +1,118 @@
+// rollback.cuh -- paged KV-cache bookkeeping after verification, on the
+// device: for every row, drop the cache positions of the rejected drafts,
+// pop the blocks the shorter sequence no longer needs and append them to the
+// free list ("LLM Inference & Speculative Decoding: From Roofline Physics to
+// Lossless Acceleration", s.6, PagedKVCacheManager.rollback_to).
+//
+// The result equals rolling the rows back one at a time in batch order: row
+// b's popped blocks land in the free list after those of rows 0..b-1, each
+// row's blocks last-first, as popping them one at a time would.  One CTA of
+// 1024 threads walks the batch in chunks of 1024 rows; a block-wide scan of
+// the per-row counts places every row's blocks.
+#pragma once
+#include <cstdint>
+
+namespace specv {
+
+constexpr int kRollbackThreads = 1024;
+
+enum : int { RB_INVALID = 128, RB_NO_ROOM = 256 };
+
+struct RollbackArgs {
+    const int32_t* num_accepted;  // [B]
+    int32_t* seq_lens;            // [B] in/out: positions held, the last k the drafts
+    int32_t* block_tables;        // [B, max_blocks] in/out: popped entries become -1
+    int32_t* num_blocks;          // [B] in/out
+    int32_t* free_list;           // [capacity]
+    int32_t* free_count;          // [1] in/out: fill of free_list
+    int32_t* row_status;          // [B] (nullable): 0, RB_INVALID or RB_NO_ROOM
+    long long capacity;
+    int B, k, max_blocks, block_size;
+};
+
+// Blocks row b gives back, or -1 if its inputs are invalid.
+__device__ __forceinline__ int rollback_count(const RollbackArgs& r, int b, int& target, int& needed) {
+    const int n = r.num_accepted[b], len = r.seq_lens[b], nb = r.num_blocks[b];
+    if (n < 0 || n > r.k || len - (r.k - n) < 0 || nb < 0 || nb > r.max_blocks) return -1;
+    target = len - (r.k - n);
+    needed = target > 0 ? (target + r.block_size - 1) / r.block_size : 0;
+    return nb > needed ? nb - needed : 0;
+}
+
+// Exclusive prefix sum over the CTA (1024 threads); *total gets the sum.
+__device__ __forceinline__ long long block_exclusive_scan(long long v, long long* warp_sums, long long* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long incl = v;
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        long long w = warp_sums[lane];
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long o = __shfl_up_sync(0xffffffffu, w, off);
+            if (lane >= off) w += o;
+        }
+        warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const long long before = warp == 0 ? 0 : warp_sums[warp - 1];
+    *total = warp_sums[31];
+    __syncthreads();  // warp_sums is reused by the next call
+    return before + incl - v;
+}
+
+__global__ void __launch_bounds__(kRollbackThreads, 1) rollback_kernel(const RollbackArgs r) {
+    __shared__ long long warp_sums[32];
+    __shared__ int no_room;
+    // 1. every row's count: does the free list have room for all of them?
+    long long total = 0;
+    for (int c0 = 0; c0 < r.B; c0 += kRollbackThreads) {
+        const int b = c0 + static_cast<int>(threadIdx.x);
+        int target = 0, needed = 0;
+        const int cnt = b < r.B ? rollback_count(r, b, target, needed) : 0;
+        long long chunk;
+        block_exclusive_scan(cnt > 0 ? cnt : 0, warp_sums, &chunk);
+        total += chunk;
+    }
+    if (threadIdx.x == 0) no_room = (static_cast<long long>(*r.free_count) + total > r.capacity) ? 1 : 0;
+    __syncthreads();
+    const long long base0 = *r.free_count;
+    __syncthreads();
+    if (no_room) {
+        if (r.row_status)
+            for (int b = threadIdx.x; b < r.B; b += kRollbackThreads) r.row_status[b] = RB_NO_ROOM;
+        return;
+    }
+    // 2. place and pop
+    long long base = base0;
+    for (int c0 = 0; c0 < r.B; c0 += kRollbackThreads) {
+        const int b = c0 + static_cast<int>(threadIdx.x);
+        int target = 0, needed = 0;
+        const int cnt = b < r.B ? rollback_count(r, b, target, needed) : 0;
+        long long chunk;
+        const long long off = base + block_exclusive_scan(cnt > 0 ? cnt : 0, warp_sums, &chunk);
+        if (b < r.B) {
+            if (cnt < 0) {
+                if (r.row_status) r.row_status[b] = RB_INVALID;
+            } else {
+                int32_t* table = r.block_tables + static_cast<long long>(b) * r.max_blocks;
+                const int nb = r.num_blocks[b];
+                for (int i = 0; i < cnt; ++i) {
+                    r.free_list[off + i] = table[nb - 1 - i];
+                    table[nb - 1 - i] = -1;
+                }
+                r.num_blocks[b] = nb - cnt;
+                r.seq_lens[b] = target;
+                if (r.row_status) r.row_status[b] = 0;
+            }
+        }
+        base += chunk;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) *r.free_count = static_cast<int32_t>(base);
+}
+
+}  // namespace specv

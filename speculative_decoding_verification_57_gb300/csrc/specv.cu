@@ -15,6 +15,7 @@
 #include "../../include/specv.h"
 #include "verify_cluster.cuh"
 #include "verify_warp.cuh"
+#include "rollback.cuh"
 
 using namespace specv;
 
@@ -358,4 +359,36 @@ const char* specv_status_string(specv_status s) {
 
 const char* specv_last_cuda_error(void) { return g_last_error; }
 
+specv_status specv_rollback(specv_handle h, const int32_t* num_accepted, int batch, int k, int32_t* seq_lens,
+                            int32_t* block_tables, int max_blocks, int32_t* num_blocks, int block_size,
+                            int32_t* free_list, int64_t free_capacity, int32_t* free_count, int32_t* row_status,
+                            void* stream) {
+    if (!h || batch < 0 || k < 0 || k > h->max_k || max_blocks < 0 || block_size < 1 || free_capacity < 0)
+        return SPECV_ERR_INVALID_ARGUMENT;
+    if (!free_count || (free_capacity > 0 && !free_list)) return SPECV_ERR_INVALID_ARGUMENT;
+    if (batch > 0 && (!num_accepted || !seq_lens || !num_blocks || (max_blocks > 0 && !block_tables)))
+        return SPECV_ERR_INVALID_ARGUMENT;
+    DeviceGuard g(h->device);
+    if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
+    RollbackArgs r;
+    r.num_accepted = num_accepted;
+    r.seq_lens = seq_lens;
+    r.block_tables = block_tables;
+    r.num_blocks = num_blocks;
+    r.free_list = free_list;
+    r.free_count = free_count;
+    r.row_status = row_status;
+    r.capacity = free_capacity;
+    r.B = batch;
+    r.k = k;
+    r.max_blocks = max_blocks;
+    r.block_size = block_size;
+    rollback_kernel<<<1, kRollbackThreads, 0, static_cast<cudaStream_t>(stream)>>>(r);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "rollback launch");
+    h->launches.fetch_add(1);
+    return SPECV_OK;
+}
+
 }  // extern "C"
+
