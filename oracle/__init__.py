@@ -53,6 +53,9 @@ def _declare(lib):
     lib.specv_oracle_residual.argtypes = [vp, vp, ctypes.c_int64, vp, dp]
     lib.specv_oracle_inverse_cdf.restype = ctypes.c_int64
     lib.specv_oracle_inverse_cdf.argtypes = [vp, ctypes.c_int64, ctypes.c_double, dp, dp]
+    lib.specv_oracle_tree_greedy.restype = ctypes.c_int
+    lib.specv_oracle_tree_greedy.argtypes = [ctypes.c_int, vp, vp, vp, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
+                                             vp, vp, vp, vp]
     lib.specv_oracle_rollback.restype = ctypes.c_int
     lib.specv_oracle_rollback.argtypes = [vp, ctypes.c_int64, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int,
                                           vp, ctypes.c_int64, vp, vp]
@@ -194,3 +197,24 @@ def rollback(num_accepted, k, seq_lens, block_tables, num_blocks, block_size, fr
         raise ValueError(f"specv_oracle_rollback: bad arguments ({rc})")
     return {"seq_lens": sl, "block_tables": bt, "num_blocks": nb, "free_list": fl, "free_count": int(fc[0]),
             "row_status": st}
+
+
+def tree_greedy(logits, tokens, parents, *, lib=None):
+    """Greedy verification of draft trees.  logits [B, M+1, V] float32 or
+    uint16 (bf16 bits): row 0 after the prefix, row 1+i after node i;
+    tokens, parents [B, M] int32 (parent -1: child of the prefix).  Returns
+    num_accepted [B], out_tokens [B, M+1], path [B, M], row_status [B]."""
+    lib = lib or load()
+    logits = np.ascontiguousarray(logits)
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    parents = np.ascontiguousarray(parents, dtype=np.int32)
+    B, m1, V = logits.shape
+    M = m1 - 1
+    out = {"num_accepted": np.empty(B, np.int32), "out_tokens": np.empty((B, M + 1), np.int32),
+           "path": np.empty((B, M), np.int32), "row_status": np.empty(B, np.int32)}
+    rc = lib.specv_oracle_tree_greedy(_dtype_code(logits), _ptr(logits), _ptr(tokens), _ptr(parents), B, M, V,
+                                      _ptr(out["num_accepted"]), _ptr(out["out_tokens"]), _ptr(out["path"]),
+                                      _ptr(out["row_status"]))
+    if rc != 0:
+        raise ValueError(f"specv_oracle_tree_greedy: bad arguments ({rc})")
+    return out

@@ -514,3 +514,74 @@ int specv_oracle_rollback(const int32_t *num_accepted, int64_t B, int k, int32_t
     }
     return 0;
 }
+
+/* ---------------------------------------------------------------- tree
+ * Greedy verification of a draft tree ([A] s.3 "Multi-Draft Tree
+ * Speculation"; [B] "SpecInfer and Tree-Based Verification": the target
+ * scores every node in one pass and the longest accepted path is kept).
+ * Row b holds M draft nodes: token[i] and parent[i] in [-1, i) (-1: a child
+ * of the prefix).  Logit row 0 is the target's prediction after the prefix,
+ * row 1 + i its prediction after node i.  Node i is accepted iff its parent
+ * is (the prefix always is) and token[i] equals the argmax (lowest index on
+ * ties) of its parent's row.  The deepest accepted node wins, the lowest
+ * index among equally deep ones; the row emits the tokens of its path from
+ * the prefix down, then the argmax of its own row (the bonus; row 0 when no
+ * node is accepted).  num_accepted = the path length.  Errors (no tokens
+ * emitted, num_accepted 0): a NaN logit in any of the M + 1 rows (bit 1), a
+ * token outside [0, V) (bit 2), a parent outside [-1, i) (bit 512).        */
+int specv_oracle_tree_greedy(int dtype, const void *logits, const int32_t *tokens, const int32_t *parents,
+                             int64_t B, int M, int64_t V, int32_t *num_accepted, int32_t *out_tokens,
+                             int32_t *path, int32_t *row_status) {
+    if (B < 0 || M < 1 || M > 4096 || V < 1 || (dtype != 0 && dtype != 1)) return -1;
+    if (!logits || !tokens || !parents || !num_accepted || !out_tokens || !row_status) return -1;
+    int64_t *amax = (int64_t *)malloc(sizeof(int64_t) * (size_t)(M + 1));
+    int *acc = (int *)malloc(sizeof(int) * (size_t)M);
+    int *depth = (int *)malloc(sizeof(int) * (size_t)M);
+    if (!amax || !acc || !depth) {
+        free(amax);
+        free(acc);
+        free(depth);
+        return -2;
+    }
+    const size_t esz = dtype == 1 ? 2 : 4;
+    for (int64_t b = 0; b < B; ++b) {
+        const int32_t *tok = tokens + b * M, *par = parents + b * M;
+        int st = 0;
+        for (int r = 0; r <= M; ++r) {
+            const void *row = (const unsigned char *)logits + ((size_t)b * (M + 1) + r) * (size_t)V * esz;
+            double mx;
+            st |= specv_oracle_argmax(dtype, row, V, &amax[r], &mx);
+        }
+        for (int i = 0; i < M; ++i) {
+            if (tok[i] < 0 || tok[i] >= V) st |= ST_TOKEN_RANGE;
+            if (par[i] < -1 || par[i] >= i) st |= 512;
+        }
+        for (int i = 0; i <= M; ++i) out_tokens[b * (M + 1) + i] = -1;
+        if (path)
+            for (int i = 0; i < M; ++i) path[b * M + i] = -1;
+        row_status[b] = st;
+        if (st) {
+            num_accepted[b] = 0;
+            continue;
+        }
+        int best = -1;
+        for (int i = 0; i < M; ++i) {
+            const int p = par[i];
+            const int parent_ok = p < 0 ? 1 : acc[p];
+            acc[i] = parent_ok && (int64_t)tok[i] == amax[p + 1];
+            depth[i] = p < 0 ? 0 : depth[p] + 1;
+            if (acc[i] && (best < 0 || depth[i] > depth[best])) best = i;
+        }
+        const int n = best < 0 ? 0 : depth[best] + 1;
+        num_accepted[b] = n;
+        for (int node = best, d = n - 1; node >= 0; node = par[node], --d) {
+            out_tokens[b * (M + 1) + d] = tok[node];
+            if (path) path[b * M + d] = node;
+        }
+        out_tokens[b * (M + 1) + n] = (int32_t)amax[best + 1];
+    }
+    free(amax);
+    free(acc);
+    free(depth);
+    return 0;
+}
