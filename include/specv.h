@@ -65,9 +65,11 @@
  *                                   infinite at an examined entry
  *                               64  an internal wait timed out (the result of
  *                                   this row is not valid)
+ *                              512  (tree verification) a parent index
+ *                                   outside [-1, node)
  *                              The walk checks position 0, 1, ... in order and
  *                              stops at the first position with an error; a
- *                              row with any of the bits 1, 2, 4, 8, 32, 64 set
+ *                              row with any of the bits 1, 2, 4, 8, 32, 64, 512 set
  *                              reports num_accepted = 0 and out_tokens = -1.
  *
  * Ownership and execution: the caller owns every buffer.  Calls are
@@ -132,6 +134,34 @@ specv_status specv_verify_greedy(specv_handle h, specv_dtype logits_dtype, const
                                  const int32_t *draft_tokens, int batch, int k, int64_t V,
                                  int32_t *num_accepted, int32_t *out_tokens, int32_t *row_status,
                                  void *stream);
+
+/* Greedy verification of draft trees ("LLM Inference & Speculative Decoding:
+ * From Roofline Physics to Lossless Acceleration", s.3 "Multi-Draft Tree
+ * Speculation"; "Speculative Decoding: Mathematical Foundations, ...",
+ * "SpecInfer and Tree-Based Verification": the target scores every node in
+ * one pass and the longest accepted path is kept).  Device pointers:
+ *   target_logits [B, M+1, V]  row 0: the prediction after the prefix;
+ *                              row 1+i: the prediction after node i
+ *   tokens        [B, M]       int32, the draft token of each node
+ *   parents       [B, M]       int32, parent node of each node, in [-1, i)
+ *                              (-1: a child of the prefix)
+ *   num_accepted  [B]          out: length of the kept path
+ *   out_tokens    [B, M+1]     out: the path's tokens from the prefix down,
+ *                              then the bonus (argmax after the path's last
+ *                              node, or of row 0), -1 after
+ *   path          [B, M]       out (nullable): the path's node indices, -1 after
+ *   row_status    [B]          out (nullable): 0, or bits 1 (a NaN logit in
+ *                              any row), 2 (a token outside [0, V)), 512 (a
+ *                              parent outside [-1, i)); such rows emit nothing
+ * A node is kept iff its parent is kept (the prefix always is) and its
+ * token is the argmax (lowest index on ties) of its parent's row; the
+ * deepest kept node wins, the lowest index among equally deep ones.  The
+ * pages define the path only in words; this is the plain reading.  A chain
+ * (parent i-1) gives exactly specv_verify_greedy.  1 <= M <= max_k. */
+specv_status specv_verify_tree_greedy(specv_handle h, specv_dtype logits_dtype, const void *target_logits,
+                                      const int32_t *tokens, const int32_t *parents, int batch, int M, int64_t V,
+                                      int32_t *num_accepted, int32_t *out_tokens, int32_t *path,
+                                      int32_t *row_status, void *stream);
 
 /* Same as specv_verify_sample, but every pointer is HOST memory (pinned
  * memory gives the fastest copies).  The handle copies the inputs to device

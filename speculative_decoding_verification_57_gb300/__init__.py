@@ -181,6 +181,34 @@ def specv_verify_greedy(h: Handle, logits, x, *, out=None, stream=None):
     return out
 
 
+def specv_verify_tree_greedy(h: Handle, logits, tokens, parents, *, out=None, stream=None):
+    """Greedy verification of draft trees: logits [B, M+1, V] (row 0 after
+    the prefix, row 1+i after node i), tokens and parents [B, M] int32
+    (parent -1: a child of the prefix).  Returns num_accepted [B],
+    out_tokens [B, M+1], path [B, M], row_status [B]."""
+    torch = _torch()
+    B, m1, V = logits.shape
+    M = m1 - 1
+    dt = _logits_dtype(logits)
+    _dev(logits, logits.dtype, "logits")
+    pt = _dev(tokens, torch.int32, "tokens", (B, M))
+    pp = _dev(parents, torch.int32, "parents", (B, M))
+    dev = logits.device
+    if out is None:
+        out = {
+            "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
+            "out_tokens": torch.empty((B, M + 1), dtype=torch.int32, device=dev),
+            "path": torch.empty((B, M), dtype=torch.int32, device=dev),
+            "row_status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+    st = _lib.load().specv_verify_tree_greedy(
+        h.ptr, dt, ctypes.c_void_p(logits.data_ptr()), ctypes.c_void_p(pt), ctypes.c_void_p(pp), B, M, V,
+        ctypes.c_void_p(out["num_accepted"].data_ptr()), ctypes.c_void_p(out["out_tokens"].data_ptr()),
+        ctypes.c_void_p(out["path"].data_ptr()), ctypes.c_void_p(out["row_status"].data_ptr()), _stream_ptr(stream))
+    _check(st, "specv_verify_tree_greedy")
+    return out
+
+
 def specv_verify_sample_host(h: Handle, logits, q, x, u, T, *, out=None, stream=None):
     """Host-buffer verification: CPU tensors in (pinned memory copies
     fastest), CPU tensors out; the call copies, verifies and synchronises.

@@ -276,6 +276,28 @@ specv_status specv_verify_greedy(specv_handle h, specv_dtype logits_dtype, const
     return run(h, logits_dtype, a, stream);
 }
 
+specv_status specv_verify_tree_greedy(specv_handle h, specv_dtype logits_dtype, const void* target_logits,
+                                      const int32_t* tokens, const int32_t* parents, int batch, int M, int64_t V,
+                                      int32_t* num_accepted, int32_t* out_tokens, int32_t* path,
+                                      int32_t* row_status, void* stream) {
+    specv_status st = check_sizes(h, logits_dtype, batch, M, V);
+    if (st != SPECV_OK) return st;
+    if (batch > 0 && (!target_logits || !tokens || !parents || !num_accepted || !out_tokens))
+        return SPECV_ERR_INVALID_ARGUMENT;
+    VerifyArgs a = {};
+    a.logits = target_logits;
+    a.x = tokens;
+    a.parents = parents;
+    a.path = path;
+    a.num_accepted = num_accepted;
+    a.out_tokens = out_tokens;
+    a.row_status = row_status;
+    a.V = V;
+    a.B = batch;
+    a.k = M;
+    return run(h, logits_dtype, a, stream);
+}
+
 specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, const void* target_logits,
                                       const float* draft_probs, const int32_t* draft_tokens,
                                       const float* uniforms, const float* temperature, int batch, int k,

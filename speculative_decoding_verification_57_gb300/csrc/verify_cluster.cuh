@@ -61,7 +61,8 @@ enum : int {
     ST_ZERO_RESIDUAL = 16,
     ST_QBAD = 32,
     ST_TIMEOUT = 64,
-    ST_ERRMASK = 1 | 2 | 4 | 8 | 32 | 64,
+    ST_PARENT = 512,  // tree verification: a parent index outside [-1, node)
+    ST_ERRMASK = 1 | 2 | 4 | 8 | 32 | 64 | 512,
 };
 
 // Stop-row weights: residual max(0, e - s q); bonus e; fallback e (zero
@@ -77,6 +78,8 @@ struct VerifyArgs {
     int32_t* num_accepted;   // [B]
     int32_t* out_tokens;     // [B, k+1]
     int32_t* row_status;     // [B] (nullable)
+    const int32_t* parents;  // [B, k] tree verification: parent node of each draft (-1: the prefix); null: a chain
+    int32_t* path;           // [B, k] tree verification: accepted node indices, root first (nullable)
     float* dbg_p;            // [B, k] (nullable)
     float* dbg_q;            // [B, k]
     float* dbg_max;          // [B, k+1]
@@ -336,6 +339,75 @@ __device__ __forceinline__ void sweep_lane(LaneAcc& A, const unsigned char* ls, 
     A.q += q0 + q1;
 }
 
+// Greedy verification of a draft tree, one warp ("LLM Inference & Speculative
+// Decoding ...", s.3 "Multi-Draft Tree Speculation"; "Speculative Decoding:
+// Mathematical Foundations, ...", "SpecInfer and Tree-Based Verification":
+// the longest accepted path is kept).  Lane i < k holds node i (token xi,
+// parent pi in [-1, i)); lane r <= k holds the argmax A of logit row r (row
+// 0 after the prefix, row 1 + i after node i) and its flags (bit 0 NaN, bit
+// 1 timeout).  A node is kept iff its token is its parent row's argmax and
+// every ancestor is kept (pointer jumping over the parent links, 5 rounds for
+// up to 32 nodes); the deepest kept node wins, the lowest index among equals;
+// the bonus is the argmax of its own row.  Writes the outputs if `write`.
+__device__ __forceinline__ int tree_greedy_warp(const VerifyArgs& a, int b, int k, int lane, int xi, int pi, int A,
+                                                int flags, bool write) {
+    const unsigned full = 0xffffffffu;
+    const bool node = lane < k;
+    int err = 0;
+    if (lane <= k && (flags & 1)) err |= ST_NONFINITE;
+    if (lane <= k && (flags & 2)) err |= ST_TIMEOUT;
+    if (node && (xi < 0 || xi >= a.V)) err |= ST_TOKEN;
+    if (node && (pi < -1 || pi >= lane)) err |= ST_PARENT;
+    err = static_cast<int>(__reduce_or_sync(full, static_cast<unsigned>(err)));
+    const int pv = (node && !(err & ST_PARENT)) ? pi : -1;
+    const int apar = __shfl_sync(full, A, pv + 1);
+    bool m = node && xi == apar;      // kept along the path to the prefix
+    int d = (node && pv >= 0) ? 1 : 0;  // depth (children of the prefix: 0)
+    int p = pv;
+    for (int s = 0; s < 5; ++s) {
+        const int src = p >= 0 ? p : lane;
+        const bool mp = __shfl_sync(full, m, src);
+        const int dp = __shfl_sync(full, d, src);
+        const int pp = __shfl_sync(full, p, src);
+        if (p >= 0) {
+            m = m && mp;
+            d += dp;
+            p = pp;
+        }
+    }
+    const int key = (node && m) ? ((d << 6) | (63 - lane)) : -1;
+    const int kb = __reduce_max_sync(full, key);
+    const int best = kb < 0 ? -1 : 63 - (kb & 63);
+    const int n = best < 0 ? 0 : (kb >> 6) + 1;
+    const int bonus = __shfl_sync(full, A, best + 1);
+    if (write) {
+        int tokv = -1, pathv = -1;
+        int cur = best;
+        for (int s = 0; s < 32 && cur >= 0; ++s) {  // cur is the same in every lane
+            const int dc = __shfl_sync(full, d, cur);
+            const int tc = __shfl_sync(full, xi, cur);
+            const int pc = __shfl_sync(full, pv, cur);
+            if (lane == dc) {
+                tokv = tc;
+                pathv = cur;
+            }
+            cur = pc;
+        }
+        if (lane == n) tokv = bonus;
+        if (err) {
+            tokv = -1;
+            pathv = -1;
+        }
+        if (lane <= k) a.out_tokens[static_cast<long long>(b) * (k + 1) + lane] = tokv;
+        if (lane < k && a.path) a.path[static_cast<long long>(b) * k + lane] = pathv;
+        if (lane == 0) {
+            a.num_accepted[b] = err ? 0 : n;
+            if (a.row_status) a.row_status[b] = err;
+        }
+    }
+    return err;
+}
+
 // Write a sampled row's outputs: the kept drafts, the drawn token, -1 after.
 __device__ __forceinline__ void write_sampled(const VerifyArgs& a, int b, int k, int j, int token, int st,
                                               const int* xs) {
@@ -381,10 +453,11 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     const float c = greedy || !t_ok ? 0.0f : kLog2e / T;
 
     // per-position scalars, lane i of warp 0 holds position i
-    int xi = -1;
+    int xi = -1, pi = lane - 1;
     float u0 = 0.0f, u1 = 0.0f, Lx = 0.0f, qx = 0.0f;
     if (warp == 0 && lane <= k && t_ok) {
         if (lane < k) xi = __ldg(a.x + static_cast<long long>(b) * k + lane);
+        if (lane < k && a.parents) pi = __ldg(a.parents + static_cast<long long>(b) * k + lane);
         if (!greedy) {
             const long long ub = (static_cast<long long>(b) * (k + 1) + lane) * 2;
             u0 = __ldg(a.u + ub);
@@ -698,85 +771,96 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             if (greedy && A == 0x7fffffff) A = 0;  // every value is -inf: index 0
         }
         __syncwarp();
-        int err = 0;
-        bool stop = false;
-        float p = 0.0f;
-        if (lane <= k && t_ok) {
-            if (flags & 2) err |= ST_TIMEOUT;
-            if (greedy) {
-                if (flags & 1) err |= ST_NONFINITE;
-                if (lane < k && (xi < 0 || xi >= V)) err |= ST_TOKEN;
-                stop = (err != 0) || lane == k || xi != A;
-            } else {
-                if (!(isfinite(M) && isfinite(S))) err |= ST_NONFINITE;
-                if (lane < k) {
-                    if (xi < 0 || xi >= V) err |= ST_TOKEN;
-                    if (!(u0 >= 0.0f && u0 < 1.0f)) err |= ST_UNIFORM;
-                    if (xi >= 0 && xi < V && !(qx >= 0.0f && qx <= FLT_MAX)) err |= ST_QBAD;
-                    if (!err) {
-                        // p_i(x_i) with the double-float exponential (a masked
-                        // entry, logit -inf, has p = 0)
-                        const df c2 = log2e_over(T);
-                        RowConst rc;
-                        rc.M = M;
-                        rc.s1 = S;
-                        rc.thr = 0.0f;
-                        rc.ch = c2.hi;
-                        rc.cl = c2.lo;
-                        p = df_val(exact_weight<BF16>(Lx, 0.0f, MODE_BONUS, rc, df_make(0.0f), sh.exp2tab)) / S;
-                        const float rho = fminf(1.0f, p / fmaxf(qx, 1e-12f));
-                        stop = !(u0 < rho);
+        if (a.parents) {
+            // a draft tree (all rows greedy): rank 0 writes the outputs
+            const int terr = tree_greedy_warp(a, b, k, lane, xi, pi, A, flags, rank == 0);
+            if (lane == 0) {
+                sh.status = terr;
+                sh.j = 0;
+            }
+            if (rank == 0 && lane <= k && a.dbg_max) a.dbg_max[static_cast<long long>(b) * (k + 1) + lane] = M;
+        }
+        if (!a.parents) {  // a chain of drafts
+            int err = 0;
+            bool stop = false;
+            float p = 0.0f;
+            if (lane <= k && t_ok) {
+                if (flags & 2) err |= ST_TIMEOUT;
+                if (greedy) {
+                    if (flags & 1) err |= ST_NONFINITE;
+                    if (lane < k && (xi < 0 || xi >= V)) err |= ST_TOKEN;
+                    stop = (err != 0) || lane == k || xi != A;
+                } else {
+                    if (!(isfinite(M) && isfinite(S))) err |= ST_NONFINITE;
+                    if (lane < k) {
+                        if (xi < 0 || xi >= V) err |= ST_TOKEN;
+                        if (!(u0 >= 0.0f && u0 < 1.0f)) err |= ST_UNIFORM;
+                        if (xi >= 0 && xi < V && !(qx >= 0.0f && qx <= FLT_MAX)) err |= ST_QBAD;
+                        if (!err) {
+                            // p_i(x_i) with the double-float exponential (a masked
+                            // entry, logit -inf, has p = 0)
+                            const df c2 = log2e_over(T);
+                            RowConst rc;
+                            rc.M = M;
+                            rc.s1 = S;
+                            rc.thr = 0.0f;
+                            rc.ch = c2.hi;
+                            rc.cl = c2.lo;
+                            p = df_val(exact_weight<BF16>(Lx, 0.0f, MODE_BONUS, rc, df_make(0.0f), sh.exp2tab)) / S;
+                            const float rho = fminf(1.0f, p / fmaxf(qx, 1e-12f));
+                            stop = !(u0 < rho);
+                        } else {
+                            stop = true;
+                        }
                     } else {
                         stop = true;
                     }
-                } else {
-                    stop = true;
                 }
             }
-        }
-        __syncwarp();
-        const unsigned mask = __ballot_sync(0xffffffffu, lane <= k && stop);
-        const int j = t_ok ? (__ffs(mask) - 1) : 0;
-        int st = t_ok ? __shfl_sync(0xffffffffu, err, j) : ST_TEMP;
-        if (t_ok && !greedy && !(st & ST_ERRMASK)) {
-            const float uj = __shfl_sync(0xffffffffu, u1, j);
-            if (!(uj >= 0.0f && uj < 1.0f)) st |= ST_UNIFORM;
-        }
-        const float Mj = __shfl_sync(0xffffffffu, M, j);
-        const float Sj = __shfl_sync(0xffffffffu, S, j);
-        const int Aj = __shfl_sync(0xffffffffu, A, j);
-        const float ujj = __shfl_sync(0xffffffffu, u1, j);
-        if (lane == 0) {
-            sh.uj = ujj;
-            sh.j = j;
-            sh.status = st;
-            sh.Mj = Mj;
-            sh.sj = Sj;
-            sh.mode = (j < k) ? (a.q ? MODE_RESIDUAL : MODE_ONEHOT) : MODE_BONUS;
-        }
-        if (lane <= k) sh.xs[lane] = xi;
-        // rank 0 writes debug values and, for greedy or failed rows, the outputs
-        if (rank == 0) {
-            if (lane <= k && t_ok) {
-                if (a.dbg_max) a.dbg_max[static_cast<long long>(b) * (k + 1) + lane] = M;
-                if (a.dbg_sumexp) a.dbg_sumexp[static_cast<long long>(b) * (k + 1) + lane] = greedy ? 0.0f : S;
-                if (lane < k) {
-                    const bool xok = xi >= 0 && xi < V;
-                    if (a.dbg_p) a.dbg_p[static_cast<long long>(b) * k + lane] = (greedy || !xok) ? 0.0f : p;
-                    if (a.dbg_q) a.dbg_q[static_cast<long long>(b) * k + lane] = (greedy || !xok) ? 0.0f : qx;
-                }
+            __syncwarp();
+            const unsigned mask = __ballot_sync(0xffffffffu, lane <= k && stop);
+            const int j = t_ok ? (__ffs(mask) - 1) : 0;
+            int st = t_ok ? __shfl_sync(0xffffffffu, err, j) : ST_TEMP;
+            if (t_ok && !greedy && !(st & ST_ERRMASK)) {
+                const float uj = __shfl_sync(0xffffffffu, u1, j);
+                if (!(uj >= 0.0f && uj < 1.0f)) st |= ST_UNIFORM;
             }
-            if (lane == 0 && a.dbg_resid) a.dbg_resid[b] = 0.0f;
-            if (greedy || !t_ok || (st & ST_ERRMASK)) {
-                const bool bad = (st & ST_ERRMASK) != 0;
-                if (lane <= k) {
-                    int tok = -1;
-                    if (!bad) tok = lane < j ? xi : (lane == j ? Aj : -1);
-                    a.out_tokens[static_cast<long long>(b) * (k + 1) + lane] = tok;
+            const float Mj = __shfl_sync(0xffffffffu, M, j);
+            const float Sj = __shfl_sync(0xffffffffu, S, j);
+            const int Aj = __shfl_sync(0xffffffffu, A, j);
+            const float ujj = __shfl_sync(0xffffffffu, u1, j);
+            if (lane == 0) {
+                sh.uj = ujj;
+                sh.j = j;
+                sh.status = st;
+                sh.Mj = Mj;
+                sh.sj = Sj;
+                sh.mode = (j < k) ? (a.q ? MODE_RESIDUAL : MODE_ONEHOT) : MODE_BONUS;
+            }
+            if (lane <= k) sh.xs[lane] = xi;
+            // rank 0 writes debug values and, for greedy or failed rows, the outputs
+            if (rank == 0) {
+                if (lane <= k && t_ok) {
+                    if (a.dbg_max) a.dbg_max[static_cast<long long>(b) * (k + 1) + lane] = M;
+                    if (a.dbg_sumexp) a.dbg_sumexp[static_cast<long long>(b) * (k + 1) + lane] = greedy ? 0.0f : S;
+                    if (lane < k) {
+                        const bool xok = xi >= 0 && xi < V;
+                        if (a.dbg_p) a.dbg_p[static_cast<long long>(b) * k + lane] = (greedy || !xok) ? 0.0f : p;
+                        if (a.dbg_q) a.dbg_q[static_cast<long long>(b) * k + lane] = (greedy || !xok) ? 0.0f : qx;
+                    }
                 }
-                if (lane == 0) {
-                    a.num_accepted[b] = bad ? 0 : j;
-                    if (a.row_status) a.row_status[b] = st;
+                if (lane == 0 && a.dbg_resid) a.dbg_resid[b] = 0.0f;
+                if (greedy || !t_ok || (st & ST_ERRMASK)) {
+                    const bool bad = (st & ST_ERRMASK) != 0;
+                    if (lane <= k) {
+                        int tok = -1;
+                        if (!bad) tok = lane < j ? xi : (lane == j ? Aj : -1);
+                        a.out_tokens[static_cast<long long>(b) * (k + 1) + lane] = tok;
+                    }
+                    if (lane == 0) {
+                        a.num_accepted[b] = bad ? 0 : j;
+                        if (a.row_status) a.row_status[b] = st;
+                    }
                 }
             }
         }

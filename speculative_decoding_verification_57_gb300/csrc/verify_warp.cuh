@@ -33,11 +33,12 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
     const df c2 = (greedy || !t_ok) ? df_make(0.0f) : log2e_over(T);
     const long long base = static_cast<long long>(b) * (k + 1) * V;
 
-    int xi = -1;
+    int xi = -1, pi = lane - 1;
     float u0 = 0.0f, u1 = 0.0f, Mi = -INFINITY, Si = 0.0f, p = 0.0f, qx = 0.0f;
     int Ai = 0x7fffffff, nanf = 0;
     if (lane <= k && t_ok) {
         if (lane < k) xi = __ldg(a.x + static_cast<long long>(b) * k + lane);
+        if (lane < k && a.parents) pi = __ldg(a.parents + static_cast<long long>(b) * k + lane);
         if (!greedy) {
             u0 = __ldg(a.u + (static_cast<long long>(b) * (k + 1) + lane) * 2);
             u1 = __ldg(a.u + (static_cast<long long>(b) * (k + 1) + lane) * 2 + 1);
@@ -83,6 +84,12 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
         }
     }
     __syncwarp();
+    if (a.parents) {
+        // a draft tree (all rows greedy)
+        tree_greedy_warp(a, b, k, lane, xi, pi, Ai == 0x7fffffff ? 0 : Ai, nanf, true);
+        if (lane <= k && a.dbg_max) a.dbg_max[static_cast<long long>(b) * (k + 1) + lane] = Mi;
+        return;
+    }
     // accept tests, one lane per position
     int err = 0;
     bool stop = false;
