@@ -42,8 +42,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--graph-calls", type=int, default=100)
-    p.add_argument("--variant", choices=["sample", "onehot"], default="sample",
-                   help="onehot: the same workload verified as one-hot drafts (q = None)")
+    p.add_argument("--variant", choices=["sample", "onehot", "tree"], default="sample",
+                   help="onehot: the same workload verified as one-hot drafts (q = None); tree: greedy "
+                        "verification of 16-node draft trees over the same vocabulary")
     return p.parse_args(argv)
 
 
@@ -80,6 +81,33 @@ def algorithmic_bytes(w, num_accepted, row_status, onehot=False):
     rejected = ok & (w.T != 0) & (num_accepted < k)
     qrow = 0 if onehot else int(rejected.sum()) * V * 4
     return (B * (k + 1) * V * esz + qrow + B * k * (8 if onehot else 12) + B * 12 + B * (k + 2) * 4)
+
+
+TREE_M = 16
+
+
+def make_tree_workload(seed, B=64, M=TREE_M, V=128256):
+    """Greedy draft trees over the benchmark vocabulary: logits as in the
+    benchmark workload (N(0, 3^2) + an +8 spike per row, bf16), each node's
+    parent uniform among the prefix and the earlier nodes, and its token the
+    argmax of its parent's row with probability 0.8 (else uniform)."""
+    import numpy as np
+
+    from speculative_decoding_verification_57_gb300 import workloads as W
+
+    rng = np.random.default_rng(seed)
+    L = rng.normal(scale=3.0, size=(B, M + 1, V))
+    L[np.arange(B)[:, None], np.arange(M + 1)[None, :], rng.integers(0, V, size=(B, M + 1))] += 8.0
+    Lb = W.f32_to_bf16_bits(L.astype(np.float32))
+    A = np.argmax(W.bf16_bits_to_f32(Lb), axis=-1)
+    par = np.array([[int(rng.integers(-1, i)) for i in range(M)] for _ in range(B)], np.int32)
+    tok = rng.integers(0, V, size=(B, M)).astype(np.int32)
+    keep = rng.random((B, M)) < 0.8
+    for b in range(B):
+        for i in range(M):
+            if keep[b, i]:
+                tok[b, i] = A[b, par[b, i] + 1]
+    return Lb, tok, par
 
 
 def kernel_source_hash():
@@ -247,6 +275,8 @@ def run_ours(args):
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
 
+    if args.variant == "tree":
+        return run_tree(args, sv, dev, rank, ws, local, hbm_peak, peak_src)
     w = W.make_config(CONFIG_INDEX, seed=57000 + CONFIG_INDEX + 1000 * rank)
     onehot = args.variant == "onehot"
     if onehot:
@@ -412,6 +442,125 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_tree(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
+    """Greedy tree verification: rows/s over 16-node trees, V = 128256 bf16."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    Lb, tok, par = make_tree_workload(57100 + 1000 * rank)
+    B, M1, V = Lb.shape
+    M = M1 - 1
+    h = sv.specv_create(local, max_batch=B, max_k=M, vocab=V)
+    L0 = torch.from_numpy(Lb.view(np.int16)).view(torch.bfloat16)
+    sets = [dict(L=L0.to(dev), t=torch.from_numpy(tok).to(dev), p=torch.from_numpy(par).to(dev))
+            for _ in range(N_SETS)]
+    outs = [dict(num_accepted=torch.empty(B, dtype=torch.int32, device=dev),
+                 out_tokens=torch.empty((B, M + 1), dtype=torch.int32, device=dev),
+                 path=torch.empty((B, M), dtype=torch.int32, device=dev),
+                 row_status=torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(N_SETS)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(i):
+        s = sets[i % N_SETS]
+        sv.specv_verify_tree_greedy(h, s["L"], s["t"], s["p"], out=outs[i % N_SETS], stream=stream)
+
+    with torch.cuda.stream(stream):
+        call(0)
+    stream.synchronize()
+    got = {kk: v.cpu().numpy() for kk, v in outs[0].items()}
+    ref = oracle.tree_greedy(Lb, tok, par)
+    if not all(np.array_equal(got[kk], ref[kk]) for kk in ref):
+        raise RuntimeError("tree verification differs from the oracle on the benchmark inputs")
+    alg = B * M1 * V * 2 + B * M * 8 + B * 4 + B * M1 * 4 + B * M * 4 + B * 4
+    G = max(1, min(args.graph_calls, args.steps))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        call(0)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                call(i)
+    reps = max(1, args.steps // G)
+    steps = reps * G
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, (args.warmup + G - 1) // G)):
+            g.replay()
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark("t0")
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    sampler.mark("t1")
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    ms_max = reduce_max(ev0.elapsed_time(ev1), ws, dev)
+    per_call_s = ms_max / 1e3 / steps
+    # end to end: pinned host inputs copied in, outputs read back, every step
+    pin = dict(L=L0.pin_memory(), t=torch.from_numpy(tok).pin_memory(), p=torch.from_numpy(par).pin_memory())
+    host_out = {kk: torch.empty_like(v, device="cpu").pin_memory() for kk, v in outs[0].items()}
+    e2e_steps = max(1, args.e2e_steps)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            s = sets[0]
+            s["L"].copy_(pin["L"], non_blocking=True)
+            s["t"].copy_(pin["t"], non_blocking=True)
+            s["p"].copy_(pin["p"], non_blocking=True)
+            call(0)
+            for kk in host_out:
+                host_out[kk].copy_(outs[0][kk], non_blocking=True)
+        stream.synchronize()
+    e2e_s = reduce_max(time.perf_counter() - t0, ws, dev)
+    if rank != 0:
+        return 0
+    cores = host_cores()
+    oracle.tree_greedy(Lb[:8], tok[:8], par[:8])
+    n, t1 = 0, time.perf_counter()
+    while time.perf_counter() - t1 < 1.5 or n < 2:
+        oracle.tree_greedy(Lb[:8], tok[:8], par[:8])
+        n += 1
+    cpu_value = 8 * n / (time.perf_counter() - t1)
+    achieved = alg / per_call_s / 1e9
+    line = {
+        "metric": "tree-verify rows/s", "value": B * steps * ws / (ms_max / 1e3), "unit": "rows/s", "n_gpus": ws,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms_max / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"greedy tree verify B={B} M={M} nodes V={V} bf16 (random trees, 0.8 of tokens "
+                               "the parent's argmax)", "B": B, "M": M, "V": V, "global_batch": B * ws,
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": f"rotating {N_SETS} input sets ({N_SETS * Lb.nbytes / 1e9:.2f} GB) > 2x L2",
+                   "launch": f"CUDA graph of {G} calls, {specv_cluster_desc(sv, h, B, M, V)}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
+                     "algorithmic_bytes_per_launch": alg},
+        "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} oracle calls x 8 rows, one thread"},
+        "e2e": {"value": B * e2e_steps * ws / e2e_s, "unit": "rows/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out.values()),
+                "steps": e2e_steps, "path": "pinned copies + specv_verify_tree_greedy + copies back, per step"},
+        "gpu_launches": steps, "mean_num_accepted": float(np.mean(got["num_accepted"])), "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 

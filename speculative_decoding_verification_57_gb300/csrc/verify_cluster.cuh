@@ -628,9 +628,12 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 }
                 if (greedy) {
                     if (lmax > m) {
-                        // first element equal to the new maximum, in index order
-                        const long long tile_e0 = v0 + h + static_cast<long long>(lt) * (kTileBytes / esz);
-                        bool found = false;
+                        // lowest tile-local index holding the new maximum: the
+                        // candidates reduced by min in a tree (chunk r of this
+                        // thread covers elements ch*per+..., ch = tid + r*128)
+                        constexpr int kPerWord = BF16 ? 2 : 1;
+                        constexpr int kCand = kPer * 4 * kPerWord;
+                        int cand[kCand];
 #pragma unroll
                         for (int r = 0; r < kPer; ++r) {
                             const int ch = tid + r * kConsumers;
@@ -638,22 +641,20 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
                                 if (BF16) {
-                                    if (!found && bf16_lo(ws[q4]) == lmax) {
-                                        found = true;
-                                        arg = static_cast<int>(tile_e0 + ch * 8 + q4 * 2);
-                                    }
-                                    if (!found && bf16_hi(ws[q4]) == lmax) {
-                                        found = true;
-                                        arg = static_cast<int>(tile_e0 + ch * 8 + q4 * 2 + 1);
-                                    }
+                                    cand[(r * 4 + q4) * 2] = bf16_lo(ws[q4]) == lmax ? ch * 8 + q4 * 2 : 0x7fffffff;
+                                    cand[(r * 4 + q4) * 2 + 1] =
+                                        bf16_hi(ws[q4]) == lmax ? ch * 8 + q4 * 2 + 1 : 0x7fffffff;
                                 } else {
-                                    if (!found && __uint_as_float(ws[q4]) == lmax) {
-                                        found = true;
-                                        arg = static_cast<int>(tile_e0 + ch * 4 + q4);
-                                    }
+                                    cand[r * 4 + q4] = __uint_as_float(ws[q4]) == lmax ? ch * 4 + q4 : 0x7fffffff;
                                 }
                             }
                         }
+#pragma unroll
+                        for (int half = kCand / 2; half > 0; half >>= 1)
+#pragma unroll
+                            for (int i2 = 0; i2 < half; ++i2) cand[i2] = min(cand[i2], cand[i2 + half]);
+                        const long long tile_e0 = v0 + h + static_cast<long long>(lt) * (kTileBytes / esz);
+                        arg = static_cast<int>(tile_e0 + cand[0]);
                         m = lmax;
                     }
                 } else if (lmax == -INFINITY) {
