@@ -26,7 +26,8 @@ ST_UNIFORM_RANGE = 4
 ST_TEMPERATURE = 8
 ST_ZERO_RESIDUAL = 16
 ST_Q_INVALID = 32
-ST_ERROR_MASK = ST_NONFINITE | ST_TOKEN_RANGE | ST_UNIFORM_RANGE | ST_TEMPERATURE | ST_Q_INVALID
+ST_FILTER = 1024
+ST_ERROR_MASK = ST_NONFINITE | ST_TOKEN_RANGE | ST_UNIFORM_RANGE | ST_TEMPERATURE | ST_Q_INVALID | ST_FILTER
 
 
 def compile_oracle(src: str = _SRC, out: str = _LIB, extra_flags=()) -> str:
@@ -56,6 +57,9 @@ def _declare(lib):
     lib.specv_oracle_tree_greedy.restype = ctypes.c_int
     lib.specv_oracle_tree_greedy.argtypes = [ctypes.c_int, vp, vp, vp, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                              vp, vp, vp, vp]
+    lib.specv_oracle_verify_warped.restype = ctypes.c_int
+    lib.specv_oracle_verify_warped.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, ctypes.c_int,
+                                               ctypes.c_int64, vp, vp, vp, vp, ctypes.c_double]
     lib.specv_oracle_rollback.restype = ctypes.c_int
     lib.specv_oracle_rollback.argtypes = [vp, ctypes.c_int64, ctypes.c_int, vp, vp, ctypes.c_int, vp, ctypes.c_int,
                                           vp, ctypes.c_int64, vp, vp]
@@ -217,4 +221,29 @@ def tree_greedy(logits, tokens, parents, *, lib=None):
                                       _ptr(out["row_status"]))
     if rc != 0:
         raise ValueError(f"specv_oracle_tree_greedy: bad arguments ({rc})")
+    return out
+
+
+def verify_warped(logits, q, x, u, T, top_k, top_p, *, boundary_eps=1e-6, lib=None):
+    """Sampled verification with top-k / top-p applied to the target p
+    (top_k [B] int32 in [1, 4096], top_p [B] float32 in (0, 1]; q None:
+    one-hot drafts).  Returns num_accepted, out_tokens, row_status,
+    boundary."""
+    lib = lib or load()
+    logits = np.ascontiguousarray(logits)
+    x = np.ascontiguousarray(x, dtype=np.int32)
+    B, k1, V = logits.shape
+    q = None if q is None else np.ascontiguousarray(q, dtype=np.float32)
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    T = np.ascontiguousarray(T, dtype=np.float32)
+    tk = np.ascontiguousarray(top_k, dtype=np.int32)
+    tp = np.ascontiguousarray(top_p, dtype=np.float32)
+    out = {"num_accepted": np.empty(B, np.int32), "out_tokens": np.empty((B, k1), np.int32),
+           "row_status": np.empty(B, np.int32), "boundary": np.empty(B, np.int32)}
+    rc = lib.specv_oracle_verify_warped(_dtype_code(logits), _ptr(logits), _ptr(q), _ptr(x), _ptr(u), _ptr(T),
+                                        _ptr(tk), _ptr(tp), B, k1 - 1, V, _ptr(out["num_accepted"]),
+                                        _ptr(out["out_tokens"]), _ptr(out["row_status"]), _ptr(out["boundary"]),
+                                        float(boundary_eps))
+    if rc != 0:
+        raise ValueError(f"specv_oracle_verify_warped: bad arguments ({rc})")
     return out

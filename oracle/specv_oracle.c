@@ -59,7 +59,8 @@
 #define ST_TEMPERATURE 8
 #define ST_ZERO_RESIDUAL 16
 #define ST_Q_INVALID 32
-#define ST_ERROR_MASK (ST_NONFINITE | ST_TOKEN_RANGE | ST_UNIFORM_RANGE | ST_TEMPERATURE | ST_Q_INVALID)
+#define ST_FILTER 1024 /* warped verification: top_k outside [1, 4096] or top_p outside (0, 1] */
+#define ST_ERROR_MASK (ST_NONFINITE | ST_TOKEN_RANGE | ST_UNIFORM_RANGE | ST_TEMPERATURE | ST_Q_INVALID | ST_FILTER)
 
 /* Exact decoding of one stored logit to double. dtype 0 = float32,
  * dtype 1 = bfloat16 (the upper 16 bits of a float32). */
@@ -583,5 +584,206 @@ int specv_oracle_tree_greedy(int dtype, const void *logits, const int32_t *token
     free(amax);
     free(acc);
     free(depth);
+    return 0;
+}
+
+/* ---------------------------------------------------------------- warping
+ * Sampled verification with top-k / top-p applied to the target p before
+ * the rule ([C] "Why the output is exactly p": temperature, top-k and top-p
+ * have to be applied to p before the rule; [D] "The rejection-sampling
+ * correctness argument": the rule composes with anything that changes p).
+ * The pages name the filters but do not define them; the readings here:
+ *   top-k: the K entries with the largest logits, the lower index first
+ *          among equal logits (exactly min(K, V) entries);
+ *   top-p: within those, in the same order, the shortest prefix whose mass
+ *          (renormalised over the K entries) reaches top_p (at least one
+ *          entry; top_p >= 1 keeps all K);
+ *   p'   = exp((l - M) / T) on the kept set P, renormalised; 0 elsewhere.
+ * The rule then runs on p' exactly as in verify_sampled_row; the residual
+ * max(0, p' - q) lives on P only (q is read there and at the draft tokens,
+ * and only there is it checked), and the inverse CDF walks P in vocabulary
+ * order.  q == NULL: one-hot drafts.  Greedy rows (T = 0) are unaffected:
+ * the argmax is always kept.                                              */
+typedef struct {
+    double *val;
+    int64_t *idx;
+    double *e;
+    int n;
+} kept_t;
+
+/* P of one row: returns ST_NONFINITE for a NaN / +inf logit or an all -inf
+ * row, else 0; fills kept->(val, idx, e) in rank order and the kept count. */
+static int warp_row(int dtype, const void *row, int64_t V, double T, int K, double top_p, kept_t *kp,
+                    double *S_out) {
+    int cnt = 0;
+    if (K > V) K = (int)V;
+    for (int64_t v = 0; v < V; ++v) {
+        double l = logit_at(dtype, row, v);
+        if (isnan(l) || l == INFINITY) return ST_NONFINITE;
+        if (cnt == K && !(l > kp->val[cnt - 1])) continue;
+        int pos = cnt < K ? cnt : K - 1;
+        if (cnt < K) ++cnt;
+        while (pos > 0 && l > kp->val[pos - 1]) { /* equal values keep the lower index first */
+            kp->val[pos] = kp->val[pos - 1];
+            kp->idx[pos] = kp->idx[pos - 1];
+            --pos;
+        }
+        kp->val[pos] = l;
+        kp->idx[pos] = v;
+    }
+    double M = kp->val[0];
+    if (M == -INFINITY) return ST_NONFINITE;
+    double SK = 0.0;
+    for (int r = 0; r < cnt; ++r) {
+        kp->e[r] = exp((kp->val[r] - M) / T);
+        SK += kp->e[r];
+    }
+    int n = cnt;
+    if (top_p < 1.0) {
+        double c = 0.0;
+        for (n = 0; n < cnt;) {
+            c += kp->e[n];
+            ++n;
+            if (c >= top_p * SK) break;
+        }
+    }
+    double S = 0.0;
+    for (int r = 0; r < n; ++r) S += kp->e[r];
+    kp->n = n;
+    *S_out = S;
+    return 0;
+}
+
+/* Inverse CDF over the kept entries in vocabulary order: the smallest index
+ * v with u * W < (sum of w over kept entries with index <= v); else the last
+ * kept index with positive weight.  w[r] belongs to kp->idx[r].            */
+static int64_t kept_inverse_cdf(const kept_t *kp, const double *w, double u, double *lo, double *hi) {
+    int order[4096] = {0};
+    int n = kp->n;
+    for (int r = 0; r < n; ++r) order[r] = r;
+    for (int a = 1; a < n; ++a) { /* insertion sort by index */
+        int t = order[a], b = a;
+        while (b > 0 && kp->idx[order[b - 1]] > kp->idx[t]) {
+            order[b] = order[b - 1];
+            --b;
+        }
+        order[b] = t;
+    }
+    double W = 0.0;
+    for (int r = 0; r < n; ++r) W += w[order[r]];
+    double target = u * W, C = 0.0;
+    for (int r = 0; r < n; ++r) {
+        double before = C;
+        C += w[order[r]];
+        if (target < C) {
+            *lo = before / W;
+            *hi = C / W;
+            return kp->idx[order[r]];
+        }
+    }
+    int last = n - 1;
+    while (last > 0 && !(w[order[last]] > 0.0)) --last;
+    *lo = *hi = 1.0;
+    return kp->idx[order[last]];
+}
+
+int specv_oracle_verify_warped(int dtype, const void *logits, const float *q, const int32_t *x, const float *u,
+                               const float *T, const int32_t *top_k, const float *top_p, int64_t B, int k,
+                               int64_t V, int32_t *num_accepted, int32_t *out_tokens, int32_t *row_status,
+                               int32_t *boundary, double boundary_eps) {
+    if (B < 0 || k < 1 || V < 1 || (dtype != 0 && dtype != 1)) return -1;
+    if (!logits || !x || !u || !T || !top_k || !top_p || !num_accepted || !out_tokens || !row_status) return -1;
+    kept_t kp;
+    kp.n = 0;
+    kp.val = (double *)malloc(sizeof(double) * 4096);
+    kp.idx = (int64_t *)malloc(sizeof(int64_t) * 4096);
+    kp.e = (double *)malloc(sizeof(double) * 4096);
+    double *w = (double *)malloc(sizeof(double) * 4096);
+    if (!kp.val || !kp.idx || !kp.e || !w) {
+        free(kp.val), free(kp.idx), free(kp.e), free(w);
+        return -2;
+    }
+    const size_t esz = dtype == 1 ? 2 : 4;
+    job_t J = {dtype, logits, q, x, u, T, B, k, V, num_accepted, out_tokens, row_status,
+               NULL, NULL, NULL, NULL, NULL, boundary, boundary_eps};
+    for (int64_t b = 0; b < B; ++b) {
+        if (boundary) boundary[b] = 0;
+        float Tf = T[b];
+        if (!temperature_ok(Tf)) {
+            finish_error(&J, b, ST_TEMPERATURE);
+            continue;
+        }
+        if (Tf == 0.0f) {
+            verify_greedy_row(&J, b);
+            continue;
+        }
+        int K = top_k[b];
+        float tp = top_p[b];
+        if (K < 1 || K > 4096 || !(tp > 0.0f && tp <= 1.0f)) {
+            finish_error(&J, b, ST_FILTER);
+            continue;
+        }
+        int j = k, st = 0;
+        double S = 0.0;
+        for (int i = 0; i <= k; ++i) {
+            const void *row = (const unsigned char *)logits + ((size_t)b * (k + 1) + i) * (size_t)V * esz;
+            st = warp_row(dtype, row, V, (double)Tf, K, (double)tp, &kp, &S);
+            if (i == k) break;
+            int32_t xi = x[b * k + i];
+            float ui = u[(b * (k + 1) + i) * 2];
+            if (xi < 0 || xi >= V) st |= ST_TOKEN_RANGE;
+            if (!uniform_ok(ui)) st |= ST_UNIFORM_RANGE;
+            double qx = 0.0;
+            if (xi >= 0 && xi < V) {
+                qx = q ? (double)q[(b * k + i) * V + xi] : 1.0;
+                if (!(qx >= 0.0 && qx <= (double)FLT_MAX)) st |= ST_Q_INVALID;
+            }
+            if (st) break;
+            double px = 0.0;
+            for (int r = 0; r < kp.n; ++r)
+                if (kp.idx[r] == xi) px = kp.e[r] / S;
+            double rho = px / (qx > 1e-12 ? qx : 1e-12);
+            if (rho > 1.0) rho = 1.0;
+            note_boundary(&J, b, i, 0, (double)ui, rho);
+            if (!((double)ui < rho)) {
+                j = i;
+                break;
+            }
+        }
+        float u1 = u[(b * (k + 1) + j) * 2 + 1];
+        if (!st && !uniform_ok(u1)) st |= ST_UNIFORM_RANGE;
+        if (st) {
+            finish_error(&J, b, st);
+            continue;
+        }
+        int status = 0;
+        double lo = 0.0, hi = 1.0;
+        int64_t token;
+        for (int r = 0; r < kp.n; ++r) w[r] = kp.e[r] / S; /* p' on P */
+        if (j < k) {
+            double Wr = 0.0;
+            const int32_t xj = x[b * k + j];
+            for (int r = 0; r < kp.n; ++r) {
+                double qv = q ? (double)q[(b * k + j) * V + kp.idx[r]] : (kp.idx[r] == xj ? 1.0 : 0.0);
+                if (!(qv >= 0.0 && qv <= (double)FLT_MAX)) st |= ST_Q_INVALID;
+                double r_ = kp.e[r] / S - qv;
+                w[r] = r_ > 0.0 ? r_ : 0.0;
+                Wr += w[r];
+            }
+            if (st) {
+                finish_error(&J, b, st);
+                continue;
+            }
+            if (!(Wr > 0.0)) {
+                status |= ST_ZERO_RESIDUAL;
+                for (int r = 0; r < kp.n; ++r) w[r] = kp.e[r] / S;
+            }
+        }
+        token = kept_inverse_cdf(&kp, w, (double)u1, &lo, &hi);
+        note_boundary(&J, b, j, 1, (double)u1, lo);
+        note_boundary(&J, b, j, 1, (double)u1, hi);
+        finish_ok(&J, b, j, token, status);
+    }
+    free(kp.val), free(kp.idx), free(kp.e), free(w);
     return 0;
 }
