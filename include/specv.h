@@ -67,9 +67,11 @@
  *                                   this row is not valid)
  *                              512  (tree verification) a parent index
  *                                   outside [-1, node)
+ *                             1024  (top-k / top-p verification) top_k
+ *                                   outside [1, 64] or top_p outside (0, 1]
  *                              The walk checks position 0, 1, ... in order and
  *                              stops at the first position with an error; a
- *                              row with any of the bits 1, 2, 4, 8, 32, 64, 512 set
+ *                              row with any of the bits 1, 2, 4, 8, 32, 64, 512, 1024 set
  *                              reports num_accepted = 0 and out_tokens = -1.
  *
  * Ownership and execution: the caller owns every buffer.  Calls are
@@ -127,6 +129,30 @@ specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const
                                  const float *uniforms, const float *temperature, int batch, int k,
                                  int64_t V, int32_t *num_accepted, int32_t *out_tokens,
                                  int32_t *row_status, const specv_debug *dbg, void *stream);
+
+/* Sampled verification with top-k / top-p applied to each target row before
+ * the rule ("Speculative decoding." lesson, "Why the output is exactly p":
+ * temperature, top-k and top-p have to be applied to p before the rule, and
+ * to q before drafting -- q is used as given).  The pages name the filters
+ * without defining them; the readings here:
+ *   top_k [B] int32, 1..64: keep the top_k largest logits, the lower index
+ *         first among equal logits;
+ *   top_p [B] fp32, (0, 1]: within those, in the same order, keep the
+ *         shortest prefix whose mass (renormalised over the top_k) reaches
+ *         top_p (at least one entry; 1 keeps all top_k).
+ * p' = exp((l - max) / T) on the kept set, renormalised; the accept test,
+ * the residual max(0, p' - q) and the bonus use p'.  The residual and the
+ * bonus are drawn over the kept set in vocabulary order; q is read (and
+ * checked, bit 32) only there and at the draft tokens.  draft_probs may be
+ * NULL (one-hot drafts).  A row whose top_k or top_p is out of range gets
+ * row_status bit 1024 and emits nothing.  Rows with temperature 0 take the
+ * greedy rule (the filters keep the argmax).  Other arguments and bits as
+ * for specv_verify_sample; no debug outputs.  One CTA per row. */
+specv_status specv_verify_sample_filtered(specv_handle h, specv_dtype logits_dtype, const void *target_logits,
+                                          const float *draft_probs, const int32_t *draft_tokens,
+                                          const float *uniforms, const float *temperature, const int32_t *top_k,
+                                          const float *top_p, int batch, int k, int64_t V, int32_t *num_accepted,
+                                          int32_t *out_tokens, int32_t *row_status, void *stream);
 
 /* Greedy verification of every row (no draft probabilities, uniforms or
  * temperatures): keep x_i while it equals the target argmax. */

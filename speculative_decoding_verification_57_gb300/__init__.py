@@ -181,6 +181,37 @@ def specv_verify_greedy(h: Handle, logits, x, *, out=None, stream=None):
     return out
 
 
+def specv_verify_sample_filtered(h: Handle, logits, q, x, u, T, top_k, top_p, *, out=None, stream=None):
+    """Sampled verification with top-k / top-p applied to the target rows:
+    as specv_verify_sample (q may be None: one-hot drafts), plus top_k [B]
+    int32 in 1..64 and top_p [B] fp32 in (0, 1], CUDA tensors."""
+    torch = _torch()
+    B, k1, V = logits.shape
+    k = k1 - 1
+    dt = _logits_dtype(logits)
+    _dev(logits, logits.dtype, "logits")
+    pq = None if q is None else _dev(q, torch.float32, "q", (B, k, V))
+    px = _dev(x, torch.int32, "x", (B, k))
+    pu = _dev(u, torch.float32, "u", (B, k + 1, 2))
+    pt = _dev(T, torch.float32, "T", (B,))
+    pk = _dev(top_k, torch.int32, "top_k", (B,))
+    pp = _dev(top_p, torch.float32, "top_p", (B,))
+    dev = logits.device
+    if out is None:
+        out = {
+            "num_accepted": torch.empty(B, dtype=torch.int32, device=dev),
+            "out_tokens": torch.empty((B, k + 1), dtype=torch.int32, device=dev),
+            "row_status": torch.empty(B, dtype=torch.int32, device=dev),
+        }
+    st = _lib.load().specv_verify_sample_filtered(
+        h.ptr, dt, ctypes.c_void_p(logits.data_ptr()), ctypes.c_void_p(pq), ctypes.c_void_p(px), ctypes.c_void_p(pu),
+        ctypes.c_void_p(pt), ctypes.c_void_p(pk), ctypes.c_void_p(pp), B, k, V,
+        ctypes.c_void_p(out["num_accepted"].data_ptr()), ctypes.c_void_p(out["out_tokens"].data_ptr()),
+        ctypes.c_void_p(out["row_status"].data_ptr()), _stream_ptr(stream))
+    _check(st, "specv_verify_sample_filtered")
+    return out
+
+
 def specv_verify_tree_greedy(h: Handle, logits, tokens, parents, *, out=None, stream=None):
     """Greedy verification of draft trees: logits [B, M+1, V] (row 0 after
     the prefix, row 1+i after node i), tokens and parents [B, M] int32

@@ -22,8 +22,9 @@ ST_ZERO_RESIDUAL = 16
 ST_Q_INVALID = 32
 ST_TIMEOUT = 64
 ST_PARENT = 512
+ST_FILTER = 1024
 ST_ERROR_MASK = (ST_NONFINITE | ST_TOKEN_RANGE | ST_UNIFORM_RANGE | ST_TEMPERATURE | ST_Q_INVALID | ST_TIMEOUT
-                 | ST_PARENT)
+                 | ST_PARENT | ST_FILTER)
 
 
 class SpecvDebug(ctypes.Structure):
@@ -62,6 +63,8 @@ def load(build_if_missing=True):
     lib.specv_verify_greedy.argtypes = [vp, i32, vp, vp, i32, i32, i64, vp, vp, vp, vp]
     lib.specv_verify_sample_host.restype = i32
     lib.specv_verify_sample_host.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp]
+    lib.specv_verify_sample_filtered.restype = i32
+    lib.specv_verify_sample_filtered.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp]
     lib.specv_verify_tree_greedy.restype = i32
     lib.specv_verify_tree_greedy.argtypes = [vp, i32, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp, vp]
     lib.specv_rollback.restype = i32

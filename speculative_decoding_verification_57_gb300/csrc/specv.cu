@@ -16,6 +16,7 @@
 #include "verify_cluster.cuh"
 #include "verify_warp.cuh"
 #include "rollback.cuh"
+#include "verify_topk.cuh"
 
 using namespace specv;
 
@@ -148,6 +149,9 @@ template <bool BF16>
 cudaError_t set_attributes() {
     cudaError_t e = cudaFuncSetAttribute(verify_cluster_kernel<BF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(verify_topk_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(topk_dyn_smem(kMaxK)));
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(verify_cluster_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(cluster_dyn_smem(16, kMaxK + 1)));
 }
@@ -274,6 +278,45 @@ specv_status specv_verify_greedy(specv_handle h, specv_dtype logits_dtype, const
     a.B = batch;
     a.k = k;
     return run(h, logits_dtype, a, stream);
+}
+
+specv_status specv_verify_sample_filtered(specv_handle h, specv_dtype logits_dtype, const void* target_logits,
+                                          const float* draft_probs, const int32_t* draft_tokens, const float* uniforms,
+                                          const float* temperature, const int32_t* top_k, const float* top_p,
+                                          int batch, int k, int64_t V, int32_t* num_accepted, int32_t* out_tokens,
+                                          int32_t* row_status, void* stream) {
+    specv_status st = check_sizes(h, logits_dtype, batch, k, V);
+    if (st != SPECV_OK) return st;
+    if (batch > 0 && (!target_logits || !draft_tokens || !uniforms || !temperature || !top_k || !top_p ||
+                      !num_accepted || !out_tokens))
+        return SPECV_ERR_INVALID_ARGUMENT;
+    if (batch == 0) return SPECV_OK;
+    DeviceGuard g(h->device);
+    if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
+    VerifyArgs a = {};
+    a.logits = target_logits;
+    a.q = draft_probs;
+    a.x = draft_tokens;
+    a.u = uniforms;
+    a.temp = temperature;
+    a.top_k = top_k;
+    a.top_p = top_p;
+    a.num_accepted = num_accepted;
+    a.out_tokens = out_tokens;
+    a.row_status = row_status;
+    a.V = V;
+    a.B = batch;
+    a.k = k;
+    const size_t dyn = topk_dyn_smem(k);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (logits_dtype == SPECV_BF16)
+        verify_topk_kernel<true><<<batch, kThreads, dyn, s>>>(a);
+    else
+        verify_topk_kernel<false><<<batch, kThreads, dyn, s>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "verify_topk launch");
+    h->launches.fetch_add(1, std::memory_order_relaxed);
+    return SPECV_OK;
 }
 
 specv_status specv_verify_tree_greedy(specv_handle h, specv_dtype logits_dtype, const void* target_logits,

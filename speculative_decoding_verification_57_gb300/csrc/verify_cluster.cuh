@@ -61,8 +61,9 @@ enum : int {
     ST_ZERO_RESIDUAL = 16,
     ST_QBAD = 32,
     ST_TIMEOUT = 64,
-    ST_PARENT = 512,  // tree verification: a parent index outside [-1, node)
-    ST_ERRMASK = 1 | 2 | 4 | 8 | 32 | 64 | 512,
+    ST_PARENT = 512,   // tree verification: a parent index outside [-1, node)
+    ST_FILTER = 1024,  // top-k / top-p verification: top_k outside [1, 64] or top_p outside (0, 1]
+    ST_ERRMASK = 1 | 2 | 4 | 8 | 32 | 64 | 512 | 1024,
 };
 
 // Stop-row weights: residual max(0, e - s q); bonus e; fallback e (zero
@@ -80,6 +81,8 @@ struct VerifyArgs {
     int32_t* row_status;     // [B] (nullable)
     const int32_t* parents;  // [B, k] tree verification: parent node of each draft (-1: the prefix); null: a chain
     int32_t* path;           // [B, k] tree verification: accepted node indices, root first (nullable)
+    const int32_t* top_k;    // [B] top-k / top-p verification: entries kept (null: the plain rule)
+    const float* top_p;      // [B] top-k / top-p verification: nucleus mass within them
     float* dbg_p;            // [B, k] (nullable)
     float* dbg_q;            // [B, k]
     float* dbg_max;          // [B, k+1]

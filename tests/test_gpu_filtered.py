@@ -1,0 +1,95 @@
+"""GPU parity of top-k / top-p verification with the oracle ("Speculative
+decoding." lesson, "Why the output is exactly p": the filters are applied to
+p before the rule).  Integer outputs must match on every row whose uniforms
+lie away from the decision edges (the oracle's boundary flag)."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_verification_57_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def h():
+    import speculative_decoding_verification_57_gb300 as sv
+
+    handle = sv.specv_create(0, max_batch=4096, max_k=31, vocab=262_144)
+    yield handle
+    sv.specv_destroy(handle)
+
+
+def _run(h, w, top_k, top_p, onehot=False):
+    import torch
+
+    import speculative_decoding_verification_57_gb300 as sv
+    from parity import to_device
+
+    L, q, x, u, T = to_device(w, "cuda:0")
+    out = sv.specv_verify_sample_filtered(h, L, None if onehot else q, x, u, T,
+                                          torch.from_numpy(np.asarray(top_k, np.int32)).cuda(),
+                                          torch.from_numpy(np.asarray(top_p, np.float32)).cuda())
+    torch.cuda.synchronize()
+    return {kk: v.cpu().numpy() for kk, v in out.items()}
+
+
+def _check(w, got, top_k, top_p, onehot=False):
+    ref = oracle.verify_warped(w.logits, None if onehot else w.q, w.x, w.u, w.T, top_k, top_p)
+    same = ((got["num_accepted"] == ref["num_accepted"]) & (got["row_status"] == ref["row_status"])
+            & (got["out_tokens"] == ref["out_tokens"]).all(1))
+    flagged = ref["boundary"] != 0
+    bad = np.nonzero(~same & ~flagged)[0]
+    assert len(bad) == 0, (bad[:5], got["out_tokens"][bad[:3]], ref["out_tokens"][bad[:3]],
+                           got["row_status"][bad[:3]], ref["row_status"][bad[:3]])
+    return int((~same).sum()), ref
+
+
+@pytest.mark.parametrize("B,k,V,dtype,K,p", [(64, 5, 128256, "bf16", 50, 0.9), (16, 4, 32000, "bf16", 20, 1.0),
+                                             (24, 3, 1000, "f32", 64, 0.7), (32, 6, 40003, "f32", 7, 0.5),
+                                             (12, 16, 151936, "f32", 1, 1.0), (9, 2, 300, "bf16", 64, 1.0)])
+def test_filtered_matches_oracle(h, B, k, V, dtype, K, p):
+    w = W.make_random(name="filtered", B=B, k=k, V=V, dtype=dtype, seed=V + K, logit_sigma=3.0, draft_sigma=0.7,
+                      temperature=0.9, spike=4.0, spike_mode="position", greedy_rows=2)
+    mism, ref = _check(w, _run(h, w, [K] * B, [p] * B), [K] * B, [p] * B)
+    assert mism <= 1
+    assert (ref["row_status"] == 0).sum() >= B // 2
+
+
+def test_filtered_one_hot_and_mixed_filters(h):
+    rng = np.random.default_rng(4)
+    w = W.make_random(name="filtered1h", B=48, k=4, V=50000, dtype="bf16", seed=5, logit_sigma=2.5, draft_sigma=0.5,
+                      temperature=1.1, spike=6.0, spike_mode="position", greedy_rows=4)
+    K = rng.integers(1, 65, size=48)
+    P = rng.choice([1.0, 0.95, 0.8, 0.3], size=48).astype(np.float32)
+    assert _check(w, _run(h, w, K, P, onehot=True), K, P, onehot=True)[0] <= 1
+    assert _check(w, _run(h, w, K, P), K, P)[0] <= 1
+
+
+def test_filtered_many_uniforms(h):
+    """The benchmark logits, top_k 40 and top_p 0.95, 20 uniform sets."""
+    base = W.make_config(3)
+    rng = np.random.default_rng(6)
+    mism = 0
+    for r in range(20):
+        w = W.Workload(base.name, base.dtype, base.logits, base.q, base.x,
+                       rng.random(base.u.shape, dtype=np.float32), base.T)
+        mism += _check(w, _run(h, w, [40] * 64, [0.95] * 64), [40] * 64, [0.95] * 64)[0]
+    assert mism <= 1
+
+
+def test_filter_errors_and_bad_rows(h):
+    w = W.make_random(name="ferr", B=8, k=3, V=5000, dtype="f32", seed=9, logit_sigma=1.0, draft_sigma=0.5,
+                      temperature=1.0)
+    w.logits[5, 0, 17] = np.nan
+    w.logits[6, 1, 3] = np.inf
+    w.x[7, 0] = 5000
+    K = [0, 65, 10, 10, 10, 10, 10, 10]
+    P = np.array([1, 1, 0, 1.5, 1, 1, 1, 1], np.float32)
+    got = _run(h, w, K, P)
+    keep = np.array([0, 2, 3, 4, 5, 6, 7])
+    sub = W.Workload(w.name, w.dtype, w.logits[keep], w.q[keep], w.x[keep], w.u[keep], w.T[keep])
+    _, ref = _check(sub, {kk: v[keep] for kk, v in got.items()}, np.asarray(K)[keep], P[keep])
+    ref = {kk: np.insert(v, 1, 0, axis=0) for kk, v in ref.items()}
+    assert ref["row_status"][[0, 2, 3, 5, 7]].tolist() == [1024, 1024, 1024, 1, 2]
+    assert got["row_status"][1] == 1024  # beyond this path's 64 (the oracle's definition takes it)
