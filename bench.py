@@ -42,7 +42,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--graph-calls", type=int, default=100)
-    p.add_argument("--variant", choices=["sample", "onehot", "tree"], default="sample",
+    p.add_argument("--variant", choices=["sample", "onehot", "tree", "filtered"], default="sample",
                    help="onehot: the same workload verified as one-hot drafts (q = None); tree: greedy "
                         "verification of 16-node draft trees over the same vocabulary")
     return p.parse_args(argv)
@@ -277,6 +277,8 @@ def run_ours(args):
 
     if args.variant == "tree":
         return run_tree(args, sv, dev, rank, ws, local, hbm_peak, peak_src)
+    if args.variant == "filtered":
+        return run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src)
     w = W.make_config(CONFIG_INDEX, seed=57000 + CONFIG_INDEX + 1000 * rank)
     onehot = args.variant == "onehot"
     if onehot:
@@ -558,6 +560,136 @@ def run_tree(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out.values()),
                 "steps": e2e_steps, "path": "pinned copies + specv_verify_tree_greedy + copies back, per step"},
+        "gpu_launches": steps, "mean_num_accepted": float(np.mean(got["num_accepted"])), "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+FILTER_TOP_K, FILTER_TOP_P = 40, 0.95
+
+
+def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
+    """Sampled verification with top-k 40 / top-p 0.95 on the target rows,
+    on the benchmark workload (B=64, k=5, V=128256 bf16)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from speculative_decoding_verification_57_gb300 import workloads as W
+
+    w = W.make_config(CONFIG_INDEX, seed=57000 + CONFIG_INDEX + 1000 * rank)
+    B, k, V = w.B, w.k, w.V
+    tk = np.full(B, FILTER_TOP_K, np.int32)
+    tp = np.full(B, FILTER_TOP_P, np.float32)
+    h = sv.specv_create(local, max_batch=B, max_k=k, vocab=V)
+    L0 = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16)
+    host = dict(L=L0, q=torch.from_numpy(w.q), x=torch.from_numpy(w.x), u=torch.from_numpy(w.u),
+                T=torch.from_numpy(w.T), tk=torch.from_numpy(tk), tp=torch.from_numpy(tp))
+    sets = [{kk: v.to(dev) for kk, v in host.items()} for _ in range(N_SETS)]
+    outs = [dict(num_accepted=torch.empty(B, dtype=torch.int32, device=dev),
+                 out_tokens=torch.empty((B, k + 1), dtype=torch.int32, device=dev),
+                 row_status=torch.empty(B, dtype=torch.int32, device=dev)) for _ in range(N_SETS)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(i, s=None, o=None):
+        s = s or sets[i % N_SETS]
+        sv.specv_verify_sample_filtered(h, s["L"], s["q"], s["x"], s["u"], s["T"], s["tk"], s["tp"],
+                                        out=o or outs[i % N_SETS], stream=stream)
+
+    with torch.cuda.stream(stream):
+        call(0)
+    stream.synchronize()
+    got = {kk: v.cpu().numpy() for kk, v in outs[0].items()}
+    if np.any(got["row_status"] & sv.ST_ERROR_MASK):
+        raise RuntimeError("filtered verify reported data errors on the benchmark inputs")
+    # every logit once; q read at the kept entries of the stop row (at most top_k per row); the
+    # per-position q(x), x, u and T; top_k, top_p; outputs
+    rejected = got["num_accepted"] < k
+    alg = (B * (k + 1) * V * 2 + int(rejected.sum()) * FILTER_TOP_K * 4 + B * k * 12 + B * 12 + B * 8
+           + B * (k + 2) * 4)
+    G = max(1, min(args.graph_calls, args.steps))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        call(0)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(G):
+                call(i)
+    reps = max(1, args.steps // G)
+    steps = reps * G
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, (args.warmup + G - 1) // G)):
+            g.replay()
+    stream.synchronize()
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark("t0")
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    sampler.mark("t1")
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    ms_max = reduce_max(ev0.elapsed_time(ev1), ws, dev)
+    per_call_s = ms_max / 1e3 / steps
+    # end to end: pinned host inputs copied in, outputs read back, every step
+    pin = {kk: v.pin_memory() for kk, v in host.items()}
+    host_out = {kk: torch.empty_like(v, device="cpu").pin_memory() for kk, v in outs[0].items()}
+    e2e_steps = max(1, args.e2e_steps)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            for kk in pin:
+                sets[0][kk].copy_(pin[kk], non_blocking=True)
+            call(0)
+            for kk in host_out:
+                host_out[kk].copy_(outs[0][kk], non_blocking=True)
+        stream.synchronize()
+    e2e_s = reduce_max(time.perf_counter() - t0, ws, dev)
+    assert np.array_equal(host_out["num_accepted"].numpy(), got["num_accepted"])
+    if rank != 0:
+        return 0
+    cores = 1
+    sl = slice(0, 8)
+    oargs = (w.logits[sl], w.q[sl], w.x[sl], w.u[sl], w.T[sl], tk[sl], tp[sl])
+    oracle.verify_warped(*oargs)
+    n, t1 = 0, time.perf_counter()
+    while time.perf_counter() - t1 < 1.5 or n < 2:
+        oracle.verify_warped(*oargs)
+        n += 1
+    cpu_value = 8 * n / (time.perf_counter() - t1)
+    achieved = alg / per_call_s / 1e9
+    line = {
+        "metric": "filtered-verify rows/s", "value": B * steps * ws / (ms_max / 1e3), "unit": "rows/s",
+        "n_gpus": ws, "steps": steps, "warmup": args.warmup, "ms_per_step": ms_max / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD + f", top_k {FILTER_TOP_K}, top_p {FILTER_TOP_P}", "B": B, "k": k, "V": V,
+                   "global_batch": B * ws, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": f"rotating {N_SETS} input sets ({N_SETS * (w.logits.nbytes + w.q.nbytes) / 1e9:.2f} GB) "
+                         "> 2x L2",
+                   "launch": f"CUDA graph of {G} calls, {B * min(k + 1, 8)} CTAs in clusters of {min(k + 1, 8)}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
+                     "algorithmic_bytes_per_launch": alg},
+        "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} oracle calls x 8 rows, one thread"},
+        "e2e": {"value": B * e2e_steps * ws / e2e_s, "unit": "rows/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out.values()),
+                "steps": e2e_steps, "path": "pinned copies + specv_verify_sample_filtered + copies back, per step"},
         "gpu_launches": steps, "mean_num_accepted": float(np.mean(got["num_accepted"])), "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

@@ -307,13 +307,21 @@ specv_status specv_verify_sample_filtered(specv_handle h, specv_dtype logits_dty
     a.V = V;
     a.B = batch;
     a.k = k;
-    const size_t dyn = topk_dyn_smem(k);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (logits_dtype == SPECV_BF16)
-        verify_topk_kernel<true><<<batch, kThreads, dyn, s>>>(a);
-    else
-        verify_topk_kernel<false><<<batch, kThreads, dyn, s>>>(a);
-    const cudaError_t e = cudaGetLastError();
+    const int C = topk_cluster(k);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(batch) * C, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = topk_dyn_smem(k);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = logits_dtype == SPECV_BF16 ? cudaLaunchKernelEx(&cfg, verify_topk_kernel<true>, a)
+                                                     : cudaLaunchKernelEx(&cfg, verify_topk_kernel<false>, a);
     if (e != cudaSuccess) return cuda_fail(e, "verify_topk launch");
     h->launches.fetch_add(1, std::memory_order_relaxed);
     return SPECV_OK;

@@ -9,21 +9,29 @@
 // largest logits, the lower index first among equal logits; top-p keeps the
 // shortest prefix of those, in the same order, whose mass renormalised over
 // the K reaches top_p.  p' is exp((l - M) / T) on the kept set P,
-// renormalised.  The residual max(0, p' - q) and the bonus live on P, so no
-// second sweep of the vocabulary is needed: the stop position's draft
-// probabilities are gathered at the kept entries.
+// renormalised.  The residual max(0, p' - q) and the bonus live on P, so the
+// vocabulary is streamed once, to select, and no softmax over V is needed:
+// the stop position's draft probabilities are gathered at the kept entries.
 //
-// One CTA per sequence: a producer warp streams every position's logits
-// through a ring of shared-memory stages; each of the four consumer warps
-// keeps the best candidates of its share in a 128-entry buffer (an element
-// enters when it reaches the warp's threshold, the 64th best so far; a full
-// buffer is sorted and cut back to 64); at the end of a position each warp
-// leaves its best 64 in a per-position merge area.  After the stream the
-// warps merge positions in parallel (256 -> 64) and warp 0 walks the
+// One thread-block cluster of C = min(k + 1, 8) CTAs per sequence; CTA c
+// owns positions c, c + C, ...  In each CTA a producer warp streams the
+// owned rows through a ring of shared-memory stages (1-D bulk copies); each
+// of the four consumer warps keeps the best 64 entries of its share in
+// registers, as 64-bit keys (two a lane, in rank order).  An entry is
+// tested against a threshold first: a packed bf16x2 (or fp32) compare with
+// the largest 64th-best value any warp of the CTA has published, so after
+// the first tiles almost every tile passes with one compare per two logits.
+// Entries that pass collect in a per-warp buffer; a full buffer is sorted
+// with a register bitonic network and merged into the warp's 64 (half
+// cleaner + bitonic merge).  At the end of a position the four warp lists
+// merge in a tree and the result goes into the leader CTA's shared memory
+// over DSMEM; after a cluster barrier the leader's warp 0 walks the
 // positions with double-float weights.
 #pragma once
 #include <cfloat>
 #include <cstdint>
+
+#include <cuda_bf16.h>
 
 #include "exp2dd.cuh"
 #include "ptx.cuh"
@@ -31,112 +39,208 @@
 
 namespace specv {
 
-constexpr int kTopKMax = 64;                     // largest top_k this path takes
-constexpr int kCandCap = 128;                    // per-warp candidate buffer
-constexpr int kMergeLen = kConsumerWarps * kTopKMax;  // one position's warp lists
+constexpr int kTopKMax = 64;       // largest top_k this path takes
+constexpr int kTopkClusterMax = 8;  // CTAs per sequence
+constexpr int kTopkLocalMax = (kMaxK + 1 + kTopkClusterMax - 1) / kTopkClusterMax;  // positions per CTA
 
 struct Cand {
     float v;  // logit
     int i;    // vocabulary index
 };
 
-// Rank order: larger logit first, lower index first among equal logits.
-__device__ __forceinline__ bool cand_before(Cand a, Cand b) { return a.v > b.v || (a.v == b.v && a.i < b.i); }
+// Rank key: a larger key comes first.  The high word orders the logit (the
+// float bits made monotone), the low word is ~index, so among equal logits
+// the lower index comes first.  Key 0 is the padding entry: no logit (NaN
+// aside, which never enters) maps to it.
+using key_t = unsigned long long;
 
-__device__ __forceinline__ Cand cand_pad() { return Cand{-INFINITY, 0x7fffffff}; }
+__device__ __forceinline__ key_t make_key(float v, int i) {
+    const uint32_t f = v == 0.0f ? 0u : __float_as_uint(v);  // -0 ranks as +0
+    const uint32_t m = (f & 0x80000000u) ? ~f : (f | 0x80000000u);
+    return (static_cast<key_t>(m) << 32) | static_cast<uint32_t>(~i);
+}
 
-// Bitonic sort of n (a power of two) candidates in shared memory into rank
-// order, by one warp.
-__device__ __forceinline__ void warp_sort_cands(Cand* buf, int n, int lane) {
-    for (int size = 2; size <= n; size <<= 1) {
+__device__ __forceinline__ float key_value(key_t k) {
+    if (k == 0) return -INFINITY;
+    const uint32_t m = static_cast<uint32_t>(k >> 32);
+    return __uint_as_float((m & 0x80000000u) ? (m & 0x7fffffffu) : ~m);
+}
+
+__device__ __forceinline__ Cand key_cand(key_t k) {
+    if (k == 0) return Cand{-INFINITY, 0x7fffffff};
+    return Cand{key_value(k), static_cast<int>(~static_cast<uint32_t>(k))};
+}
+
+__device__ __forceinline__ key_t shfl_xor_key(key_t k, int m) {
+    const uint32_t lo = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(k), m);
+    const uint32_t hi = __shfl_xor_sync(0xffffffffu, static_cast<uint32_t>(k >> 32), m);
+    return (static_cast<key_t>(hi) << 32) | lo;
+}
+
+__device__ __forceinline__ key_t shfl_key(key_t k, int src) {
+    const uint32_t lo = __shfl_sync(0xffffffffu, static_cast<uint32_t>(k), src);
+    const uint32_t hi = __shfl_sync(0xffffffffu, static_cast<uint32_t>(k >> 32), src);
+    return (static_cast<key_t>(hi) << 32) | lo;
+}
+
+// One compare-exchange stage across lanes (lane ^ stride): the lane keeps
+// the larger key when it wants the first of the pair, else the smaller.
+__device__ __forceinline__ key_t cx_lanes(key_t a, int stride, bool want_first) {
+    const key_t o = shfl_xor_key(a, stride);
+    return ((o > a) == want_first) ? o : a;
+}
+
+// Bitonic sort of 64 keys held two a lane (element lane and lane + 32) into
+// descending order.
+__device__ __forceinline__ void sort64(key_t& a0, key_t& a1, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = lane; t < n / 2; t += 32) {
-                const int i = 2 * stride * (t / stride) + (t % stride);
-                const int j = i + stride;
-                const bool up = (i & size) == 0;  // this block ends in rank order
-                const Cand a = buf[i], b = buf[j];
-                if (up ? cand_before(b, a) : cand_before(a, b)) {
-                    buf[i] = b;
-                    buf[j] = a;
+            if (stride == 32) {
+                if (a1 > a0) {
+                    const key_t t = a0;
+                    a0 = a1;
+                    a1 = t;
                 }
+            } else {
+                const bool lower = (lane & stride) == 0;
+                a0 = cx_lanes(a0, stride, lower == ((lane & size) == 0));
+                a1 = cx_lanes(a1, stride, lower == (((lane + 32) & size) == 0));
             }
-            __syncwarp();
         }
     }
 }
 
-// Sort the warp's buffer, keep the best 64 and raise the threshold to the
-// 64th (while fewer than 64 are known every element qualifies).
-__device__ __forceinline__ void warp_compact(Cand* wb, int& cnt, float& thr, int lane) {
-    for (int t = cnt + lane; t < kCandCap; t += 32) wb[t] = cand_pad();
-    __syncwarp();
-    warp_sort_cands(wb, kCandCap, lane);
-    if (cnt >= kTopKMax) {
-        cnt = kTopKMax;
-        thr = wb[kTopKMax - 1].v;
+// a = the 64 largest of a and b, both descending, in descending order: the
+// half cleaner of a ++ reverse(b), then a bitonic merge.
+__device__ __forceinline__ void merge64(key_t& a0, key_t& a1, key_t b0, key_t b1, int lane) {
+    const key_t r0 = shfl_xor_key(b1, 31);  // b[63 - lane]
+    const key_t r1 = shfl_xor_key(b0, 31);  // b[31 - lane]
+    a0 = a0 > r0 ? a0 : r0;
+    a1 = a1 > r1 ? a1 : r1;
+    if (a1 > a0) {
+        const key_t t = a0;
+        a0 = a1;
+        a1 = t;
     }
-}
-
-// Add each lane's pending elements (bit e of pend: element e, get(e) gives
-// it) that reach the threshold to the warp's buffer, one per lane a round.
-template <typename Get>
-__device__ __forceinline__ void warp_insert(Cand* wb, int& cnt, float& thr, uint32_t pend, Get get, int lane) {
-    const unsigned full = 0xffffffffu;
-    for (;;) {
-        const bool has = pend != 0;
-        if (!__any_sync(full, has)) break;
-        const int e = has ? __ffs(pend) - 1 : 0;
-        const Cand c = has ? get(e) : cand_pad();
-        if (has) pend &= pend - 1;
-        bool take = has && !(c.v < thr);  // ties enter; the sort orders them
-        unsigned bal = __ballot_sync(full, take);
-        if (cnt + __popc(bal) > kCandCap) {
-            warp_compact(wb, cnt, thr, lane);
-            take = take && !(c.v < thr);
-            bal = __ballot_sync(full, take);
-        }
-        if (take) wb[cnt + __popc(bal & lanemask_lt())] = c;
-        cnt += __popc(bal);
-        __syncwarp();
+#pragma unroll
+    for (int stride = 16; stride > 0; stride >>= 1) {
+        const bool lower = (lane & stride) == 0;
+        a0 = cx_lanes(a0, stride, lower);
+        a1 = cx_lanes(a1, stride, lower);
     }
 }
 
 struct alignas(16) TopkSmem {
     unsigned long long full[kStages];
     unsigned long long empty[kStages];
-    int tstart[kMaxK + 2];  // first tile of each position
-    int head[kMaxK + 1];    // unaligned leading elements of each row
-    int nbytes[kMaxK + 1];  // bytes of the 16-byte aligned interior
-    int bad[kMaxK + 1];     // bit 0: a NaN was seen at this position; bit 1: a +inf
-    int timeout;
-    float2 exp2tab[128];
+    key_t wb[kConsumerWarps][kTopKMax];  // per-warp candidate buffers; the walk's scratch
+    key_t ms[3][kTopKMax];               // lists on their way through the end-of-position merge
+    int tstart[kTopkLocalMax + 1];       // first tile of each owned position
+    int head[kTopkLocalMax];             // unaligned leading elements of each owned row
+    int nbytes[kTopkLocalMax];           // bytes of the 16-byte aligned interior
+    float wthr[kTopkLocalMax][kConsumerWarps];  // published 64th-best values (inclusive bounds)
+    int lbad[kTopkLocalMax];             // bit 0: a NaN in this CTA's share of an owned position
+    int ltimeout;
+    int bad[kMaxK + 1];                  // leader: bit 0 NaN, bit 1 the owner timed out
     int xs[kMaxK + 1];
+    float2 exp2tab[128];
 };
 
-// Dynamic shared memory of the top-k kernel: the ring, the per-position merge
-// areas [k+1][kMergeLen], the per-warp candidate buffers [4][kCandCap].
+// Dynamic shared memory: the ring, then the leader's lists [k+1][64].
 inline size_t topk_dyn_smem(int k) {
-    return static_cast<size_t>(kRingBytes) + static_cast<size_t>(k + 1) * kMergeLen * sizeof(Cand) +
-           static_cast<size_t>(kConsumerWarps) * kCandCap * sizeof(Cand);
+    return static_cast<size_t>(kRingBytes) + static_cast<size_t>(k + 1) * kTopKMax * sizeof(key_t);
+}
+
+inline int topk_cluster(int k) { return k + 1 < kTopkClusterMax ? k + 1 : kTopkClusterMax; }
+
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t geu_bf16x2(uint32_t w, __nv_bfloat162 t) {
+    return __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w), t);
+}
+
+// A consumer warp's selection state for one position.
+struct WarpTop {
+    key_t c0, c1;  // the best 64 so far, ranks lane and lane + 32 (0: none)
+    key_t t63;     // rank 63: an entry must beat it to enter
+    int cnt;       // entries waiting in the warp's buffer
+};
+
+__device__ __forceinline__ void warp_flush(WarpTop& w, key_t* wb, int lane) {
+    __syncwarp();
+    key_t s0 = lane < w.cnt ? wb[lane] : 0;
+    key_t s1 = lane + 32 < w.cnt ? wb[lane + 32] : 0;
+    __syncwarp();
+    sort64(s0, s1, lane);
+    merge64(w.c0, w.c1, s0, s1, lane);
+    w.t63 = shfl_key(w.c1, 31);
+    w.cnt = 0;
+}
+
+// Offer each lane's pending elements (bit e of pend; get(e, v, idx) reads
+// element e) to the warp's 64, one element a lane per round.  A NaN never
+// enters; it sets nan.
+template <typename Get>
+__device__ __forceinline__ void warp_take(WarpTop& w, key_t* wb, uint32_t pend, Get get, int lane, int& nan) {
+    const unsigned full = 0xffffffffu;
+    for (;;) {
+        const bool has = pend != 0;
+        if (!__any_sync(full, has)) break;
+        key_t key = 0;
+        bool take = false;
+        if (has) {
+            const int e = __ffs(pend) - 1;
+            pend &= pend - 1;
+            float v;
+            int idx;
+            get(e, v, idx);
+            if (v != v) {
+                nan = 1;
+            } else {
+                key = make_key(v, idx);
+                take = key > w.t63;
+            }
+        }
+        __syncwarp();
+        unsigned bal = __ballot_sync(full, take);
+        if (w.cnt + __popc(bal) > kTopKMax) {
+            warp_flush(w, wb, lane);
+            take = take && key > w.t63;
+            bal = __ballot_sync(full, take);
+        }
+        if (take) wb[w.cnt + __popc(bal & lanemask_lt())] = key;
+        w.cnt += __popc(bal);
+        __syncwarp();
+    }
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kThreads, 1) verify_topk_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ __align__(16) TopkSmem sh;
     constexpr int esz = BF16 ? 2 : 4;
     constexpr int kPer = kTileBytes / 16 / kConsumers;  // 16-byte chunks per consumer thread and tile
     constexpr int kEpc = 16 / esz;                       // elements per chunk
+    const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const bool producer = warp == kConsumerWarps;
-    const int b = blockIdx.x;
+    const int C = static_cast<int>(cluster_size());
+    const int crank = static_cast<int>(cluster_rank());
+    const int b = static_cast<int>(blockIdx.x) / C;
     const int k = a.k;
     const long long V = a.V;
     const int n = static_cast<int>(V);
+    const int P = (k - crank) / C + 1;  // owned positions crank + C p, p < P
     const unsigned char* lg = reinterpret_cast<const unsigned char*>(a.logits);
     unsigned char* ring = dyn_smem;
-    Cand* merge = reinterpret_cast<Cand*>(dyn_smem + kRingBytes);             // [k+1][kMergeLen]
-    Cand* wbuf = merge + static_cast<size_t>(k + 1) * kMergeLen + warp * kCandCap;  // this warp's buffer
+    key_t* lists = reinterpret_cast<key_t*>(dyn_smem + kRingBytes);  // [k+1][64]; the leader's are read
 
     const float T = a.temp ? __ldg(a.temp + b) : 0.0f;
     const bool greedy = T == 0.0f;
@@ -144,170 +248,229 @@ __global__ void __launch_bounds__(kThreads, 1) verify_topk_kernel(const VerifyAr
     const int K = a.top_k ? __ldg(a.top_k + b) : kTopKMax;
     const float top_p = a.top_p ? __ldg(a.top_p + b) : 1.0f;
     const bool f_ok = greedy || (K >= 1 && K <= kTopKMax && top_p > 0.0f && top_p <= 1.0f);
+    const bool run = t_ok && f_ok;
 
     // ---------------------------------------------------------------- setup
     if (tid < 128) sh.exp2tab[tid] = g_exp2_table[tid];
-    if (tid <= k) {
-        sh.bad[tid] = 0;
-        sh.xs[tid] = tid < k ? __ldg(a.x + static_cast<long long>(b) * k + tid) : -1;
-    }
-    auto issue = [&](int tt, int it) {
-        int i = 0;
-        while (sh.tstart[i + 1] <= tt) ++i;
-        const int off = (tt - sh.tstart[i]) * kTileBytes;
-        const int bytes = min(kTileBytes, sh.nbytes[i] - off);
-        const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + sh.head[i];
-        const int slot = it % kStages;
+    if (tid <= k) sh.xs[tid] = tid < k ? __ldg(a.x + static_cast<long long>(b) * k + tid) : -1;
+    if (tid < kTopkLocalMax * kConsumerWarps) sh.wthr[tid / kConsumerWarps][tid % kConsumerWarps] = -INFINITY;
+    if (tid < kTopkLocalMax) sh.lbad[tid] = 0;
+    auto issue = [&](int tt) {
+        int p = 0;
+        while (sh.tstart[p + 1] <= tt) ++p;
+        const int i = crank + C * p;
+        const int off = (tt - sh.tstart[p]) * kTileBytes;
+        const int bytes = min(kTileBytes, sh.nbytes[p] - off);
+        const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + sh.head[p];
+        const int slot = tt % kStages;
         const uint32_t bar = smem_u32(&sh.full[slot]);
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>(bytes));
         bulk_g2s(smem_u32(ring + slot * kTileBytes), lg + e0 * esz + off, static_cast<uint32_t>(bytes), bar);
     };
-    int it_prod = 0;
+    int issued = 0;
     if (producer && lane == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
             mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
         }
-        sh.timeout = 0;
+        sh.ltimeout = 0;
         fence_mbar_init();
         fence_proxy_async_smem();
         int acc = 0;
-        for (int i = 0; i <= k; ++i) {
-            const uintptr_t addr = reinterpret_cast<uintptr_t>(lg + (static_cast<long long>(b) * (k + 1) + i) * V * esz);
+        for (int p = 0; p < P; ++p) {
+            const int i = crank + C * p;
+            const uintptr_t addr =
+                reinterpret_cast<uintptr_t>(lg + (static_cast<long long>(b) * (k + 1) + i) * V * esz);
             int h = static_cast<int>(((16 - (addr & 15)) & 15) / esz);
             if (h > n) h = n;
             const int nb = ((n - h) * esz) & ~15;
-            sh.head[i] = h;
-            sh.nbytes[i] = nb;
-            sh.tstart[i] = acc;
-            acc += (nb + kTileBytes - 1) / kTileBytes;
+            sh.head[p] = h;
+            sh.nbytes[p] = nb;
+            sh.tstart[p] = acc;
+            if (run) acc += (nb + kTileBytes - 1) / kTileBytes;
         }
-        sh.tstart[k + 1] = acc;
-        if (t_ok && f_ok)
-            for (; it_prod < min(kStages, acc); ++it_prod) issue(it_prod, it_prod);
+        sh.tstart[P] = acc;
+        for (; issued < min(kStages, acc); ++issued) issue(issued);
     }
     __syncthreads();
-    const int total = (t_ok && f_ok) ? sh.tstart[k + 1] : 0;
+    cluster_arrive();  // the matching wait comes before the first store into the leader
+    const int total = sh.tstart[P];
 
     // ---------------------------------------------------------------- stream
     if (producer) {
         if (lane == 0) {
-            for (int tt = it_prod; tt < total; ++tt) {
-                const int slot = tt % kStages;
-                if (sh.timeout || (tt >= kStages && !mbar_wait_bounded(smem_u32(&sh.empty[slot]),
-                                                                        ((tt / kStages) & 1) ^ 1, kWaitPolls))) {
-                    atomicOr(&sh.timeout, 1);
+            for (; issued < total; ++issued) {
+                const int slot = issued % kStages;
+                if (sh.ltimeout || !mbar_wait_bounded(smem_u32(&sh.empty[slot]), ((issued / kStages) & 1) ^ 1,
+                                                      kWaitPolls)) {
+                    atomicOr(&sh.ltimeout, 1);
                     break;
                 }
-                issue(tt, tt);
+                issue(issued);
+            }
+            if (sh.ltimeout) {
+                // no copy may still be writing this CTA's shared memory when it exits
+                for (int s = 0; s < kStages && s < issued; ++s) {
+                    const int last = s + kStages * ((issued - 1 - s) / kStages);
+                    mbar_wait_bounded(smem_u32(&sh.full[s]), (last / kStages) & 1, kWaitPolls);
+                }
             }
         }
         __syncwarp();
+        cluster_wait();
     } else {
         int it = 0;
-        for (int i = 0; i <= k && t_ok && f_ok; ++i) {
-            int cnt = 0;
-            float thr = -INFINITY;
+        key_t* wb = sh.wb[warp];
+        for (int p = 0; p < P; ++p) {
+            const int i = crank + C * p;
+            WarpTop w;
+            w.c0 = w.c1 = w.t63 = 0;
+            w.cnt = 0;
+            int nan = 0;
+            bool fresh = true;
             const long long row_e0 = (static_cast<long long>(b) * (k + 1) + i) * V;
-            const int h = sh.head[i];
-            const int interior = sh.nbytes[i] / esz;
-            const int ntiles = sh.tstart[i + 1] - sh.tstart[i];
-            // unaligned head and tail: thread 0 reads them with plain loads
+            const int h = sh.head[p];
+            const int interior = sh.nbytes[p] / esz;
+            const int ntiles = sh.tstart[p + 1] - sh.tstart[p];
+            // unaligned head and tail: warp 0 reads them with plain loads, a lane an element
             auto scalar_part = [&](int lo, int hi) {
-                uint32_t pend = 0;
-                int bad = 0;
-                if (tid == 0)
-                    for (int e = lo; e < hi; ++e) {
-                        const float l = load_logit(a.logits, row_e0 + e, BF16);
-                        bad |= (l != l ? 1 : 0) | (l == INFINITY ? 2 : 0);
-                        pend |= 1u << (e - lo);
-                    }
-                if (bad) atomicOr(&sh.bad[i], bad);
-                __syncwarp();
-                if (warp == 0)
-                    warp_insert(wbuf, cnt, thr, pend,
-                                [&](int e) { return Cand{load_logit(a.logits, row_e0 + lo + e, BF16), lo + e}; }, lane);
+                warp_take(w, wb, lane < hi - lo ? 1u : 0u, [&](int, float& v, int& idx) {
+                    idx = lo + lane;
+                    v = load_logit(a.logits, row_e0 + idx, BF16);
+                }, lane, nan);
             };
-            if (warp == 0 && h > 0) scalar_part(0, h);
+            if (run && warp == 0 && h > 0) scalar_part(0, h);
             for (int lt = 0; lt < ntiles; ++lt, ++it) {
                 const int slot = it % kStages;
-                const bool ok = __all_sync(0xffffffffu, !sh.timeout && mbar_wait_bounded(smem_u32(&sh.full[slot]),
-                                                                                          (it / kStages) & 1,
-                                                                                          kWaitPolls));
+                const bool ok = __all_sync(full, !sh.ltimeout && mbar_wait_bounded(smem_u32(&sh.full[slot]),
+                                                                                   (it / kStages) & 1, kWaitPolls));
                 if (!ok) {
-                    if (lane == 0) atomicOr(&sh.timeout, 1);
-                    break;
+                    if (lane == 0) atomicOr(&sh.ltimeout, 1);
+                    continue;  // the rest of the stream is skipped, the barrier sequence kept
                 }
-                const int bytes = min(kTileBytes, sh.nbytes[i] - lt * kTileBytes);
+                const int bytes = min(kTileBytes, sh.nbytes[p] - lt * kTileBytes);
                 const int nch = bytes >> 4;
-                const unsigned char* tile = ring + slot * kTileBytes;
+                const uint32_t tile = smem_u32(ring + slot * kTileBytes);
                 const int tile_e = h + lt * (kTileBytes / esz);  // row index of the tile's first element
-                // this lane's elements: chunk r = tid + 128 r, element q of the chunk -> bit r * kEpc + q
-                float mx = -INFINITY, mx2 = -INFINITY;
-                int bad = 0;
-                uint32_t ge = 0;
+                uint4 d[kPer];
 #pragma unroll
                 for (int r = 0; r < kPer; ++r) {
                     const int ch = tid + r * kConsumers;
-                    if (ch < nch) {
+                    d[r] = ch < nch ? ld_shared_v4(tile + ch * 16) : make_uint4(0u, 0u, 0u, 0u);
+                }
+                // the entry bound: the best 64th value any warp has published
+                float tau = fmaxf(key_value(w.t63), fmaxf(fmaxf(sh.wthr[p][0], sh.wthr[p][1]),
+                                                          fmaxf(sh.wthr[p][2], sh.wthr[p][3])));
+                if (fresh) {
+                    // a position's first tile: at least 64 of the warp's elements reach the
+                    // smallest second-largest of the 32 lanes (a NaN counts as -inf here)
+                    float mx = -INFINITY, mx2 = -INFINITY;
 #pragma unroll
-                        for (int q = 0; q < kEpc; ++q) {
-                            const float l = BF16 ? bf16_lo(reinterpret_cast<const uint16_t*>(tile + ch * 16)[q])
-                                                 : reinterpret_cast<const float*>(tile + ch * 16)[q];
-                            bad |= (l != l ? 1 : 0) | (l == INFINITY ? 2 : 0);
-                            if (l > mx) {
-                                mx2 = mx;
-                                mx = l;
-                            } else if (l > mx2) {
-                                mx2 = l;
+                    for (int r = 0; r < kPer; ++r) {
+                        if (tid + r * kConsumers < nch) {
+                            const uint32_t wd[4] = {d[r].x, d[r].y, d[r].z, d[r].w};
+#pragma unroll
+                            for (int q = 0; q < kEpc; ++q) {
+                                float l;
+                                if constexpr (BF16)
+                                    l = (q & 1) ? bf16_hi(wd[q >> 1]) : bf16_lo(wd[q >> 1]);
+                                else
+                                    l = __uint_as_float(wd[q & 3]);
+                                l = l == l ? l : -INFINITY;
+                                mx2 = fmaxf(mx2, fminf(mx, l));
+                                mx = fmaxf(mx, l);
                             }
-                            ge |= (l >= thr ? 1u : 0u) << (r * kEpc + q);
+                        }
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) mx2 = fminf(mx2, __shfl_xor_sync(full, mx2, off));
+                    tau = fmaxf(tau, mx2);
+                    if (lane == 0) sh.wthr[p][warp] = fmaxf(sh.wthr[p][warp], mx2);
+                    fresh = false;
+                }
+                // elements that may enter (NaN included: it is caught and flagged in warp_take)
+                uint32_t pend = 0;
+                if constexpr (BF16) {
+                    const __nv_bfloat162 t2 = __float2bfloat162_rn(tau);
+                    uint32_t m[kPer][4];
+                    uint32_t any = 0;
+#pragma unroll
+                    for (int r = 0; r < kPer; ++r) {
+                        const bool v = tid + r * kConsumers < nch;
+                        m[r][0] = v ? geu_bf16x2(d[r].x, t2) : 0u;
+                        m[r][1] = v ? geu_bf16x2(d[r].y, t2) : 0u;
+                        m[r][2] = v ? geu_bf16x2(d[r].z, t2) : 0u;
+                        m[r][3] = v ? geu_bf16x2(d[r].w, t2) : 0u;
+                        any |= m[r][0] | m[r][1] | m[r][2] | m[r][3];
+                    }
+                    if (any) {
+#pragma unroll
+                        for (int r = 0; r < kPer; ++r)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                pend |= ((m[r][q] & 1u) | ((m[r][q] >> 15) & 2u)) << (r * 8 + q * 2);
+                    }
+                } else {
+#pragma unroll
+                    for (int r = 0; r < kPer; ++r) {
+                        if (tid + r * kConsumers < nch) {
+                            const uint32_t wd[4] = {d[r].x, d[r].y, d[r].z, d[r].w};
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                pend |= (__uint_as_float(wd[q]) < tau ? 0u : 1u) << (r * 4 + q);
                         }
                     }
                 }
-                bad = static_cast<int>(__reduce_or_sync(0xffffffffu, static_cast<unsigned>(bad)));
-                if (bad && lane == 0) atomicOr(&sh.bad[i], bad);
-                if (thr == -INFINITY) {
-                    // a position's first tile: at least 64 of its elements reach
-                    // the smallest second-largest of the 32 lanes
-                    float t0 = mx2;
-                    for (int off = 16; off > 0; off >>= 1) t0 = fminf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
-                    thr = t0;
+                if (__any_sync(full, pend != 0)) {
+                    warp_take(w, wb, pend, [&](int e, float& v, int& idx) {
+                        const int r = e / kEpc, q = e % kEpc, ch = tid + r * kConsumers;
+                        v = BF16 ? __uint_as_float(static_cast<uint32_t>(ld_shared_u16(tile + ch * 16 + q * 2)) << 16)
+                                 : ld_shared_f32(tile + ch * 16 + q * 4);
+                        idx = tile_e + ch * kEpc + q;
+                    }, lane, nan);
+                    if (lane == 0 && w.t63 != 0) sh.wthr[p][warp] = fmaxf(sh.wthr[p][warp], key_value(w.t63));
                 }
-                // elements below the (possibly raised) threshold drop out in warp_insert
-                warp_insert(wbuf, cnt, thr, ge, [&](int e) {
-                    const int r = e / kEpc, q = e % kEpc, ch = tid + r * kConsumers;
-                    const float l = BF16 ? bf16_lo(reinterpret_cast<const uint16_t*>(tile + ch * 16)[q])
-                                         : reinterpret_cast<const float*>(tile + ch * 16)[q];
-                    return Cand{l, tile_e + ch * kEpc + q};
-                }, lane);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.empty[slot]));
             }
-            if (warp == 0 && h + interior < n) scalar_part(h + interior, n);
-            // the warp's best 64 of this position go to the merge area
-            warp_compact(wbuf, cnt, thr, lane);
-            Cand* dst = merge + static_cast<size_t>(i) * kMergeLen + warp * kTopKMax;
-            for (int t = lane; t < kTopKMax; t += 32) dst[t] = t < cnt ? wbuf[t] : cand_pad();
-            __syncwarp();
+            if (run && warp == 0 && h + interior < n) scalar_part(h + interior, n);
+            if (w.cnt > 0) warp_flush(w, wb, lane);
+            if (__any_sync(full, nan) && lane == 0) atomicOr(&sh.lbad[p], 1);
+            // the four warp lists merge in a tree: (1 -> 0, 3 -> 2), then 2 -> 0
+            if (warp == 1 || warp == 3) {
+                sh.ms[warp >> 1][lane] = w.c0;
+                sh.ms[warp >> 1][lane + 32] = w.c1;
+            }
+            consumers_sync();
+            if (warp == 0 || warp == 2) merge64(w.c0, w.c1, sh.ms[warp >> 1][lane], sh.ms[warp >> 1][lane + 32], lane);
+            if (warp == 2) {
+                sh.ms[2][lane] = w.c0;
+                sh.ms[2][lane + 32] = w.c1;
+            }
+            consumers_sync();
+            if (warp == 0) {
+                merge64(w.c0, w.c1, sh.ms[2][lane], sh.ms[2][lane + 32], lane);
+                if (p == 0) cluster_wait();  // the leader has started: its shared memory may be written
+                const uint32_t dst = map_rank(smem_u32(lists + static_cast<size_t>(i) * kTopKMax), 0);
+                st_cluster_v2(dst + lane * 8, static_cast<uint32_t>(w.c0), static_cast<uint32_t>(w.c0 >> 32));
+                st_cluster_v2(dst + (lane + 32) * 8, static_cast<uint32_t>(w.c1), static_cast<uint32_t>(w.c1 >> 32));
+                if (lane == 0)
+                    st_cluster_u32(map_rank(smem_u32(&sh.bad[i]), 0),
+                                   static_cast<uint32_t>(sh.lbad[p] | (sh.ltimeout ? 2 : 0)));
+            }
         }
+        if (warp != 0) cluster_wait();
     }
-    __syncthreads();
-
-    // ---------------------------------------------------------------- merge
-    // each position's four warp lists (256) sorted: its best 64 come first
-    if (!producer && t_ok && f_ok && !sh.timeout)
-        for (int i = warp; i <= k; i += kConsumerWarps) warp_sort_cands(merge + static_cast<size_t>(i) * kMergeLen,
-                                                                          kMergeLen, lane);
-    __syncthreads();
+    cluster_sync();  // every list and flag is in the leader
+    if (crank != 0 || warp != 0) return;
 
     // ---------------------------------------------------------------- walk
-    if (warp != 0) return;
-    int st = !t_ok ? ST_TEMP : (!f_ok ? ST_FILTER : (sh.timeout ? ST_TIMEOUT : 0));
+    const bool timed_out = __any_sync(full, lane <= k && (sh.bad[lane] & 2));
+    int st = !t_ok ? ST_TEMP : (!f_ok ? ST_FILTER : (timed_out ? ST_TIMEOUT : 0));
     int j = 0, token = -1;
     if (!st && greedy) {
         for (int i = 0; i <= k; ++i) {
-            const int A = merge[static_cast<size_t>(i) * kMergeLen].i;
+            const int A = key_cand(lists[static_cast<size_t>(i) * kTopKMax]).i;
             const int x = i < k ? sh.xs[i] : -1;
             int pst = (sh.bad[i] & 1) ? ST_NONFINITE : 0;  // a NaN: the argmax is undefined
             if (i < k && (x < 0 || x >= V)) pst |= ST_TOKEN;
@@ -329,16 +492,16 @@ __global__ void __launch_bounds__(kThreads, 1) verify_topk_kernel(const VerifyAr
         rc.ch = c2.hi;
         rc.cl = c2.lo;
         // lane r holds ranks r and r + 32 of the current position
-        Cand c0 = cand_pad(), c1 = cand_pad();
+        Cand c0 = key_cand(0), c1 = key_cand(0);
         df e0 = df_make(0.0f), e1 = df_make(0.0f), SP = df_make(0.0f);
         int np = 0;
         for (int i = 0; i <= k; ++i) {
-            const Cand* m = merge + static_cast<size_t>(i) * kMergeLen;
-            c0 = m[lane];
-            c1 = m[lane + 32];
-            rc.M = m[0].v;
-            // this position's errors, in the walk's order of checks
-            int pst = (sh.bad[i] || rc.M == -INFINITY) ? ST_NONFINITE : 0;  // NaN, +inf, or all -inf
+            const key_t* m = lists + static_cast<size_t>(i) * kTopKMax;
+            c0 = key_cand(m[lane]);
+            c1 = key_cand(m[lane + 32]);
+            rc.M = key_value(m[0]);
+            // this position's errors, in the walk's order of checks (+inf: the maximum is infinite)
+            int pst = ((sh.bad[i] & 1) || !(rc.M > -INFINITY && rc.M < INFINITY)) ? ST_NONFINITE : 0;
             const int x = i < k ? sh.xs[i] : -1;
             float u0 = 0.0f, qx = 0.0f;
             if (i < k) {
@@ -366,8 +529,8 @@ __global__ void __launch_bounds__(kThreads, 1) verify_topk_kernel(const VerifyAr
             np = K;
             if (top_p < 1.0f) {
                 const df target = df_mul_f(SK, top_p);
-                const unsigned h0 = __ballot_sync(0xffffffffu, lane < K && !df_less(s0, target));
-                const unsigned h1 = __ballot_sync(0xffffffffu, lane + 32 < K && !df_less(s1, target));
+                const unsigned h0 = __ballot_sync(full, lane < K && !df_less(s0, target));
+                const unsigned h1 = __ballot_sync(full, lane + 32 < K && !df_less(s1, target));
                 np = h0 ? __ffs(h0) : (h1 ? 32 + __ffs(h1) : K);
             }
             SP = np <= 32 ? df_shfl(s0, np - 1) : df_shfl(s1, np - 33);
@@ -377,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_topk_kernel(const VerifyAr
             }
             // p'(x): x among the kept ranks
             const bool h0 = lane < np && c0.i == x, h1 = lane + 32 < np && c1.i == x;
-            const unsigned b0 = __ballot_sync(0xffffffffu, h0), b1 = __ballot_sync(0xffffffffu, h1);
+            const unsigned b0 = __ballot_sync(full, h0), b1 = __ballot_sync(full, h1);
             float px = 0.0f;
             if (b0 || b1) {
                 const df ex = b0 ? df_shfl(e0, __ffs(b0) - 1) : df_shfl(e1, __ffs(b1) - 1);
@@ -404,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_topk_kernel(const VerifyAr
                 const float q0 = v0 ? (qrow ? __ldg(qrow + c0.i) : (c0.i == xj ? 1.0f : 0.0f)) : 0.0f;
                 const float q1 = v1 ? (qrow ? __ldg(qrow + c1.i) : (c1.i == xj ? 1.0f : 0.0f)) : 0.0f;
                 const bool qb = !(q0 >= 0.0f && q0 <= FLT_MAX) || !(q1 >= 0.0f && q1 <= FLT_MAX);
-                if (__any_sync(0xffffffffu, qb)) st |= ST_QBAD;
+                if (__any_sync(full, qb)) st |= ST_QBAD;
                 const df r0 = minus_sq(e0, SP, q0), r1 = minus_sq(e1, SP, q1);
                 w0 = (v0 && r0.hi + r0.lo > 0.0f) ? r0 : df_make(0.0f);
                 w1 = (v1 && r1.hi + r1.lo > 0.0f) ? r1 : df_make(0.0f);
@@ -419,13 +582,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_topk_kernel(const VerifyAr
                 // the kept entries in vocabulary order (rank of each index among them)
                 int o0 = 0, o1 = 0;
                 for (int s2 = 0; s2 < np; ++s2) {
-                    const int is = s2 < 32 ? __shfl_sync(0xffffffffu, c0.i, s2) : __shfl_sync(0xffffffffu, c1.i, s2 - 32);
+                    const int is = s2 < 32 ? __shfl_sync(full, c0.i, s2) : __shfl_sync(full, c1.i, s2 - 32);
                     o0 += is < c0.i ? 1 : 0;
                     o1 += is < c1.i ? 1 : 0;
                 }
-                // scratch: this warp's candidate buffer holds (weight hi, index) then (weight lo, index)
-                Cand* ohi = wbuf;
-                Cand* olo = wbuf + kTopKMax;
+                // scratch (the candidate buffers, free now): (weight hi, index) then (weight lo, index)
+                Cand* ohi = reinterpret_cast<Cand*>(sh.wb[0]);
+                Cand* olo = reinterpret_cast<Cand*>(sh.wb[1]);
                 for (int t = lane; t < kTopKMax; t += 32) {
                     ohi[t] = Cand{0.0f, 0x7fffffff};
                     olo[t] = Cand{0.0f, 0x7fffffff};
@@ -446,15 +609,15 @@ __global__ void __launch_bounds__(kThreads, 1) verify_topk_kernel(const VerifyAr
                 const df W = df_shfl(p1, 31);
                 const df target = df_mul_f(W, u1);
                 const bool pos0 = a0.hi + a0.lo > 0.0f, pos1 = a1.hi + a1.lo > 0.0f;
-                const unsigned g0 = __ballot_sync(0xffffffffu, pos0 && df_less(target, p0));
-                const unsigned g1 = __ballot_sync(0xffffffffu, pos1 && df_less(target, p1));
+                const unsigned g0 = __ballot_sync(full, pos0 && df_less(target, p0));
+                const unsigned g1 = __ballot_sync(full, pos1 && df_less(target, p1));
                 int slot = -1;
                 if (g0)
                     slot = __ffs(g0) - 1;
                 else if (g1)
                     slot = 32 + __ffs(g1) - 1;
                 else {  // only through rounding at the top edge: the last positive entry
-                    const unsigned q0b = __ballot_sync(0xffffffffu, pos0), q1b = __ballot_sync(0xffffffffu, pos1);
+                    const unsigned q0b = __ballot_sync(full, pos0), q1b = __ballot_sync(full, pos1);
                     slot = q1b ? 32 + 31 - __clz(q1b) : (q0b ? 31 - __clz(q0b) : 0);
                 }
                 token = ohi[slot].i;

@@ -93,3 +93,26 @@ def test_filter_errors_and_bad_rows(h):
     ref = {kk: np.insert(v, 1, 0, axis=0) for kk, v in ref.items()}
     assert ref["row_status"][[0, 2, 3, 5, 7]].tolist() == [1024, 1024, 1024, 1, 2]
     assert got["row_status"][1] == 1024  # beyond this path's 64 (the oracle's definition takes it)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_filtered_ties_and_degenerate_rows(h, dtype):
+    """Equal logits (the lower index first), -0 beside +0, an all -inf
+    position, +inf, and many positions (k = 31, several per CTA)."""
+    B, k, V = 10, 31, 3001
+    w = W.make_random(name="fties", B=B, k=k, V=V, dtype=dtype, seed=77, logit_sigma=2.0, draft_sigma=0.6,
+                      temperature=1.0, greedy_rows=2)
+    L = W.bf16_bits_to_f32(w.logits) if dtype == "bf16" else w.logits.copy()
+    rng = np.random.default_rng(78)
+    L[0] = 0.0                                    # flat: every entry ties
+    L[1] = np.round(L[1] * 2.0) / 2.0             # few distinct values
+    L[2] = np.where(rng.random(L[2].shape) < 0.5, -0.0, 0.0)
+    L[2, :, 5] = 0.25
+    L[3, 0] = -np.inf                              # an all -inf position
+    L[4, 0, 17] = np.inf
+    L[5] = np.round(L[5]) - 3.0                    # ties around the 64th entry
+    w.x[0] = rng.integers(0, 64, size=k)           # inside the flat row's kept set
+    logits = W.f32_to_bf16_bits(L.astype(np.float32)) if dtype == "bf16" else L.astype(np.float32)
+    w = W.Workload(w.name, w.dtype, logits, w.q, w.x, w.u, w.T)
+    for K, p in [(64, 1.0), (13, 0.8), (1, 1.0)]:
+        _check(w, _run(h, w, [K] * B, [p] * B), [K] * B, [p] * B)
