@@ -118,10 +118,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def measured_traffic():
-    """DRAM traffic per launch of the verify kernel from the committed ncu
-    summary, if it was taken on the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", "verify_cluster_kernel_B64_k5_V128256_bf16.json")
+def measured_traffic(name="verify_cluster_kernel_B64_k5_V128256_bf16"):
+    """DRAM traffic per launch of a kernel from its committed ncu summary,
+    if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", name + ".json")
     try:
         with open(path) as f:
             d = json.load(f)
@@ -681,7 +681,8 @@ def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
                          "> 2x L2",
                    "launch": f"CUDA graph of {G} calls, {B * min(k + 1, 8)} CTAs in clusters of {min(k + 1, 8)}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak,
+                     "traffic": measured_traffic("verify_topk_kernel_B64_k5_V128256_bf16"),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
                      "algorithmic_bytes_per_launch": alg},
         "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": cores, "kind": "oracle",

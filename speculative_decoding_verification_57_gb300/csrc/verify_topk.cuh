@@ -15,15 +15,15 @@
 //
 // One thread-block cluster of C = min(k + 1, 8) CTAs per sequence; CTA c
 // owns positions c, c + C, ...  In each CTA a producer warp streams the
-// owned rows through a ring of shared-memory stages (1-D bulk copies); each
-// of the four consumer warps keeps the best 64 entries of its share in
-// registers, as 64-bit keys (two a lane, in rank order).  An entry is
-// tested against a threshold first: a packed bf16x2 (or fp32) compare with
-// the largest 64th-best value any warp of the CTA has published, so after
-// the first tiles almost every tile passes with one compare per two logits.
-// Entries that pass collect in a per-warp buffer; a full buffer is sorted
-// with a register bitonic network and merged into the warp's 64 (half
-// cleaner + bitonic merge).  At the end of a position the four warp lists
+// owned rows through a ring of shared-memory stages (1-D bulk copies); the
+// four consumer warps take the tiles in turn, whole, and each keeps the best
+// 64 entries of its tiles in registers, as 64-bit keys (two a lane, in rank
+// order).  A block of a tile is tested against the CTA's entry bound first:
+// one packed bf16x2 maximum per two logits and one compare, so most blocks
+// are done there.  Entries that pass collect in a per-warp buffer (a warp
+// scan places a whole tile's at once); a full buffer is sorted with a
+// register bitonic network and merged into the warp's 64 (half cleaner +
+// bitonic merge).  At the end of a position the four warp lists
 // merge in a tree and the result goes into the leader CTA's shared memory
 // over DSMEM; after a cluster barrier the leader's warp 0 walks the
 // positions with double-float weights.
@@ -42,6 +42,8 @@ namespace specv {
 constexpr int kTopKMax = 64;       // largest top_k this path takes
 constexpr int kTopkClusterMax = 8;  // CTAs per sequence
 constexpr int kTopkLocalMax = (kMaxK + 1 + kTopkClusterMax - 1) / kTopkClusterMax;  // positions per CTA
+constexpr int kTopkStages = 8;     // ring stages of kTileBytes: the four warps drift apart by a few tiles
+constexpr int kTopkRingBytes = kTopkStages * kTileBytes;
 
 struct Cand {
     float v;  // logit
@@ -54,17 +56,22 @@ struct Cand {
 // aside, which never enters) maps to it.
 using key_t = unsigned long long;
 
-__device__ __forceinline__ key_t make_key(float v, int i) {
-    const uint32_t f = v == 0.0f ? 0u : __float_as_uint(v);  // -0 ranks as +0
-    const uint32_t m = (f & 0x80000000u) ? ~f : (f | 0x80000000u);
-    return (static_cast<key_t>(m) << 32) | static_cast<uint32_t>(~i);
+// Float bits made monotone as unsigned (-0 ranks as +0); 0 stands for "none".
+__device__ __forceinline__ uint32_t ord_f32(float v) {
+    const uint32_t f = v == 0.0f ? 0u : __float_as_uint(v);
+    return (f & 0x80000000u) ? ~f : (f | 0x80000000u);
 }
 
-__device__ __forceinline__ float key_value(key_t k) {
-    if (k == 0) return -INFINITY;
-    const uint32_t m = static_cast<uint32_t>(k >> 32);
+__device__ __forceinline__ float unord_f32(uint32_t m) {
+    if (m == 0) return -INFINITY;
     return __uint_as_float((m & 0x80000000u) ? (m & 0x7fffffffu) : ~m);
 }
+
+__device__ __forceinline__ key_t make_key(float v, int i) {
+    return (static_cast<key_t>(ord_f32(v)) << 32) | static_cast<uint32_t>(~i);
+}
+
+__device__ __forceinline__ float key_value(key_t k) { return unord_f32(static_cast<uint32_t>(k >> 32)); }
 
 __device__ __forceinline__ Cand key_cand(key_t k) {
     if (k == 0) return Cand{-INFINITY, 0x7fffffff};
@@ -133,14 +140,19 @@ __device__ __forceinline__ void merge64(key_t& a0, key_t& a1, key_t b0, key_t b1
 }
 
 struct alignas(16) TopkSmem {
-    unsigned long long full[kStages];
-    unsigned long long empty[kStages];
+    unsigned long long full[kTopkStages];
+    unsigned long long empty[kTopkStages];
     key_t wb[kConsumerWarps][kTopKMax];  // per-warp candidate buffers; the walk's scratch
     key_t ms[3][kTopKMax];               // lists on their way through the end-of-position merge
     int tstart[kTopkLocalMax + 1];       // first tile of each owned position
     int head[kTopkLocalMax];             // unaligned leading elements of each owned row
     int nbytes[kTopkLocalMax];           // bytes of the 16-byte aligned interior
-    float wthr[kTopkLocalMax][kConsumerWarps];  // published 64th-best values (inclusive bounds)
+    // Entry bound of each owned position (ord_f32; only rises): a logit below it
+    // cannot be among the position's best 64.  It is the larger of any warp's
+    // 64th-best value and the smallest of the four warps' 16th-best values
+    // (b16): either way at least 64 distinct entries reach it.
+    uint32_t tau[kTopkLocalMax];
+    float b16[kTopkLocalMax][kConsumerWarps];
     int lbad[kTopkLocalMax];             // bit 0: a NaN in this CTA's share of an owned position
     int ltimeout;
     int bad[kMaxK + 1];                  // leader: bit 0 NaN, bit 1 the owner timed out
@@ -150,7 +162,7 @@ struct alignas(16) TopkSmem {
 
 // Dynamic shared memory: the ring, then the leader's lists [k+1][64].
 inline size_t topk_dyn_smem(int k) {
-    return static_cast<size_t>(kRingBytes) + static_cast<size_t>(k + 1) * kTopKMax * sizeof(key_t);
+    return static_cast<size_t>(kTopkRingBytes) + static_cast<size_t>(k + 1) * kTopKMax * sizeof(key_t);
 }
 
 inline int topk_cluster(int k) { return k + 1 < kTopkClusterMax ? k + 1 : kTopkClusterMax; }
@@ -171,6 +183,7 @@ struct WarpTop {
     key_t c0, c1;  // the best 64 so far, ranks lane and lane + 32 (0: none)
     key_t t63;     // rank 63: an entry must beat it to enter
     int cnt;       // entries waiting in the warp's buffer
+    int nf;        // flushes so far
 };
 
 __device__ __forceinline__ void warp_flush(WarpTop& w, key_t* wb, int lane) {
@@ -182,42 +195,74 @@ __device__ __forceinline__ void warp_flush(WarpTop& w, key_t* wb, int lane) {
     merge64(w.c0, w.c1, s0, s1, lane);
     w.t63 = shfl_key(w.c1, 31);
     w.cnt = 0;
+    ++w.nf;
 }
 
-// Offer each lane's pending elements (bit e of pend; get(e, v, idx) reads
-// element e) to the warp's 64, one element a lane per round.  A NaN never
-// enters; it sets nan.
-template <typename Get>
-__device__ __forceinline__ void warp_take(WarpTop& w, key_t* wb, uint32_t pend, Get get, int lane, int& nan) {
+// Append each lane's pending elements (bit e of pend[s]; get(s, e, v, idx)
+// reads that element) to the warp's buffer.  The offsets come from one
+// ballot per bit of the counts; each lane then writes its elements, two at a
+// time, and a full buffer is flushed into the 64.  A NaN never enters (it
+// leaves a padding entry) and sets nan.
+template <int NW, typename Get>
+__device__ __forceinline__ void warp_take(WarpTop& w, key_t* wb, uint32_t (&pend)[NW], Get get, int lane, int& nan) {
+    static_assert(NW >= 1 && NW <= 4, "at most 128 pending bits a lane");
     const unsigned full = 0xffffffffu;
+    unsigned long long pl = pend[0], ph = 0;
+    if constexpr (NW > 1) pl |= static_cast<unsigned long long>(pend[1]) << 32;
+    if constexpr (NW > 2) ph = pend[2];
+    if constexpr (NW > 3) ph |= static_cast<unsigned long long>(pend[3]) << 32;
+    const uint32_t lt = lanemask_lt();
+    auto next = [&]() {  // the lowest pending bit (0..127), cleared
+        int g;
+        if (pl) {
+            g = __ffsll(pl) - 1;
+            pl &= pl - 1;
+        } else {
+            g = 64 + __ffsll(ph) - 1;
+            ph &= ph - 1;
+        }
+        return g;
+    };
+    auto key_of = [&](int g) {
+        float v;
+        int idx;
+        get(g >> 5, g & 31, v, idx);
+        if (v != v) {
+            nan = 1;
+            return key_t(0);
+        }
+        return make_key(v, idx);
+    };
     for (;;) {
-        const bool has = pend != 0;
-        if (!__any_sync(full, has)) break;
-        key_t key = 0;
-        bool take = false;
-        if (has) {
-            const int e = __ffs(pend) - 1;
-            pend &= pend - 1;
-            float v;
-            int idx;
-            get(e, v, idx);
-            if (v != v) {
-                nan = 1;
-            } else {
-                key = make_key(v, idx);
-                take = key > w.t63;
-            }
+        const int c = __popcll(pl) + __popcll(ph);  // <= 128
+        int before = 0, tot = 0;
+#pragma unroll
+        for (int bit = 0; bit < 8; ++bit) {
+            const unsigned bb = __ballot_sync(full, (c >> bit) & 1);
+            before += __popc(bb & lt) << bit;
+            tot += __popc(bb) << bit;
+        }
+        if (tot == 0) return;
+        int o = w.cnt + before;
+        while ((pl | ph) != 0 && o < kTopKMax) {
+            const int g0 = next();
+            const bool two = (pl | ph) != 0 && o + 1 < kTopKMax;
+            const int g1 = two ? next() : g0;
+            const key_t k0 = key_of(g0);
+            const key_t k1 = key_of(g1);
+            wb[o] = k0;
+            if (two) wb[o + 1] = k1;
+            o += two ? 2 : 1;
         }
         __syncwarp();
-        unsigned bal = __ballot_sync(full, take);
-        if (w.cnt + __popc(bal) > kTopKMax) {
-            warp_flush(w, wb, lane);
-            take = take && key > w.t63;
-            bal = __ballot_sync(full, take);
+        const int room = kTopKMax - w.cnt;
+        if (tot < room) {
+            w.cnt += tot;
+            return;
         }
-        if (take) wb[w.cnt + __popc(bal & lanemask_lt())] = key;
-        w.cnt += __popc(bal);
-        __syncwarp();
+        w.cnt = kTopKMax;
+        warp_flush(w, wb, lane);  // what did not fit is still pending
+        if (tot == room) return;
     }
 }
 
@@ -226,7 +271,6 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ __align__(16) TopkSmem sh;
     constexpr int esz = BF16 ? 2 : 4;
-    constexpr int kPer = kTileBytes / 16 / kConsumers;  // 16-byte chunks per consumer thread and tile
     constexpr int kEpc = 16 / esz;                       // elements per chunk
     const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -240,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
     const int P = (k - crank) / C + 1;  // owned positions crank + C p, p < P
     const unsigned char* lg = reinterpret_cast<const unsigned char*>(a.logits);
     unsigned char* ring = dyn_smem;
-    key_t* lists = reinterpret_cast<key_t*>(dyn_smem + kRingBytes);  // [k+1][64]; the leader's are read
+    key_t* lists = reinterpret_cast<key_t*>(dyn_smem + kTopkRingBytes);  // [k+1][64]; the leader's are read
 
     const float T = a.temp ? __ldg(a.temp + b) : 0.0f;
     const bool greedy = T == 0.0f;
@@ -253,8 +297,11 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
     // ---------------------------------------------------------------- setup
     if (tid < 128) sh.exp2tab[tid] = g_exp2_table[tid];
     if (tid <= k) sh.xs[tid] = tid < k ? __ldg(a.x + static_cast<long long>(b) * k + tid) : -1;
-    if (tid < kTopkLocalMax * kConsumerWarps) sh.wthr[tid / kConsumerWarps][tid % kConsumerWarps] = -INFINITY;
-    if (tid < kTopkLocalMax) sh.lbad[tid] = 0;
+    if (tid < kTopkLocalMax * kConsumerWarps) sh.b16[tid / kConsumerWarps][tid % kConsumerWarps] = -INFINITY;
+    if (tid < kTopkLocalMax) {
+        sh.lbad[tid] = 0;
+        sh.tau[tid] = 0u;
+    }
     auto issue = [&](int tt) {
         int p = 0;
         while (sh.tstart[p + 1] <= tt) ++p;
@@ -262,16 +309,16 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
         const int off = (tt - sh.tstart[p]) * kTileBytes;
         const int bytes = min(kTileBytes, sh.nbytes[p] - off);
         const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + sh.head[p];
-        const int slot = tt % kStages;
+        const int slot = tt % kTopkStages;
         const uint32_t bar = smem_u32(&sh.full[slot]);
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>(bytes));
         bulk_g2s(smem_u32(ring + slot * kTileBytes), lg + e0 * esz + off, static_cast<uint32_t>(bytes), bar);
     };
     int issued = 0;
     if (producer && lane == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kTopkStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
-            mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
+            mbar_init(smem_u32(&sh.empty[s]), 1);  // the one warp that took the tile
         }
         sh.ltimeout = 0;
         fence_mbar_init();
@@ -290,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
             if (run) acc += (nb + kTileBytes - 1) / kTileBytes;
         }
         sh.tstart[P] = acc;
-        for (; issued < min(kStages, acc); ++issued) issue(issued);
+        for (; issued < min(kTopkStages, acc); ++issued) issue(issued);
     }
     __syncthreads();
     cluster_arrive();  // the matching wait comes before the first store into the leader
@@ -300,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
     if (producer) {
         if (lane == 0) {
             for (; issued < total; ++issued) {
-                const int slot = issued % kStages;
-                if (sh.ltimeout || !mbar_wait_bounded(smem_u32(&sh.empty[slot]), ((issued / kStages) & 1) ^ 1,
+                const int slot = issued % kTopkStages;
+                if (sh.ltimeout || !mbar_wait_bounded(smem_u32(&sh.empty[slot]), ((issued / kTopkStages) & 1) ^ 1,
                                                       kWaitPolls)) {
                     atomicOr(&sh.ltimeout, 1);
                     break;
@@ -310,65 +357,77 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
             }
             if (sh.ltimeout) {
                 // no copy may still be writing this CTA's shared memory when it exits
-                for (int s = 0; s < kStages && s < issued; ++s) {
-                    const int last = s + kStages * ((issued - 1 - s) / kStages);
-                    mbar_wait_bounded(smem_u32(&sh.full[s]), (last / kStages) & 1, kWaitPolls);
+                for (int s = 0; s < kTopkStages && s < issued; ++s) {
+                    const int last = s + kTopkStages * ((issued - 1 - s) / kTopkStages);
+                    mbar_wait_bounded(smem_u32(&sh.full[s]), (last / kTopkStages) & 1, kWaitPolls);
                 }
             }
         }
         __syncwarp();
         cluster_wait();
     } else {
-        int it = 0;
         key_t* wb = sh.wb[warp];
         for (int p = 0; p < P; ++p) {
             const int i = crank + C * p;
             WarpTop w;
             w.c0 = w.c1 = w.t63 = 0;
             w.cnt = 0;
+            w.nf = 0;
             int nan = 0;
-            bool fresh = true;
             const long long row_e0 = (static_cast<long long>(b) * (k + 1) + i) * V;
             const int h = sh.head[p];
             const int interior = sh.nbytes[p] / esz;
-            const int ntiles = sh.tstart[p + 1] - sh.tstart[p];
+            const int t0 = sh.tstart[p];
+            const int ntiles = sh.tstart[p + 1] - t0;
             // unaligned head and tail: warp 0 reads them with plain loads, a lane an element
             auto scalar_part = [&](int lo, int hi) {
-                warp_take(w, wb, lane < hi - lo ? 1u : 0u, [&](int, float& v, int& idx) {
+                uint32_t pe[1] = {lane < hi - lo ? 1u : 0u};
+                warp_take(w, wb, pe, [&](int, int, float& v, int& idx) {
                     idx = lo + lane;
                     v = load_logit(a.logits, row_e0 + idx, BF16);
                 }, lane, nan);
             };
             if (run && warp == 0 && h > 0) scalar_part(0, h);
-            for (int lt = 0; lt < ntiles; ++lt, ++it) {
-                const int slot = it % kStages;
-                const bool ok = __all_sync(full, !sh.ltimeout && mbar_wait_bounded(smem_u32(&sh.full[slot]),
-                                                                                   (it / kStages) & 1, kWaitPolls));
-                if (!ok) {
-                    if (lane == 0) atomicOr(&sh.ltimeout, 1);
-                    continue;  // the rest of the stream is skipped, the barrier sequence kept
+            // publish the warp's bounds after its 64 changed
+            auto publish = [&]() {
+                const key_t r15 = shfl_key(w.c0, 15);
+                if (lane == 0) {
+                    if (w.t63) atomicMax(&sh.tau[p], static_cast<uint32_t>(w.t63 >> 32));
+                    if (r15) {
+                        sh.b16[p][warp] = fmaxf(sh.b16[p][warp], key_value(r15));
+                        const float m = fminf(fminf(sh.b16[p][0], sh.b16[p][1]), fminf(sh.b16[p][2], sh.b16[p][3]));
+                        if (m > -INFINITY) atomicMax(&sh.tau[p], ord_f32(m));
+                    }
                 }
-                const int bytes = min(kTileBytes, sh.nbytes[p] - lt * kTileBytes);
-                const int nch = bytes >> 4;
+                __syncwarp();
+            };
+            // Warp w takes tiles w, w + 4, ... of the position whole: lane l reads chunks
+            // l + 32 j (j < 16) in four blocks of four.  The first pass runs in every warp,
+            // with or without a tile, for the barrier that shares the first bounds.
+            for (int lt = warp; ntiles > 0; lt += kConsumerWarps) {
+                const bool first = lt == warp;
+                if (!first && lt >= ntiles) break;
+                const bool has = lt < ntiles;
+                const int it = t0 + lt;
+                const int slot = it % kTopkStages;
+                const bool ok = has && __all_sync(full, !sh.ltimeout &&
+                                                            mbar_wait_bounded(smem_u32(&sh.full[slot]),
+                                                                              (it / kTopkStages) & 1, kWaitPolls));
+                if (has && !ok && lane == 0) atomicOr(&sh.ltimeout, 1);
+                const int nch = ok ? min(kTileBytes, sh.nbytes[p] - lt * kTileBytes) >> 4 : 0;
                 const uint32_t tile = smem_u32(ring + slot * kTileBytes);
                 const int tile_e = h + lt * (kTileBytes / esz);  // row index of the tile's first element
-                uint4 d[kPer];
-#pragma unroll
-                for (int r = 0; r < kPer; ++r) {
-                    const int ch = tid + r * kConsumers;
-                    d[r] = ch < nch ? ld_shared_v4(tile + ch * 16) : make_uint4(0u, 0u, 0u, 0u);
-                }
-                // the entry bound: the best 64th value any warp has published
-                float tau = fmaxf(key_value(w.t63), fmaxf(fmaxf(sh.wthr[p][0], sh.wthr[p][1]),
-                                                          fmaxf(sh.wthr[p][2], sh.wthr[p][3])));
-                if (fresh) {
-                    // a position's first tile: at least 64 of the warp's elements reach the
-                    // smallest second-largest of the 32 lanes (a NaN counts as -inf here)
+                float tau_first = -INFINITY;
+                if (first) {
+                    // bounds from the lanes' largest two values of the first block (a NaN
+                    // counts as -inf here)
                     float mx = -INFINITY, mx2 = -INFINITY;
 #pragma unroll
-                    for (int r = 0; r < kPer; ++r) {
-                        if (tid + r * kConsumers < nch) {
-                            const uint32_t wd[4] = {d[r].x, d[r].y, d[r].z, d[r].w};
+                    for (int r = 0; r < 4; ++r) {
+                        const int ch = lane + 32 * r;
+                        if (ch < nch) {
+                            const uint4 dd = ld_shared_v4(tile + ch * 16);
+                            const uint32_t wd[4] = {dd.x, dd.y, dd.z, dd.w};
 #pragma unroll
                             for (int q = 0; q < kEpc; ++q) {
                                 float l;
@@ -382,53 +441,91 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
                             }
                         }
                     }
+                    // 64 entries reach the smallest second-largest of the 32 lanes
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) mx2 = fminf(mx2, __shfl_xor_sync(full, mx2, off));
-                    tau = fmaxf(tau, mx2);
-                    if (lane == 0) sh.wthr[p][warp] = fmaxf(sh.wthr[p][warp], mx2);
-                    fresh = false;
-                }
-                // elements that may enter (NaN included: it is caught and flagged in warp_take)
-                uint32_t pend = 0;
-                if constexpr (BF16) {
-                    const __nv_bfloat162 t2 = __float2bfloat162_rn(tau);
-                    uint32_t m[kPer][4];
-                    uint32_t any = 0;
+                    // 16 entries reach the 16th largest lane maximum: sort the maxima, descending
 #pragma unroll
-                    for (int r = 0; r < kPer; ++r) {
-                        const bool v = tid + r * kConsumers < nch;
-                        m[r][0] = v ? geu_bf16x2(d[r].x, t2) : 0u;
-                        m[r][1] = v ? geu_bf16x2(d[r].y, t2) : 0u;
-                        m[r][2] = v ? geu_bf16x2(d[r].z, t2) : 0u;
-                        m[r][3] = v ? geu_bf16x2(d[r].w, t2) : 0u;
-                        any |= m[r][0] | m[r][1] | m[r][2] | m[r][3];
-                    }
-                    if (any) {
+                    for (int size = 2; size <= 32; size <<= 1) {
 #pragma unroll
-                        for (int r = 0; r < kPer; ++r)
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                pend |= ((m[r][q] & 1u) | ((m[r][q] >> 15) & 2u)) << (r * 8 + q * 2);
-                    }
-                } else {
-#pragma unroll
-                    for (int r = 0; r < kPer; ++r) {
-                        if (tid + r * kConsumers < nch) {
-                            const uint32_t wd[4] = {d[r].x, d[r].y, d[r].z, d[r].w};
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                pend |= (__uint_as_float(wd[q]) < tau ? 0u : 1u) << (r * 4 + q);
+                        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                            const float o = __shfl_xor_sync(full, mx, stride);
+                            const bool first_of_pair = ((lane & stride) == 0) == ((lane & size) == 0);
+                            mx = first_of_pair ? fmaxf(mx, o) : fminf(mx, o);
                         }
                     }
+                    const float m16 = __shfl_sync(full, mx, 15);
+                    if (lane == 0) {
+                        sh.b16[p][warp] = m16;
+                        if (mx2 > -INFINITY) atomicMax(&sh.tau[p], ord_f32(mx2));
+                    }
+                    consumers_sync();
+                    tau_first = fmaxf(mx2, fminf(fminf(sh.b16[p][0], sh.b16[p][1]), fminf(sh.b16[p][2], sh.b16[p][3])));
+                    if (lane == 0 && tau_first > -INFINITY) atomicMax(&sh.tau[p], ord_f32(tau_first));
                 }
-                if (__any_sync(full, pend != 0)) {
-                    warp_take(w, wb, pend, [&](int e, float& v, int& idx) {
-                        const int r = e / kEpc, q = e % kEpc, ch = tid + r * kConsumers;
-                        v = BF16 ? __uint_as_float(static_cast<uint32_t>(ld_shared_u16(tile + ch * 16 + q * 2)) << 16)
-                                 : ld_shared_f32(tile + ch * 16 + q * 4);
-                        idx = tile_e + ch * kEpc + q;
+                if (!ok) continue;  // no tile here, or the stream gave up: the barrier sequence is kept
+                const float tau = fmaxf(tau_first, unord_f32(sh.tau[p]));
+                // elements that may enter (NaN included: it is caught and flagged in warp_take)
+                uint32_t pend[4];
+#pragma unroll
+                for (int sb = 0; sb < 4; ++sb) {
+                    uint4 d[4];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int ch = lane + 32 * (sb * 4 + r);
+                        d[r] = ch < nch ? ld_shared_v4(tile + ch * 16) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    uint32_t pm = 0;
+                    if constexpr (BF16) {
+                        // bit r*4+q: the low element of word q of chunk r; bit 16+r*4+q: the high one
+                        const __nv_bfloat162 t2 = __float2bfloat162_rn(tau);
+                        uint32_t cm[4];  // each chunk's maximum (NaN kept)
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            cm[r] = lane + 32 * (sb * 4 + r) < nch
+                                        ? max_nan_bf16x2(max_nan_bf16x2(d[r].x, d[r].y), max_nan_bf16x2(d[r].z, d[r].w))
+                                        : 0xff80ff80u;  // (-inf, -inf)
+                        const uint32_t mw = max_nan_bf16x2(max_nan_bf16x2(cm[0], cm[1]), max_nan_bf16x2(cm[2], cm[3]));
+                        if (geu_bf16x2(mw, t2)) {
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                if (lane + 32 * (sb * 4 + r) < nch && geu_bf16x2(cm[r], t2)) {
+                                    const uint32_t wd[4] = {d[r].x, d[r].y, d[r].z, d[r].w};
+#pragma unroll
+                                    for (int q = 0; q < 4; ++q)
+                                        pm |= (geu_bf16x2(wd[q], t2) & 0x00010001u) << (r * 4 + q);
+                                }
+                            }
+                        }
+                    } else {
+                        // bit r*4+q: element q of chunk r
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            if (lane + 32 * (sb * 4 + r) < nch) {
+                                const uint32_t wd[4] = {d[r].x, d[r].y, d[r].z, d[r].w};
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    pm |= (__uint_as_float(wd[q]) < tau ? 0u : 1u) << (r * 4 + q);
+                            }
+                        }
+                    }
+                    pend[sb] = pm;
+                }
+                if (__any_sync(full, (pend[0] | pend[1] | pend[2] | pend[3]) != 0)) {
+                    const int nf0 = w.nf;
+                    warp_take(w, wb, pend, [&](int sb, int e, float& v, int& idx) {
+                        if constexpr (BF16) {
+                            const int r = (e & 15) >> 2, q = 2 * (e & 3) + (e >> 4);
+                            const int ch = lane + 32 * (sb * 4 + r);
+                            v = __uint_as_float(static_cast<uint32_t>(ld_shared_u16(tile + ch * 16 + q * 2)) << 16);
+                            idx = tile_e + ch * kEpc + q;
+                        } else {
+                            const int r = e >> 2, q = e & 3, ch = lane + 32 * (sb * 4 + r);
+                            v = ld_shared_f32(tile + ch * 16 + q * 4);
+                            idx = tile_e + ch * kEpc + q;
+                        }
                     }, lane, nan);
-                    if (lane == 0 && w.t63 != 0) sh.wthr[p][warp] = fmaxf(sh.wthr[p][warp], key_value(w.t63));
+                    if (w.nf != nf0) publish();
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&sh.empty[slot]));
@@ -460,6 +557,15 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
             }
         }
         if (warp != 0) cluster_wait();
+    }
+    // the walk's per-position inputs (lane i: position i), loaded while the cluster barrier completes
+    float pu0 = 0.0f, pu1 = 0.0f, pqx = 0.0f;
+    if (crank == 0 && warp == 0 && lane <= k) {
+        const long long ub = (static_cast<long long>(b) * (k + 1) + lane) * 2;
+        pu0 = __ldg(a.u + ub);
+        pu1 = __ldg(a.u + ub + 1);
+        const int x = lane < k ? sh.xs[lane] : -1;
+        if (x >= 0 && x < V) pqx = a.q ? __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + x) : 1.0f;
     }
     cluster_sync();  // every list and flag is in the leader
     if (crank != 0 || warp != 0) return;
@@ -505,13 +611,11 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
             const int x = i < k ? sh.xs[i] : -1;
             float u0 = 0.0f, qx = 0.0f;
             if (i < k) {
-                u0 = __ldg(a.u + (static_cast<long long>(b) * (k + 1) + i) * 2);
+                u0 = __shfl_sync(full, pu0, i);
+                qx = __shfl_sync(full, pqx, i);
                 if (x < 0 || x >= V) pst |= ST_TOKEN;
                 if (!(u0 >= 0.0f && u0 < 1.0f)) pst |= ST_UNIFORM;
-                if (x >= 0 && x < V) {
-                    qx = a.q ? __ldg(a.q + (static_cast<long long>(b) * k + i) * V + x) : 1.0f;
-                    if (!(qx >= 0.0f && qx <= FLT_MAX)) pst |= ST_QBAD;
-                }
+                if (x >= 0 && x < V && !(qx >= 0.0f && qx <= FLT_MAX)) pst |= ST_QBAD;
             }
             if (pst) {
                 st |= pst;
@@ -554,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
         }
         float u1 = 0.0f;
         if (!st) {
-            u1 = __ldg(a.u + (static_cast<long long>(b) * (k + 1) + j) * 2 + 1);
+            u1 = __shfl_sync(full, pu1, j);
             if (!(u1 >= 0.0f && u1 < 1.0f)) st |= ST_UNIFORM;
         }
         if (!st) {
@@ -579,31 +683,19 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
                 }
             }
             if (!(st & ST_ERRMASK)) {
-                // the kept entries in vocabulary order (rank of each index among them)
-                int o0 = 0, o1 = 0;
-                for (int s2 = 0; s2 < np; ++s2) {
-                    const int is = s2 < 32 ? __shfl_sync(full, c0.i, s2) : __shfl_sync(full, c1.i, s2 - 32);
-                    o0 += is < c0.i ? 1 : 0;
-                    o1 += is < c1.i ? 1 : 0;
-                }
-                // scratch (the candidate buffers, free now): (weight hi, index) then (weight lo, index)
-                Cand* ohi = reinterpret_cast<Cand*>(sh.wb[0]);
-                Cand* olo = reinterpret_cast<Cand*>(sh.wb[1]);
-                for (int t = lane; t < kTopKMax; t += 32) {
-                    ohi[t] = Cand{0.0f, 0x7fffffff};
-                    olo[t] = Cand{0.0f, 0x7fffffff};
-                }
-                __syncwarp();
-                if (v0) {
-                    ohi[o0] = Cand{w0.hi, c0.i};
-                    olo[o0] = Cand{w0.lo, c0.i};
-                }
-                if (v1) {
-                    ohi[o1] = Cand{w1.hi, c1.i};
-                    olo[o1] = Cand{w1.lo, c1.i};
-                }
-                __syncwarp();
-                const df a0 = df{ohi[lane].v, olo[lane].v}, a1 = df{ohi[lane + 32].v, olo[lane + 32].v};
+                // the kept entries in vocabulary order: sort (index, rank) keys, the lowest index first
+                key_t o0 = v0 ? (static_cast<key_t>(~static_cast<uint32_t>(c0.i)) << 32) | static_cast<uint32_t>(lane) : 0;
+                key_t o1 = v1 ? (static_cast<key_t>(~static_cast<uint32_t>(c1.i)) << 32) | static_cast<uint32_t>(lane + 32)
+                              : 0;
+                sort64(o0, o1, lane);
+                // the weight of the entry at each sorted place
+                auto weight_at = [&](key_t o) {
+                    const int r = static_cast<int>(o & 63u);
+                    const float hA = __shfl_sync(full, w0.hi, r & 31), lA = __shfl_sync(full, w0.lo, r & 31);
+                    const float hB = __shfl_sync(full, w1.hi, r & 31), lB = __shfl_sync(full, w1.lo, r & 31);
+                    return o == 0 ? df_make(0.0f) : (r < 32 ? df{hA, lA} : df{hB, lB});
+                };
+                const df a0 = weight_at(o0), a1 = weight_at(o1);
                 const df p0 = df_warp_incl_scan(a0, lane);
                 const df p1 = df_sum(df_shfl(p0, 31), df_warp_incl_scan(a1, lane));
                 const df W = df_shfl(p1, 31);
@@ -620,7 +712,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
                     const unsigned q0b = __ballot_sync(full, pos0), q1b = __ballot_sync(full, pos1);
                     slot = q1b ? 32 + 31 - __clz(q1b) : (q0b ? 31 - __clz(q0b) : 0);
                 }
-                token = ohi[slot].i;
+                const key_t kA = shfl_key(o0, slot & 31), kB = shfl_key(o1, slot & 31);
+                token = static_cast<int>(~static_cast<uint32_t>((slot < 32 ? kA : kB) >> 32));
             }
         }
     }
