@@ -42,7 +42,7 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--graph-calls", type=int, default=100)
-    p.add_argument("--variant", choices=["sample", "onehot", "tree", "filtered"], default="sample",
+    p.add_argument("--variant", choices=["sample", "onehot", "tree", "filtered", "rollback"], default="sample",
                    help="onehot: the same workload verified as one-hot drafts (q = None); tree: greedy "
                         "verification of 16-node draft trees over the same vocabulary")
     return p.parse_args(argv)
@@ -279,6 +279,8 @@ def run_ours(args):
         return run_tree(args, sv, dev, rank, ws, local, hbm_peak, peak_src)
     if args.variant == "filtered":
         return run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src)
+    if args.variant == "rollback":
+        return run_rollback(args, sv, dev, rank, ws, local, hbm_peak, peak_src)
     w = W.make_config(CONFIG_INDEX, seed=57000 + CONFIG_INDEX + 1000 * rank)
     onehot = args.variant == "onehot"
     if onehot:
@@ -692,6 +694,158 @@ def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out.values()),
                 "steps": e2e_steps, "path": "pinned copies + specv_verify_sample_filtered + copies back, per step"},
         "gpu_launches": steps, "mean_num_accepted": float(np.mean(got["num_accepted"])), "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+RB_B, RB_K, RB_BS, RB_MB = 4096, 8, 16, 64
+
+
+def run_rollback(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
+    """Paged-KV rollback after a verify step: B=4096 rows, k=8 drafts,
+    16-position blocks, up to 64 blocks a row."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from speculative_decoding_verification_57_gb300 import workloads as W
+
+    B, k, bs, mb = RB_B, RB_K, RB_BS, RB_MB
+    na, lens, tables, nb = W.make_rollback_batch(57200 + 1000 * rank, B, k, bs, mb)
+    cap = B * mb
+    h = sv.specv_create(local, max_batch=B, max_k=k, vocab=1024)
+    base = {kk: torch.from_numpy(v).to(dev) for kk, v in dict(na=na, lens=lens, tables=tables, nb=nb).items()}
+    work = {kk: v.clone() for kk, v in base.items()}
+    free = torch.full((cap,), -1, dtype=torch.int32, device=dev)
+    fc = torch.zeros(1, dtype=torch.int32, device=dev)
+    st = torch.empty(B, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def reset():
+        for kk in work:
+            work[kk].copy_(base[kk], non_blocking=True)
+        fc.zero_()
+
+    def call():
+        sv.specv_rollback(h, work["na"], k, work["lens"], work["tables"], work["nb"], bs, free, fc, row_status=st,
+                          stream=stream)
+
+    with torch.cuda.stream(stream):
+        reset()
+        call()
+    stream.synchronize()
+    ref = oracle.rollback(na, k, lens, tables, nb, bs, np.full(cap, -1, np.int32), 0)
+    got = dict(seq_lens=work["lens"].cpu().numpy(), block_tables=work["tables"].cpu().numpy(),
+               num_blocks=work["nb"].cpu().numpy(), row_status=st.cpu().numpy())
+    if not all(np.array_equal(got[kk], ref[kk]) for kk in got) or int(fc.item()) != ref["free_count"] or \
+            not np.array_equal(free.cpu().numpy(), ref["free_list"]):
+        raise RuntimeError("rollback differs from the oracle on the benchmark inputs")
+    popped = int(ref["free_count"])
+    # per row: read num_accepted, seq_len, num_blocks; write seq_len, num_blocks, status;
+    # per popped block: read its table entry, write -1 there and the block into the free list
+    alg = B * 24 + popped * 12 + 8
+    # the call changes its inputs: every replay restores them first; the restore alone is
+    # timed too and subtracted
+    G = max(1, min(args.graph_calls, 50))
+
+    def graph(with_call):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            reset()
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(G):
+                    reset()
+                    if with_call:
+                        call()
+        return g
+
+    g_both, g_reset = graph(True), graph(False)
+    reps = max(1, args.steps // G)
+    steps = reps * G
+
+    def timed(g):
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup // G)):
+                g.replay()
+        stream.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        return ev0.elapsed_time(ev1)
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.mark("t0")
+    ms_both = timed(g_both)
+    sampler.mark("t1")
+    ms_reset = timed(g_reset)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop() if rank == 0 else None
+    ms = reduce_max(max(ms_both - ms_reset, 1e-6), ws, dev)
+    per_call_s = ms / 1e3 / steps
+    # end to end: pinned host state in, rollback, the changed state and the free list back
+    pin = {kk: torch.from_numpy(v).pin_memory() for kk, v in dict(na=na, lens=lens, tables=tables, nb=nb).items()}
+    host_out = {kk: torch.empty_like(work[kk], device="cpu").pin_memory() for kk in ("lens", "tables", "nb")}
+    host_free = torch.empty_like(free, device="cpu").pin_memory()
+    host_fc = torch.empty(1, dtype=torch.int32).pin_memory()
+    e2e_steps = max(1, args.e2e_steps)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        with torch.cuda.stream(stream):
+            for kk in pin:
+                work[kk].copy_(pin[kk], non_blocking=True)
+            fc.zero_()
+            call()
+            for kk in host_out:
+                host_out[kk].copy_(work[kk], non_blocking=True)
+            host_fc.copy_(fc, non_blocking=True)
+            host_free[:popped].copy_(free[:popped], non_blocking=True)
+        stream.synchronize()
+    e2e_s = reduce_max(time.perf_counter() - t0, ws, dev)
+    if rank != 0:
+        return 0
+    oracle.rollback(na, k, lens, tables, nb, bs, np.full(cap, -1, np.int32), 0)
+    n, t1 = 0, time.perf_counter()
+    while time.perf_counter() - t1 < 1.5 or n < 2:
+        oracle.rollback(na, k, lens, tables, nb, bs, np.full(cap, -1, np.int32), 0)
+        n += 1
+    cpu_value = B * n / (time.perf_counter() - t1)
+    achieved = alg / per_call_s / 1e9
+    line = {
+        "metric": "rollback rows/s", "value": B * steps * ws / (ms / 1e3), "unit": "rows/s", "n_gpus": ws,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": f"paged-KV rollback B={B} k={k} block_size={bs} max_blocks={mb} (lengths uniform "
+                               "in [k, 1024], num_accepted uniform in 0..k)", "B": B, "k": k,
+                   "global_batch": B * ws, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": "inputs (1.1 MB) stay in L2; every call first restores them from a device copy, "
+                         "that restore timed alone and subtracted",
+                   "launch": f"CUDA graph of {G} calls, one CTA of 1024 threads"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
+                     "algorithmic_bytes_per_launch": alg,
+                     "note": "latency-bound: one CTA, two block-wide scans over the batch"},
+        "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} oracle calls x {B} rows, one thread"},
+        "e2e": {"value": B * e2e_steps * ws / e2e_s, "unit": "rows/s",
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values()),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out.values()) + 4 + popped * 4,
+                "steps": e2e_steps, "path": "pinned copies + specv_rollback + copies back, per step"},
+        "gpu_launches": steps, "blocks_freed_per_call": popped, "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     return 0

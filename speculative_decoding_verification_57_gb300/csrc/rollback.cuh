@@ -7,8 +7,8 @@
 // The result equals rolling the rows back one at a time in batch order: row
 // b's popped blocks land in the free list after those of rows 0..b-1, each
 // row's blocks last-first, as popping them one at a time would.  One CTA of
-// 1024 threads walks the batch in chunks of 1024 rows; a block-wide scan of
-// the per-row counts places every row's blocks.
+// 1024 threads; thread t owns a contiguous run of rows, so one block-wide
+// exclusive scan of the per-thread counts places every row's blocks.
 #pragma once
 #include <cstdint>
 
@@ -66,53 +66,48 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 
 __global__ void __launch_bounds__(kRollbackThreads, 1) rollback_kernel(const RollbackArgs r) {
     __shared__ long long warp_sums[32];
-    __shared__ int no_room;
-    // 1. every row's count: does the free list have room for all of them?
-    long long total = 0;
-    for (int c0 = 0; c0 < r.B; c0 += kRollbackThreads) {
-        const int b = c0 + static_cast<int>(threadIdx.x);
+    // thread t owns rows [lo, hi): contiguous runs in thread order keep batch order
+    const long long per = (static_cast<long long>(r.B) + kRollbackThreads - 1) / kRollbackThreads;
+    const long long lo0 = static_cast<long long>(threadIdx.x) * per;
+    const int lo = static_cast<int>(lo0 < r.B ? lo0 : r.B);
+    const int hi = static_cast<int>(lo0 + per < r.B ? lo0 + per : r.B);
+    // 1. the run's count, its place in the free list, and the total
+    long long mine = 0;
+    for (int b = lo; b < hi; ++b) {
         int target = 0, needed = 0;
-        const int cnt = b < r.B ? rollback_count(r, b, target, needed) : 0;
-        long long chunk;
-        block_exclusive_scan(cnt > 0 ? cnt : 0, warp_sums, &chunk);
-        total += chunk;
+        const int cnt = rollback_count(r, b, target, needed);
+        mine += cnt > 0 ? cnt : 0;
     }
-    if (threadIdx.x == 0) no_room = (static_cast<long long>(*r.free_count) + total > r.capacity) ? 1 : 0;
-    __syncthreads();
+    long long total = 0;
+    const long long before = block_exclusive_scan(mine, warp_sums, &total);
     const long long base0 = *r.free_count;
-    __syncthreads();
-    if (no_room) {
+    __syncthreads();  // every thread has read free_count before thread 0 writes it
+    if (base0 + total > r.capacity) {
         if (r.row_status)
-            for (int b = threadIdx.x; b < r.B; b += kRollbackThreads) r.row_status[b] = RB_NO_ROOM;
+            for (int b = lo; b < hi; ++b) r.row_status[b] = RB_NO_ROOM;
         return;
     }
-    // 2. place and pop
-    long long base = base0;
-    for (int c0 = 0; c0 < r.B; c0 += kRollbackThreads) {
-        const int b = c0 + static_cast<int>(threadIdx.x);
+    // 2. pop, last block first, into the run's place
+    long long off = base0 + before;
+    for (int b = lo; b < hi; ++b) {
         int target = 0, needed = 0;
-        const int cnt = b < r.B ? rollback_count(r, b, target, needed) : 0;
-        long long chunk;
-        const long long off = base + block_exclusive_scan(cnt > 0 ? cnt : 0, warp_sums, &chunk);
-        if (b < r.B) {
-            if (cnt < 0) {
-                if (r.row_status) r.row_status[b] = RB_INVALID;
-            } else {
-                int32_t* table = r.block_tables + static_cast<long long>(b) * r.max_blocks;
-                const int nb = r.num_blocks[b];
-                for (int i = 0; i < cnt; ++i) {
-                    r.free_list[off + i] = table[nb - 1 - i];
-                    table[nb - 1 - i] = -1;
-                }
-                r.num_blocks[b] = nb - cnt;
-                r.seq_lens[b] = target;
-                if (r.row_status) r.row_status[b] = 0;
-            }
+        const int cnt = rollback_count(r, b, target, needed);
+        if (cnt < 0) {
+            if (r.row_status) r.row_status[b] = RB_INVALID;
+            continue;
         }
-        base += chunk;
+        int32_t* table = r.block_tables + static_cast<long long>(b) * r.max_blocks;
+        const int nb = r.num_blocks[b];
+        for (int i = 0; i < cnt; ++i) {
+            r.free_list[off + i] = table[nb - 1 - i];
+            table[nb - 1 - i] = -1;
+        }
+        off += cnt;
+        r.num_blocks[b] = nb - cnt;
+        r.seq_lens[b] = target;
+        if (r.row_status) r.row_status[b] = 0;
     }
-    __syncthreads();
-    if (threadIdx.x == 0) *r.free_count = static_cast<int32_t>(base);
+    if (threadIdx.x == 0) *r.free_count = static_cast<int32_t>(base0 + total);
 }
 
 }  // namespace specv

@@ -244,3 +244,20 @@ CONFIGS = {1: _c1, 2: _c2, 3: _c3, 4: _c4, 5: _c5}
 def make_config(index: int, seed: int | None = None) -> Workload:
     """Named configuration ``index`` (1..5); default seed 57000 + index."""
     return CONFIGS[index](57000 + index if seed is None else seed)
+
+
+def make_rollback_batch(seed: int, B: int, k: int, block_size: int, max_blocks: int):
+    """Paged-cache state after a verify step of B rows with k drafts each:
+    num_accepted uniform on 0..k; every row holds between k and
+    max_blocks * block_size positions, its blocks a slice of one random
+    permutation of the pool.  Returns (num_accepted, seq_lens, block_tables,
+    num_blocks), int32."""
+    rng = np.random.default_rng(np.random.SeedSequence(seed))
+    lens = rng.integers(k, max_blocks * block_size + 1, size=B).astype(np.int32)
+    nb = ((lens + block_size - 1) // block_size).astype(np.int32)
+    tables = np.full((B, max_blocks), -1, np.int32)
+    perm = rng.permutation(B * max_blocks).astype(np.int32)
+    for b in range(B):
+        tables[b, : nb[b]] = perm[b * max_blocks: b * max_blocks + nb[b]]
+    na = rng.integers(0, k + 1, size=B).astype(np.int32)
+    return na, lens, tables, nb
