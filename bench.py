@@ -110,24 +110,33 @@ def make_tree_workload(seed, B=64, M=TREE_M, V=128256):
     return Lb, tok, par
 
 
-def kernel_source_hash():
+# The sources each profiled kernel is built from: a committed ncu summary
+# counts only while these are unchanged.
+KERNEL_SOURCES = {
+    "verify_cluster_kernel_B64_k5_V128256_bf16": ["verify_cluster.cuh", "ptx.cuh", "exp2dd.cuh", "specv.cu"],
+    "verify_topk_kernel_B64_k5_V128256_bf16": ["verify_topk.cuh", "verify_cluster.cuh", "ptx.cuh", "exp2dd.cuh",
+                                               "specv.cu"],
+}
+
+
+def kernel_source_hash(files):
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "speculative_decoding_verification_57_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
+    for name in files:
+        with open(os.path.join(ROOT, "speculative_decoding_verification_57_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def measured_traffic(name="verify_cluster_kernel_B64_k5_V128256_bf16"):
     """DRAM traffic per launch of a kernel from its committed ncu summary,
-    if it was taken on the current kernel sources."""
+    if it was taken on the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", name + ".json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    if d.get("kernel_hash") != kernel_source_hash():
+    if d.get("kernel_hash") != kernel_source_hash(KERNEL_SOURCES[name]):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -199,15 +208,33 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def time_oracle(w, budget_s, max_rows=None):
+def cpu_model():
+    """The host CPU's name as /proc/cpuinfo gives it (x86: model name; Arm:
+    implementer / part codes)."""
+    import platform
+
+    try:
+        info = open("/proc/cpuinfo").read().splitlines()
+    except OSError:
+        return platform.machine()
+    for key in ("model name", "Model"):
+        for line in info:
+            if line.startswith(key):
+                return line.split(":", 1)[1].strip()
+    impl = next((l.split(":", 1)[1].strip() for l in info if l.startswith("CPU implementer")), "?")
+    part = next((l.split(":", 1)[1].strip() for l in info if l.startswith("CPU part")), "?")
+    return f"{platform.machine()} implementer {impl} part {part}"
+
+
+def time_oracle(w, budget_s, max_rows=None, nthreads=None):
     """Rows/s of the float64 oracle over (a bounded sample of) workload w
-    on all host cores."""
+    on nthreads host threads (default: all cores)."""
     import oracle
 
     rows = w.B if max_rows is None else min(w.B, max_rows)
     sl = slice(0, rows)
     args = (w.logits[sl], None if w.q is None else w.q[sl], w.x[sl], w.u[sl], w.T[sl])
-    cores = host_cores()
+    cores = host_cores() if nthreads is None else nthreads
     oracle.verify(*args, nthreads=cores)  # warm (page in)
     n, t0 = 0, time.perf_counter()
     while True:
@@ -217,6 +244,22 @@ def time_oracle(w, budget_s, max_rows=None):
         if el >= budget_s and n >= 2:
             break
     return rows * n / el, cores, f"{n} oracle calls x {rows} rows of the benchmark workload, {el:.2f} s wall"
+
+
+def oracle_parity(w, got):
+    """The timed call's outputs against the oracle on the same inputs: rows
+    that differ, and how many of them the oracle flags (a uniform within
+    1e-6 of a decision edge)."""
+    import numpy as np
+
+    import oracle
+
+    ref = oracle.verify(w.logits, w.q, w.x, w.u, w.T, nthreads=host_cores())
+    same = ((got["num_accepted"] == ref["num_accepted"]) & (got["row_status"] == ref["row_status"])
+            & (got["out_tokens"] == ref["out_tokens"]).all(1))
+    flagged = ref["boundary"] != 0
+    return {"rows": int(len(same)), "differ": int((~same).sum()), "differ_unflagged": int((~same & ~flagged).sum()),
+            "flagged": int(flagged.sum())}
 
 
 def run_reference(args):
@@ -405,6 +448,8 @@ def run_ours(args):
         return 0
 
     cpu_value, cores, sample = time_oracle(w, budget_s=1.5)
+    cpu_one, _, _ = time_oracle(w, budget_s=1.0, max_rows=8, nthreads=1)
+    parity = oracle_parity(w, got)
     achieved = alg / per_call_s / 1e9
     traffic = measured_traffic()
     line = {
@@ -434,7 +479,9 @@ def run_ours(args):
             "traffic": traffic, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
             "algorithmic_bytes_per_launch": alg, "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
         },
-        "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": cores, "kind": "oracle", "sample": sample,
+                         "single_thread_value": cpu_one, "cpu_model": cpu_model()},
+        "parity": parity,
         "e2e": {"value": B * args.e2e_steps * ws / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                 "path": "specv_verify_sample_host (pinned host buffers, copies + kernel + sync per step)"},
