@@ -112,10 +112,13 @@ def make_tree_workload(seed, B=64, M=TREE_M, V=128256):
 
 # The sources each profiled kernel is built from: a committed ncu summary
 # counts only while these are unchanged.
+_CLUSTER_SOURCES = ["verify_cluster.cuh", "ptx.cuh", "exp2dd.cuh", "specv.cu"]
 KERNEL_SOURCES = {
-    "verify_cluster_kernel_B64_k5_V128256_bf16": ["verify_cluster.cuh", "ptx.cuh", "exp2dd.cuh", "specv.cu"],
-    "verify_topk_kernel_B64_k5_V128256_bf16": ["verify_topk.cuh", "verify_cluster.cuh", "ptx.cuh", "exp2dd.cuh",
-                                               "specv.cu"],
+    "verify_cluster_kernel_B64_k5_V128256_bf16": _CLUSTER_SOURCES,
+    "verify_cluster_kernel_onehot_B64_k5_V128256_bf16": _CLUSTER_SOURCES,
+    "verify_cluster_kernel_tree_B64_M16_V128256_bf16": _CLUSTER_SOURCES,
+    "verify_topk_kernel_B64_k5_V128256_bf16": ["verify_topk.cuh"] + _CLUSTER_SOURCES,
+    "rollback_kernel_B4096_k8": ["rollback.cuh", "specv.cu"],
 }
 
 
@@ -451,7 +454,8 @@ def run_ours(args):
     cpu_one, _, _ = time_oracle(w, budget_s=1.0, max_rows=8, nthreads=1)
     parity = oracle_parity(w, got)
     achieved = alg / per_call_s / 1e9
-    traffic = measured_traffic()
+    traffic = measured_traffic("verify_cluster_kernel_onehot_B64_k5_V128256_bf16" if onehot
+                               else "verify_cluster_kernel_B64_k5_V128256_bf16")
     line = {
         "metric": "verify rows/s",
         "value": value,
@@ -600,7 +604,8 @@ def run_tree(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
                    "l2": f"rotating {N_SETS} input sets ({N_SETS * Lb.nbytes / 1e9:.2f} GB) > 2x L2",
                    "launch": f"CUDA graph of {G} calls, {specv_cluster_desc(sv, h, B, M, V)}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak,
+                     "traffic": measured_traffic("verify_cluster_kernel_tree_B64_M16_V128256_bf16"),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
                      "algorithmic_bytes_per_launch": alg},
         "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": 1, "kind": "oracle",
@@ -882,10 +887,10 @@ def run_rollback(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
                          "that restore timed alone and subtracted",
                    "launch": f"CUDA graph of {G} calls, one CTA of 1024 threads"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": measured_traffic("rollback_kernel_B4096_k8"),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
                      "algorithmic_bytes_per_launch": alg,
-                     "note": "latency-bound: one CTA, two block-wide scans over the batch"},
+                     "note": "latency-bound: one CTA, one block-wide scan over the batch"},
         "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": 1, "kind": "oracle",
                          "sample": f"{n} oracle calls x {B} rows, one thread"},
         "e2e": {"value": B * e2e_steps * ws / e2e_s, "unit": "rows/s",

@@ -110,6 +110,11 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of a cluster barrier (release on arrive, acquire on wait),
+// for work between them.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 // Address of the same shared variable in CTA `rank` of this cluster.
 __device__ __forceinline__ uint32_t map_rank(uint32_t local, uint32_t rank) {
     uint32_t r;
@@ -150,6 +155,10 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
 
 __device__ __forceinline__ void st_cluster_v2(uint32_t addr, uint32_t a, uint32_t b) {
     asm volatile("st.shared::cluster.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // Named barrier 1 over the first 128 threads of the CTA (the consumer warps).

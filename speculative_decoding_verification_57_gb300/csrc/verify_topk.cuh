@@ -167,13 +167,6 @@ inline size_t topk_dyn_smem(int k) {
 
 inline int topk_cluster(int k) { return k + 1 < kTopkClusterMax ? k + 1 : kTopkClusterMax; }
 
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
-
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ uint32_t geu_bf16x2(uint32_t w, __nv_bfloat162 t) {
     return __hgeu2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w), t);
 }
