@@ -31,6 +31,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda_bf16.h>
+
 #include "exp2dd.cuh"
 #include "ptx.cuh"
 
@@ -607,16 +609,23 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 cons_release(it_cons);  // the data is in registers
                 float lmax;
                 if (BF16) {
-                    uint32_t mx = 0xff80ff80u, mn = 0xff80ff80u;
+                    if (greedy) {
+                        // one NaN-propagating maximum: a NaN only flags the row (its
+                        // argmax is undefined), so it may hide the tile's other values
+                        uint32_t mx = 0xff80ff80u;
 #pragma unroll
-                    for (int r = 0; r < kPer; ++r) {
-                        mx = max_bf16x2(max_bf16x2(mx, w[r].x), max_bf16x2(w[r].y, max_bf16x2(w[r].z, w[r].w)));
-                        if (greedy)
-                            mn = max_nan_bf16x2(max_nan_bf16x2(mn, w[r].x),
+                        for (int r = 0; r < kPer; ++r)
+                            mx = max_nan_bf16x2(max_nan_bf16x2(mx, w[r].x),
                                                 max_nan_bf16x2(w[r].y, max_nan_bf16x2(w[r].z, w[r].w)));
+                        lmax = max_nan_f32(bf16_lo(mx), bf16_hi(mx));
+                        if (lmax != lmax) nan_seen = true;
+                    } else {
+                        uint32_t mx = 0xff80ff80u;
+#pragma unroll
+                        for (int r = 0; r < kPer; ++r)
+                            mx = max_bf16x2(max_bf16x2(mx, w[r].x), max_bf16x2(w[r].y, max_bf16x2(w[r].z, w[r].w)));
+                        lmax = fmaxf(bf16_lo(mx), bf16_hi(mx));
                     }
-                    lmax = fmaxf(bf16_lo(mx), bf16_hi(mx));
-                    if (greedy && (bf16_lo(mn) != bf16_lo(mn) || bf16_hi(mn) != bf16_hi(mn))) nan_seen = true;
                 } else {
                     float mx = -INFINITY, mn = -INFINITY;
 #pragma unroll
@@ -630,10 +639,38 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                     if (greedy && mn != mn) nan_seen = true;
                 }
                 if (greedy) {
-                    if (lmax > m) {
+                    if (BF16 && lmax > m) {
+                        // lowest tile-local index holding the new maximum: the first
+                        // chunk whose maximum equals it (chunk r covers elements
+                        // ch*8 .. ch*8+7, ch = tid + r*128), then the first such
+                        // element in it; the packed compare takes -0 == +0
+                        const uint32_t h16 = __float_as_uint(lmax) >> 16;
+                        const uint32_t lmw = h16 | (h16 << 16);
+                        const __nv_bfloat162 lm2 = *reinterpret_cast<const __nv_bfloat162*>(&lmw);
+                        int rs = kPer - 1;
+#pragma unroll
+                        for (int r = kPer - 2; r >= 0; --r) {
+                            const uint32_t cmr = max_bf16x2(max_bf16x2(w[r].x, w[r].y), max_bf16x2(w[r].z, w[r].w));
+                            if (__heq2_mask(*reinterpret_cast<const __nv_bfloat162*>(&cmr), lm2)) rs = r;
+                        }
+                        uint4 wc = w[kPer - 1];
+#pragma unroll
+                        for (int r = kPer - 2; r >= 0; --r)
+                            if (r == rs) wc = w[r];
+                        const uint32_t ws[4] = {wc.x, wc.y, wc.z, wc.w};
+                        int q8 = 7;
+#pragma unroll
+                        for (int q4 = 3; q4 >= 0; --q4) {
+                            const uint32_t eqm = __heq2_mask(*reinterpret_cast<const __nv_bfloat162*>(&ws[q4]), lm2);
+                            if (eqm) q8 = q4 * 2 + ((eqm & 0xffffu) ? 0 : 1);
+                        }
+                        const long long tile_e0 = v0 + h + static_cast<long long>(lt) * (kTileBytes / esz);
+                        arg = static_cast<int>(tile_e0 + (tid + rs * kConsumers) * 8 + q8);
+                        m = lmax;
+                    } else if (!BF16 && lmax > m) {
                         // lowest tile-local index holding the new maximum: the
                         // candidates reduced by min in a tree (chunk r of this
-                        // thread covers elements ch*per+..., ch = tid + r*128)
+                        // thread covers elements ch*4+..., ch = tid + r*128)
                         constexpr int kPerWord = BF16 ? 2 : 1;
                         constexpr int kCand = kPer * 4 * kPerWord;
                         int cand[kCand];
