@@ -439,7 +439,10 @@ def run_ours(args):
     for _ in range(args.e2e_steps):
         sv.specv_verify_sample_host(h, pin["L"], pin["q"], pin["x"], pin["u"], pin["T"], out=host_out, stream=stream)
     e2e_s = reduce_max(time.perf_counter() - t0, ws, dev)
-    h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
+    # q is page-locked, so the kernel reads in place only the entries it needs: q at
+    # the draft tokens and the rejecting rows' stop rows; the other inputs are copied
+    q_in_place = 0 if onehot else (int(((got["num_accepted"] < k) & (w.T > 0)).sum()) * V * 4 + B * k * 4)
+    h2d = sum(t.numel() * t.element_size() for kk, t in pin.items() if t is not None and kk != "q") + q_in_place
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
     assert np.array_equal(host_out["num_accepted"].numpy(), got["num_accepted"])
 
@@ -488,7 +491,9 @@ def run_ours(args):
         "parity": parity,
         "e2e": {"value": B * args.e2e_steps * ws / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-                "path": "specv_verify_sample_host (pinned host buffers, copies + kernel + sync per step)"},
+                "q_bytes_read_in_place": q_in_place,
+                "path": "specv_verify_sample_host (pinned host buffers: logits, x, u, T copied, q read in place "
+                        "by the kernel; kernel + outputs copied back + sync per step)"},
         "gpu_launches": gpu_launches,
         "host_launch_calls": launches_host,
         "mean_num_accepted": float(np.mean(got["num_accepted"])),

@@ -194,7 +194,11 @@ specv_status specv_verify_tree_greedy(specv_handle h, specv_dtype logits_dtype, 
  * memory gives the fastest copies).  The handle copies the inputs to device
  * buffers it owns (allocated on the first call, grown when a larger call
  * comes; this is the one call that may allocate), verifies, copies the three
- * outputs back and synchronises `stream` before returning. */
+ * outputs back and synchronises `stream` before returning.  draft_probs in
+ * page-locked host memory (cudaHostAlloc / cudaHostRegister) is not copied:
+ * the kernel reads in place the entries the rule needs (q at the draft
+ * tokens and the stop rows), with plain loads; pageable draft_probs is
+ * copied like the other inputs. */
 specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, const void *target_logits,
                                       const float *draft_probs, const int32_t *draft_tokens,
                                       const float *uniforms, const float *temperature, int batch,

@@ -230,10 +230,11 @@ specv_status specv_create(specv_handle* out, int device, int max_batch, int max_
     return SPECV_OK;
 }
 
-specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const void* target_logits,
-                                 const float* draft_probs, const int32_t* draft_tokens, const float* uniforms,
-                                 const float* temperature, int batch, int k, int64_t V, int32_t* num_accepted,
-                                 int32_t* out_tokens, int32_t* row_status, const specv_debug* dbg, void* stream) {
+static specv_status verify_sample(specv_handle h, specv_dtype logits_dtype, const void* target_logits,
+                                  const float* draft_probs, const int32_t* draft_tokens, const float* uniforms,
+                                  const float* temperature, int batch, int k, int64_t V, int32_t* num_accepted,
+                                  int32_t* out_tokens, int32_t* row_status, const specv_debug* dbg, void* stream,
+                                  bool q_host) {
     specv_status st = check_sizes(h, logits_dtype, batch, k, V);
     if (st != SPECV_OK) return st;
     if (batch > 0 && (!target_logits || !draft_tokens || !uniforms || !temperature ||
@@ -258,7 +259,16 @@ specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const
     a.V = V;
     a.B = batch;
     a.k = k;
+    a.q_host = q_host ? 1 : 0;
     return run(h, logits_dtype, a, stream);
+}
+
+specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const void* target_logits,
+                                 const float* draft_probs, const int32_t* draft_tokens, const float* uniforms,
+                                 const float* temperature, int batch, int k, int64_t V, int32_t* num_accepted,
+                                 int32_t* out_tokens, int32_t* row_status, const specv_debug* dbg, void* stream) {
+    return verify_sample(h, logits_dtype, target_logits, draft_probs, draft_tokens, uniforms, temperature, batch, k,
+                         V, num_accepted, out_tokens, row_status, dbg, stream, false);
 }
 
 specv_status specv_verify_greedy(specv_handle h, specv_dtype logits_dtype, const void* target_logits,
@@ -364,7 +374,18 @@ specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, 
     auto al = [](size_t x) { return (x + 255) / 256 * 256; };
     const size_t nL = B * (K + 1) * VV * esz, nQ = B * K * VV * 4, nX = B * K * 4, nU = B * (K + 1) * 2 * 4,
                  nT = B * 4, nA = B * 4, nO = B * (K + 1) * 4, nS = B * 4;
-    const size_t nQc = draft_probs ? nQ : 0;  // one-hot drafts: no q to copy
+    // page-locked q is read in place by the kernel: only the entries the rule
+    // needs (the draft tokens' and the stop rows') cross the link
+    const float* q_mapped = nullptr;
+    if (draft_probs) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, draft_probs) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+            pa.devicePointer)
+            q_mapped = static_cast<const float*>(pa.devicePointer);
+        else
+            cudaGetLastError();
+    }
+    const size_t nQc = (draft_probs && !q_mapped) ? nQ : 0;  // one-hot drafts or in-place q: no q to copy
     const size_t need = al(nL) + al(nQc) + al(nX) + al(nU) + al(nT) + al(nA) + al(nO) + al(nS);
     DeviceGuard g(h->device);
     if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
@@ -390,10 +411,11 @@ specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, 
     SPECV_CUDA(cudaMemcpyAsync(dX, draft_tokens, nX, cudaMemcpyHostToDevice, s));
     SPECV_CUDA(cudaMemcpyAsync(dU, uniforms, nU, cudaMemcpyHostToDevice, s));
     SPECV_CUDA(cudaMemcpyAsync(dT, temperature, nT, cudaMemcpyHostToDevice, s));
-    st = specv_verify_sample(h, logits_dtype, dL, draft_probs ? reinterpret_cast<const float*>(dQ) : nullptr,
-                             reinterpret_cast<const int32_t*>(dX), reinterpret_cast<const float*>(dU),
-                             reinterpret_cast<const float*>(dT), batch, k, V, reinterpret_cast<int32_t*>(dA),
-                             reinterpret_cast<int32_t*>(dO), reinterpret_cast<int32_t*>(dS), nullptr, stream);
+    const float* q_arg = q_mapped ? q_mapped : (draft_probs ? reinterpret_cast<const float*>(dQ) : nullptr);
+    st = verify_sample(h, logits_dtype, dL, q_arg, reinterpret_cast<const int32_t*>(dX),
+                       reinterpret_cast<const float*>(dU), reinterpret_cast<const float*>(dT), batch, k, V,
+                       reinterpret_cast<int32_t*>(dA), reinterpret_cast<int32_t*>(dO), reinterpret_cast<int32_t*>(dS),
+                       nullptr, stream, q_mapped != nullptr);
     if (st != SPECV_OK) return st;
     SPECV_CUDA(cudaMemcpyAsync(num_accepted, dA, nA, cudaMemcpyDeviceToHost, s));
     SPECV_CUDA(cudaMemcpyAsync(out_tokens, dO, nO, cudaMemcpyDeviceToHost, s));

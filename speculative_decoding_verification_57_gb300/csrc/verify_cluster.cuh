@@ -95,6 +95,7 @@ struct VerifyArgs {
     int k;
     int slice;               // elements per CTA, a multiple of 64
     int pk;                  // positions per partial array in shared memory (>= k + 1)
+    int q_host;              // q is page-locked host memory read in place: plain loads only, no bulk copies
 };
 
 struct Partial {
@@ -926,7 +927,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         // aligned at the slice start, and whole groups of 8 entries
         const bool la = (reinterpret_cast<uintptr_t>(lg + (lrow + v0) * esz) & 15) == 0;
         const bool qa = qrow && (reinterpret_cast<uintptr_t>(qrow + v0) & 15) == 0;
-        sh.p2fast = la && (sh.mode != MODE_RESIDUAL || qa) && (n % kChunk) == 0;
+        sh.p2fast = la && (sh.mode != MODE_RESIDUAL || (qa && !a.q_host)) && (n % kChunk) == 0;
         sh.ntiles2 = (n + kP2Elems - 1) / kP2Elems;
         // pass-2 slots: [q (residual rows)][logits], one tile each
         sh.loff2 = (sh.mode == MODE_RESIDUAL) ? kP2Elems * 4 : 0;

@@ -209,15 +209,20 @@ def test_deterministic(h):
         np.testing.assert_array_equal(a[key], b[key])
 
 
-def test_host_buffer_entry(h):
+@pytest.mark.parametrize("q_pinned", [True, False])
+def test_host_buffer_entry(h, q_pinned):
+    """Host buffers in: page-locked q is read in place by the kernel,
+    pageable q is copied; both give the oracle's outputs."""
     import torch
 
     import speculative_decoding_verification_57_gb300 as sv
 
     w = W.make_config(2)
     L = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).pin_memory()
-    out = sv.specv_verify_sample_host(h, L, torch.from_numpy(w.q).pin_memory(), torch.from_numpy(w.x).pin_memory(),
-                                      torch.from_numpy(w.u).pin_memory(), torch.from_numpy(w.T).pin_memory())
+    q = torch.from_numpy(w.q)
+    out = sv.specv_verify_sample_host(h, L, q.pin_memory() if q_pinned else q.clone(),
+                                      torch.from_numpy(w.x).pin_memory(), torch.from_numpy(w.u).pin_memory(),
+                                      torch.from_numpy(w.T).pin_memory())
     _acc(compare(w, {kk: v.numpy() for kk, v in out.items()}))
 
 
