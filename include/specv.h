@@ -144,7 +144,8 @@ specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const
  * the residual max(0, p' - q) and the bonus use p'.  The residual and the
  * bonus are drawn over the kept set in vocabulary order; q is read (and
  * checked, bit 32) only there and at the draft tokens.  draft_probs may be
- * NULL (one-hot drafts).  A row whose top_k or top_p is out of range gets
+ * NULL (one-hot drafts), device memory, or page-locked host memory, read in
+ * place (pageable host memory: SPECV_ERR_INVALID_ARGUMENT).  A row whose top_k or top_p is out of range gets
  * row_status bit 1024 and emits nothing.  Rows with temperature 0 take the
  * greedy rule (the filters keep the argmax).  Other arguments and bits as
  * for specv_verify_sample; no debug outputs.  One thread-block cluster of

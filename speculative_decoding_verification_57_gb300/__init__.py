@@ -183,14 +183,20 @@ def specv_verify_greedy(h: Handle, logits, x, *, out=None, stream=None):
 
 def specv_verify_sample_filtered(h: Handle, logits, q, x, u, T, top_k, top_p, *, out=None, stream=None):
     """Sampled verification with top-k / top-p applied to the target rows:
-    as specv_verify_sample (q may be None: one-hot drafts), plus top_k [B]
-    int32 in 1..64 and top_p [B] fp32 in (0, 1], CUDA tensors."""
+    as specv_verify_sample (q may be None: one-hot drafts, or a pinned CPU
+    tensor, read in place), plus top_k [B] int32 in 1..64 and top_p [B]
+    fp32 in (0, 1], CUDA tensors."""
     torch = _torch()
     B, k1, V = logits.shape
     k = k1 - 1
     dt = _logits_dtype(logits)
     _dev(logits, logits.dtype, "logits")
-    pq = None if q is None else _dev(q, torch.float32, "q", (B, k, V))
+    if q is not None and not q.is_cuda:
+        if not q.is_pinned() or q.dtype != torch.float32 or not q.is_contiguous() or tuple(q.shape) != (B, k, V):
+            raise ValueError("a CPU q must be a pinned, contiguous float32 tensor of shape [B, k, V]")
+        pq = q.data_ptr()
+    else:
+        pq = None if q is None else _dev(q, torch.float32, "q", (B, k, V))
     px = _dev(x, torch.int32, "x", (B, k))
     pu = _dev(u, torch.float32, "u", (B, k + 1, 2))
     pt = _dev(T, torch.float32, "T", (B,))

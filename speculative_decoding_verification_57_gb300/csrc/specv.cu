@@ -303,9 +303,24 @@ specv_status specv_verify_sample_filtered(specv_handle h, specv_dtype logits_dty
     if (batch == 0) return SPECV_OK;
     DeviceGuard g(h->device);
     if (!g.ok) return cuda_fail(cudaErrorInvalidDevice, "cudaSetDevice");
+    // draft_probs may be page-locked host memory: the kernel reads the few
+    // entries it needs in place (plain loads); pageable host memory is refused
+    const float* q = draft_probs;
+    if (q) {
+        cudaPointerAttributes pa;
+        if (cudaPointerGetAttributes(&pa, q) != cudaSuccess) {
+            cudaGetLastError();
+            return SPECV_ERR_INVALID_ARGUMENT;
+        }
+        if (pa.type == cudaMemoryTypeUnregistered) return SPECV_ERR_INVALID_ARGUMENT;
+        if (pa.type == cudaMemoryTypeHost) {
+            if (!pa.devicePointer) return SPECV_ERR_INVALID_ARGUMENT;
+            q = static_cast<const float*>(pa.devicePointer);
+        }
+    }
     VerifyArgs a = {};
     a.logits = target_logits;
-    a.q = draft_probs;
+    a.q = q;
     a.x = draft_tokens;
     a.u = uniforms;
     a.temp = temperature;

@@ -116,3 +116,21 @@ def test_filtered_ties_and_degenerate_rows(h, dtype):
     w = W.Workload(w.name, w.dtype, logits, w.q, w.x, w.u, w.T)
     for K, p in [(64, 1.0), (13, 0.8), (1, 1.0)]:
         _check(w, _run(h, w, [K] * B, [p] * B), [K] * B, [p] * B)
+
+
+def test_filtered_pinned_host_q(h):
+    """q in page-locked host memory is read in place."""
+    import torch
+
+    import speculative_decoding_verification_57_gb300 as sv
+    from parity import to_device
+
+    w = W.make_random(name="fpin", B=16, k=4, V=32000, dtype="bf16", seed=21, logit_sigma=3.0, draft_sigma=0.7,
+                      temperature=0.9, spike=4.0, spike_mode="position", greedy_rows=2)
+    L, _, x, u, T = to_device(w, "cuda:0")
+    K, P = [40] * 16, [0.9] * 16
+    out = sv.specv_verify_sample_filtered(h, L, torch.from_numpy(w.q).pin_memory(), x, u, T,
+                                          torch.tensor(K, dtype=torch.int32, device="cuda:0"),
+                                          torch.tensor(P, dtype=torch.float32, device="cuda:0"))
+    torch.cuda.synchronize()
+    assert _check(w, {kk: v.cpu().numpy() for kk, v in out.items()}, K, P)[0] <= 1
