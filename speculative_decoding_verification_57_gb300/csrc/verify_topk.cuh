@@ -656,7 +656,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
         }
         if (!st) {
             // weights on the kept set: max(0, e - S_P q) at a rejection, e for the bonus
-            const bool v0 = lane < np, v1 = lane + 32 < np;
+            // kept: ranks below np that hold an entry (with V < 64 the list ends in padding)
+            const bool v0 = lane < np && c0.i != 0x7fffffff, v1 = lane + 32 < np && c1.i != 0x7fffffff;
             df w0 = v0 ? e0 : df_make(0.0f), w1 = v1 ? e1 : df_make(0.0f);
             if (j < k) {
                 const int xj = sh.xs[j];

@@ -134,3 +134,13 @@ def test_filtered_pinned_host_q(h):
                                           torch.tensor(P, dtype=torch.float32, device="cuda:0"))
     torch.cuda.synchronize()
     assert _check(w, {kk: v.cpu().numpy() for kk, v in out.items()}, K, P)[0] <= 1
+
+
+@pytest.mark.parametrize("V,dtype,K,p,k", [(50, "f32", 64, 1.0, 3), (37, "bf16", 40, 0.5, 2), (2049, "bf16", 64, 0.05, 1),
+                                           (8, "f32", 3, 1.0, 6)])
+def test_filtered_small_vocabularies(h, V, dtype, K, p, k):
+    """V below the 64 kept entries (padded lists), top-p cutting to a single
+    entry, one draft, tiny vocabularies."""
+    w = W.make_random(name="fsmall", B=20, k=k, V=V, dtype=dtype, seed=V * 7 + K, logit_sigma=2.0, draft_sigma=0.8,
+                      temperature=1.0, greedy_rows=2)
+    assert _check(w, _run(h, w, [K] * 20, [p] * 20), [K] * 20, [p] * 20)[0] <= 1
