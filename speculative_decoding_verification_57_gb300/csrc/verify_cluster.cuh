@@ -718,7 +718,13 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                         s = (m == -INFINITY) ? s * 0.0f : s * ex2((m - lmax) * c);
                         m = lmax;
                     }
-                    const f2 mm = pack2(m, m), cc = pack2(c, c);
+                    // exponents as one fma a pair: l c - r with r = m c rounded; the
+                    // rounding error of r (err = m c - r, exact through an fma) scales
+                    // every term of the tile alike and is taken out once, to first
+                    // order (|err| <= ulp(m c) / 2, so the neglected term is ~1e-12)
+                    const float rr = m * c;
+                    const float err = fmaf(m, c, -rr);
+                    const f2 cc = pack2(c, c), nr = pack2(-rr, -rr);
                     f2 acc = pack2(0.0f, 0.0f);
 #pragma unroll
                     for (int r = 0; r < kPer; ++r) {
@@ -726,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                         if (BF16) {
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
-                                const f2 d = mul2(sub2(pack2(bf16_lo(ws[q4]), bf16_hi(ws[q4])), mm), cc);
+                                const f2 d = fma2(pack2(bf16_lo(ws[q4]), bf16_hi(ws[q4])), cc, nr);
                                 float d0, d1;
                                 unpack2(d, d0, d1);
                                 acc = add2(acc, pack2(ex2(d0), ex2(d1)));
@@ -734,8 +740,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                         } else {
 #pragma unroll
                             for (int q4 = 0; q4 < 4; q4 += 2) {
-                                const f2 d =
-                                    mul2(sub2(pack2(__uint_as_float(ws[q4]), __uint_as_float(ws[q4 + 1])), mm), cc);
+                                const f2 d = fma2(pack2(__uint_as_float(ws[q4]), __uint_as_float(ws[q4 + 1])), cc, nr);
                                 float d0, d1;
                                 unpack2(d, d0, d1);
                                 acc = add2(acc, pack2(ex2(d0), ex2(d1)));
@@ -744,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                     }
                     float a0, a1;
                     unpack2(acc, a0, a1);
-                    s += a0 + a1;
+                    s += (a0 + a1) * fmaf(-err, kLn2, 1.0f);  // back to the scale of m
                 }
             }
             if (tid == 0)
