@@ -144,3 +144,31 @@ def test_filtered_small_vocabularies(h, V, dtype, K, p, k):
     w = W.make_random(name="fsmall", B=20, k=k, V=V, dtype=dtype, seed=V * 7 + K, logit_sigma=2.0, draft_sigma=0.8,
                       temperature=1.0, greedy_rows=2)
     assert _check(w, _run(h, w, [K] * 20, [p] * 20), [K] * 20, [p] * 20)[0] <= 1
+
+
+def test_filtered_refuses_pageable_q(h):
+    """A pageable CPU q is refused before launch (the kernel never sees it)."""
+    import ctypes
+
+    import torch
+
+    import speculative_decoding_verification_57_gb300 as sv
+    from speculative_decoding_verification_57_gb300 import _lib
+    from parity import to_device
+
+    w = W.make_random(name="fpage", B=4, k=2, V=4096, dtype="bf16", seed=5, logit_sigma=2.0, draft_sigma=0.5,
+                      temperature=1.0)
+    L, _, x, u, T = to_device(w, "cuda:0")
+    q = torch.from_numpy(w.q)  # pageable
+    tk = torch.full((4,), 10, dtype=torch.int32, device="cuda:0")
+    tp = torch.full((4,), 1.0, dtype=torch.float32, device="cuda:0")
+    outs = [torch.empty(4, dtype=torch.int32, device="cuda:0"), torch.empty((4, 3), dtype=torch.int32, device="cuda:0"),
+            torch.empty(4, dtype=torch.int32, device="cuda:0")]
+    st = _lib.load().specv_verify_sample_filtered(
+        h.ptr, sv.SPECV_BF16, ctypes.c_void_p(L.data_ptr()), ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(x.data_ptr()),
+        ctypes.c_void_p(u.data_ptr()), ctypes.c_void_p(T.data_ptr()), ctypes.c_void_p(tk.data_ptr()),
+        ctypes.c_void_p(tp.data_ptr()), 4, 2, 4096, ctypes.c_void_p(outs[0].data_ptr()),
+        ctypes.c_void_p(outs[1].data_ptr()), ctypes.c_void_p(outs[2].data_ptr()), None)
+    assert st == 1  # SPECV_ERR_INVALID_ARGUMENT
+    with pytest.raises(ValueError):
+        sv.specv_verify_sample_filtered(h, L, q, x, u, T, tk, tp)
