@@ -29,7 +29,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 WORKLOAD = "verify B=64 k=5 V=128256 bf16 T=1 (Llama-3 vocabulary, +8 spike, q=softmax(L+N(0,1)))"
-CONFIG_INDEX = 3
+WORKLOAD_NAME = "benchmark"
 N_SETS = 4
 NOMINAL_HBM_GBS = 8000.0
 
@@ -277,7 +277,7 @@ def run_reference(args):
         return 0
     from speculative_decoding_verification_57_gb300 import workloads as W
 
-    w = W.make_config(CONFIG_INDEX)
+    w = W.make_workload(WORKLOAD_NAME)
     import oracle
 
     cores = host_cores()
@@ -333,7 +333,7 @@ def run_ours(args):
         return run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src)
     if args.variant == "rollback":
         return run_rollback(args, sv, dev, rank, ws, local, hbm_peak, peak_src)
-    w = W.make_config(CONFIG_INDEX, seed=57000 + CONFIG_INDEX + 1000 * rank)
+    w = W.make_workload(WORKLOAD_NAME, seed=W.WORKLOADS[WORKLOAD_NAME][1] + 1000 * rank)
     onehot = args.variant == "onehot"
     if onehot:
         w = W.Workload(w.name, w.dtype, w.logits, None, w.x, w.u, w.T)
@@ -640,7 +640,7 @@ def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
 
     from speculative_decoding_verification_57_gb300 import workloads as W
 
-    w = W.make_config(CONFIG_INDEX, seed=57000 + CONFIG_INDEX + 1000 * rank)
+    w = W.make_workload(WORKLOAD_NAME, seed=W.WORKLOADS[WORKLOAD_NAME][1] + 1000 * rank)
     B, k, V = w.B, w.k, w.V
     tk = np.full(B, FILTER_TOP_K, np.int32)
     tp = np.full(B, FILTER_TOP_P, np.float32)

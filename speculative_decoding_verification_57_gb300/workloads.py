@@ -14,17 +14,18 @@ models around the verify step:
 * the verify step's uniforms U[b, i, slot] in [0, 1) and per-row
   temperatures.
 
-Every configuration uses ``numpy.random.default_rng`` sub-streams spawned
+Every workload uses ``numpy.random.default_rng`` sub-streams spawned
 from one ``SeedSequence``: one each for target logits, draft noise, draft
 token uniforms and verify uniforms, so that changing one never shifts the
 others.  Logit values are drawn in float64 and rounded to the stored type
 (bf16 by round-to-nearest-even of the float32 value).
 
-The five named configurations follow the workloads the verify step is
-measured on: a V=1000 toy, V=32000 bf16 with a Zipf(1.1)-ranked boost, the
-Llama-3 vocabulary (128,256 entries, "Speculative decoding." lesson, "First:
-what an output distribution is") at B=64 and at B=256 with half the rows
-greedy, and an fp32 V=151,936 case at small batch.
+The five named workloads (``make_workload``) follow the shapes the verify
+step is measured on: ``toy`` (V=1000 fp32), ``zipf`` (V=32000 bf16 with a
+Zipf(1.1)-ranked boost), ``benchmark`` and ``mixed`` (the Llama-3 vocabulary,
+128,256 entries, "Speculative decoding." lesson, "First: what an output
+distribution is", at B=64, and at B=256 with half the rows greedy), and
+``split_v`` (an fp32 V=151,936 case at small batch).
 """
 from __future__ import annotations
 
@@ -34,8 +35,8 @@ import numpy as np
 
 __all__ = [
     "Workload",
-    "CONFIGS",
-    "make_config",
+    "WORKLOADS",
+    "make_workload",
     "make_random",
     "make_from_distributions",
     "f32_to_bf16_bits",
@@ -209,41 +210,50 @@ def make_from_distributions(
     return Workload(name, "f32", logits, q, x, u, T)
 
 
-def _c1(seed):
+def _toy(seed):
     return make_random(name="toy B=1 k=4 V=1000 fp32", B=1, k=4, V=1000, dtype="f32",
                        seed=seed, logit_sigma=2.0, draft_sigma=1.0, temperature=1.0)
 
 
-def _c2(seed):
+def _zipf(seed):
     return make_random(name="B=8 k=4 V=32000 bf16 zipf", B=8, k=4, V=32000, dtype="bf16",
                        seed=seed, logit_sigma=3.0, draft_sigma=1.5, temperature=0.8,
                        spike=6.0, spike_mode="zipf")
 
 
-def _c3(seed):
+def _benchmark(seed):
     return make_random(name="B=64 k=5 V=128256 bf16", B=64, k=5, V=128256, dtype="bf16",
                        seed=seed, logit_sigma=3.0, draft_sigma=1.0, temperature=1.0,
                        spike=8.0, spike_mode="position")
 
 
-def _c4(seed):
+def _mixed(seed):
     sig = np.random.default_rng(np.random.SeedSequence([seed, 1])).uniform(0.5, 3.0, size=256)
     return make_random(name="B=256 k=8 V=128256 bf16 half greedy", B=256, k=8, V=128256,
                        dtype="bf16", seed=seed, logit_sigma=3.0, draft_sigma=sig,
                        temperature=0.7, spike=8.0, spike_mode="position", greedy_rows=128)
 
 
-def _c5(seed):
+def _split_v(seed):
     return make_random(name="B=16 k=16 V=151936 fp32", B=16, k=16, V=151936, dtype="f32",
                        seed=seed, logit_sigma=4.0, draft_sigma=2.0, temperature=1.0)
 
 
-CONFIGS = {1: _c1, 2: _c2, 3: _c3, 4: _c4, 5: _c5}
+# name -> (builder, default seed)
+WORKLOADS = {
+    "toy": (_toy, 57001),
+    "zipf": (_zipf, 57002),
+    "benchmark": (_benchmark, 57003),
+    "mixed": (_mixed, 57004),
+    "split_v": (_split_v, 57005),
+}
 
 
-def make_config(index: int, seed: int | None = None) -> Workload:
-    """Named configuration ``index`` (1..5); default seed 57000 + index."""
-    return CONFIGS[index](57000 + index if seed is None else seed)
+def make_workload(name: str, seed: int | None = None) -> Workload:
+    """The named workload (``toy``, ``zipf``, ``benchmark``, ``mixed``,
+    ``split_v``), from its default seed unless one is given."""
+    build, default_seed = WORKLOADS[name]
+    return build(default_seed if seed is None else seed)
 
 
 def make_rollback_batch(seed: int, B: int, k: int, block_size: int, max_blocks: int):

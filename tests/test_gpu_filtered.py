@@ -68,7 +68,7 @@ def test_filtered_one_hot_and_mixed_filters(h):
 
 def test_filtered_many_uniforms(h):
     """The benchmark logits, top_k 40 and top_p 0.95, 20 uniform sets."""
-    base = W.make_config(3)
+    base = W.make_workload("benchmark")
     rng = np.random.default_rng(6)
     mism = 0
     for r in range(20):

@@ -32,19 +32,19 @@ def _acc(stats):
     return stats
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
-def test_named_config_parity(h, cfg):
-    w = W.make_config(cfg)
+@pytest.mark.parametrize("name", ["zipf", "benchmark", "mixed", "split_v"])
+def test_named_workload_parity(h, name):
+    w = W.make_workload(name)
     got = run_gpu(h, w, debug=True)
     stats = _acc(compare(w, got, check_debug=True))
-    print(cfg, stats)
+    print(name, stats)
 
 
 def test_toy_config_2000_rounds(h):
     """The toy workload: 2000 independent rounds of B=1, V=1000, fp32."""
     mism = 0
     for r in range(2000):
-        w = W.make_config(1, seed=57001 + 1000 * r)
+        w = W.make_workload("toy", seed=57001 + 1000 * r)
         got = run_gpu(h, w)
         mism += compare(w, got)["mismatched"]
     assert mism <= 1
@@ -202,7 +202,7 @@ def test_masked_vocabulary(h, V, dtype):
 
 
 def test_deterministic(h):
-    w = W.make_config(2)
+    w = W.make_workload("zipf")
     a = run_gpu(h, w, debug=True)
     b = run_gpu(h, w, debug=True)
     for key in a:
@@ -217,7 +217,7 @@ def test_host_buffer_entry(h, q_pinned):
 
     import speculative_decoding_verification_57_gb300 as sv
 
-    w = W.make_config(2)
+    w = W.make_workload("zipf")
     L = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).pin_memory()
     q = torch.from_numpy(w.q)
     out = sv.specv_verify_sample_host(h, L, q.pin_memory() if q_pinned else q.clone(),
@@ -243,7 +243,7 @@ def test_bench_workload_many_uniforms(h):
     launch configuration, with 40 independent uniform sets: every row
     matches the oracle except at flagged boundaries, and disagreements stay
     below 1e-4 of all rows."""
-    base = W.make_config(3)
+    base = W.make_workload("benchmark")
     rng = np.random.default_rng(99)
     mism = rows = 0
     for r in range(40):
@@ -274,7 +274,7 @@ def test_one_hot_drafts(h, V, k, B, dtype):
 
 def test_one_hot_many_uniforms(h):
     """The benchmark logits with one-hot drafts over 20 uniform sets."""
-    base = W.make_config(3)
+    base = W.make_workload("benchmark")
     rng = np.random.default_rng(5)
     for r in range(20):
         w = W.Workload(base.name, base.dtype, base.logits, None, base.x,

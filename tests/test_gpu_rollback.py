@@ -74,7 +74,7 @@ def test_rollback_after_verify(h):
     from speculative_decoding_verification_57_gb300 import workloads as W
     from parity import to_device
 
-    w = W.make_config(2)
+    w = W.make_workload("zipf")
     L, q, x, u, T = to_device(w, "cuda:0")
     hv = sv.specv_create(0, max_batch=w.B, max_k=w.k, vocab=w.V)
     out = sv.specv_verify_sample(hv, L, q, x, u, T)
