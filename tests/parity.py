@@ -3,9 +3,11 @@
 Integer outputs (num_accepted, out_tokens, row_status) must be equal.  The
 one exception is a row whose uniform lies within 1e-6 of a decision edge of
 the oracle (its ``boundary`` flag): there the two precisions may land on
-either side, so the GPU outcome must instead equal the oracle's outcome with
-that uniform nudged to either side of the edge.  Such disagreements are
-counted; intermediate values are compared at 1e-5 relative.
+either side, so the GPU outcome must instead equal the oracle's outcome for
+that uniform moved by at most 1e-6 (the accept test: nudged to either side
+of the edge; the draw: found by bisection, the token being non-decreasing in
+the uniform).  Such disagreements are counted; intermediate values are
+compared at 1e-5 relative.
 """
 import numpy as np
 
@@ -57,15 +59,39 @@ def compare(w, got, ref=None, *, check_debug=False):
     for b in mism:
         idx = int(ref["boundary"][b]) - 1
         i, slot = idx // 2, idx % 2
-        alts = set()
         sub = (w.logits[b:b + 1], None if w.q is None else w.q[b:b + 1], w.x[b:b + 1], w.T[b:b + 1])
-        for d in NUDGES:
-            for sgn in (-1.0, 1.0):
-                uu = w.u[b:b + 1].copy()
-                uu[0, i, slot] = np.float32(np.clip(uu[0, i, slot] + sgn * d, 0.0, np.nextafter(np.float32(1), np.float32(0))))
-                r = oracle.verify(sub[0], sub[1], sub[2], uu, sub[3])
-                alts.add(_outcome(r, 0))
-        assert _outcome(got, b) in alts, (b, _outcome(got, b), alts)
+        top = np.nextafter(np.float32(1), np.float32(0))
+
+        def outcome_at(u_val):
+            uu = w.u[b:b + 1].copy()
+            uu[0, i, slot] = np.float32(np.clip(u_val, 0.0, top))
+            return _outcome(oracle.verify(sub[0], sub[1], sub[2], uu, sub[3]), 0)
+
+        want = _outcome(got, b)
+        have = _outcome(ref, b)
+        u0 = float(w.u[b, i, slot])
+        j = have[0]
+        same_but_draw = (want[0] == j and want[2] == have[2]
+                         and all(want[1][t] == have[1][t] for t in range(len(want[1])) if t != j))
+        if slot == 1 and same_but_draw:
+            # the draw: the token is non-decreasing in u, so some u' within 1e-6
+            # gives the GPU's token iff bisection over [u - 1e-6, u + 1e-6] finds it
+            tok = want[1][j]
+            lo, hi = np.float32(max(0.0, u0 - 1e-6)), np.float32(min(float(top), u0 + 1e-6))
+            t_lo, t_hi = outcome_at(lo)[1][j], outcome_at(hi)[1][j]
+            found = tok in (t_lo, t_hi)
+            while not found and t_lo < tok < t_hi:
+                mid = np.float32((np.float64(lo) + np.float64(hi)) / 2)
+                if mid <= lo or mid >= hi:
+                    break
+                t_mid = outcome_at(mid)[1][j]
+                found = t_mid == tok
+                lo, hi = (mid, hi) if t_mid < tok else (lo, mid)
+            assert found, (b, want, have, "no draw uniform within 1e-6 gives the GPU's token")
+        else:
+            # the accept test: two outcomes, either side of the edge
+            alts = {outcome_at(u0 + sgn * d) for d in NUDGES for sgn in (-1.0, 1.0)}
+            assert want in alts, (b, want, alts)
     if check_debug:
         ok = same & ((ref["row_status"] & oracle.ST_ERROR_MASK) == 0)
         greedy = w.T == 0

@@ -1,0 +1,55 @@
+"""The parity checker's treatment of flagged rows (CPU): a GPU token that
+the oracle gives for some draw uniform within 1e-6 is accepted, one that no
+such uniform gives is refused."""
+import numpy as np
+import pytest
+
+import oracle
+from parity import compare
+from speculative_decoding_verification_57_gb300 import workloads as W
+
+
+def _edge_row():
+    """The toy workload with row 0's draw uniform moved onto a CDF edge of
+    its stop position (found by bisection on the oracle)."""
+    w = W.make_workload("toy")
+    ref = oracle.verify(w.logits, w.q, w.x, w.u, w.T)
+    j = int(ref["num_accepted"][0])
+    lo, hi = np.float32(0.0), np.float32(0.999)
+    u = w.u.copy()
+
+    def tok(v):
+        u[0, j, 1] = v
+        return int(oracle.verify(w.logits, w.q, w.x, u, w.T)["out_tokens"][0][j])
+
+    t_lo = tok(lo)
+    for _ in range(60):  # narrow to two adjacent float32 values on either side of an edge
+        mid = np.float32((np.float64(lo) + np.float64(hi)) / 2)
+        if mid <= lo or mid >= hi:
+            break
+        if tok(mid) == t_lo:
+            lo = mid
+        else:
+            hi = mid
+    a, b = tok(lo), tok(hi)
+    u[0, j, 1] = lo  # the row sits at the edge, on a's side
+    return W.Workload(w.name, w.dtype, w.logits, w.q, w.x, u, w.T), j, a, b
+
+
+def test_flagged_draw_across_the_edge_is_accepted():
+    w, j, a, b = _edge_row()
+    ref = oracle.verify(w.logits, w.q, w.x, w.u, w.T)
+    assert ref["boundary"][0] != 0 and a != b
+    got = {kk: np.array(v, copy=True) for kk, v in ref.items()}
+    got["out_tokens"][0][j] = b  # the other side of the edge
+    st = compare(w, got, ref=ref)
+    assert st["mismatched"] == 1
+
+
+def test_flagged_draw_far_from_the_edge_is_refused():
+    w, j, a, b = _edge_row()
+    ref = oracle.verify(w.logits, w.q, w.x, w.u, w.T)
+    got = {kk: np.array(v, copy=True) for kk, v in ref.items()}
+    got["out_tokens"][0][j] = b + 1 if b + 1 < w.V else a - 1  # a whole slot further
+    with pytest.raises(AssertionError):
+        compare(w, got, ref=ref)
