@@ -1,6 +1,6 @@
-"""The parity checker's treatment of flagged rows (CPU): a GPU token that
-the oracle gives for some draw uniform within 1e-6 is accepted, one that no
-such uniform gives is refused."""
+"""The parity checker's treatment of flagged rows (CPU): a GPU token whose
+CDF slot meets [u - 1e-6, u + 1e-6] is accepted, one a whole slot further
+is refused."""
 import numpy as np
 import pytest
 
