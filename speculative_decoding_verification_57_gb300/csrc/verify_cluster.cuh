@@ -262,7 +262,7 @@ __device__ __forceinline__ void df2_add(f2& H, f2& L, f2 X) {
 // One lane's sums over its 32 consecutive stop-row entries of a tile.
 // Weights are in e-units (the row's sum of exponentials times p): residual
 // mode r = max(0, e - s1 q), bonus / fallback mode e.  Small entries are
-// summed in floats, eight at a time, and folded into the pairs; large entries
+// summed in floats, sixteen at a time, and folded into the pairs; large entries
 // (estimate above thr) are left out here and added exactly afterwards.
 struct LaneAcc {
     f2 wh, wl;       // (weights, sum of e) as (hi, lo) pairs, packed
@@ -330,8 +330,8 @@ __device__ __forceinline__ void sweep_lane(LaneAcc& A, const unsigned char* ls, 
         } else {
             sw = add2(sw, add2(ES0, ES1));
         }
-        if (st & 1) {
-            // fold the eight entries of the last two pieces into the pairs
+        if ((st & 3) == 3) {
+            // fold the sixteen entries of the last four pieces into the pairs
             float a0, a1, b0, b1;
             unpack2(sw, a0, a1);
             unpack2(se, b0, b1);
