@@ -64,6 +64,66 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
     return before + incl - v;
 }
 
+// Batches of up to kRollbackThreads * kRollbackCached rows: each thread keeps
+// its rows in registers, loads them all before the scan and every table
+// entry it pops (the first two a row) before its first store, so the
+// loads of a run overlap instead of queueing behind one another.
+constexpr int kRollbackCached = 4;
+
+__device__ __forceinline__ void rollback_cached(const RollbackArgs& r, int lo, int hi, long long* warp_sums) {
+    int cnt[kRollbackCached], tgt[kRollbackCached], nbv[kRollbackCached];
+    long long mine = 0;
+#pragma unroll
+    for (int t = 0; t < kRollbackCached; ++t) {
+        const int b = lo + t;
+        cnt[t] = 0;
+        tgt[t] = 0;
+        nbv[t] = 0;
+        if (b < hi) {
+            int needed = 0;
+            cnt[t] = rollback_count(r, b, tgt[t], needed);
+            nbv[t] = r.num_blocks[b];
+            mine += cnt[t] > 0 ? cnt[t] : 0;
+        }
+    }
+    long long total = 0;
+    const long long before = block_exclusive_scan(mine, warp_sums, &total);
+    const long long base0 = *r.free_count;
+    __syncthreads();  // every thread has read free_count before thread 0 writes it
+    if (base0 + total > r.capacity) {
+        if (r.row_status)
+            for (int b = lo; b < hi; ++b) r.row_status[b] = RB_NO_ROOM;
+        return;
+    }
+    int v0[kRollbackCached], v1[kRollbackCached];  // the first two blocks each row pops
+#pragma unroll
+    for (int t = 0; t < kRollbackCached; ++t) {
+        const int32_t* table = r.block_tables + static_cast<long long>(lo + t) * r.max_blocks;
+        v0[t] = cnt[t] >= 1 ? table[nbv[t] - 1] : -1;
+        v1[t] = cnt[t] >= 2 ? table[nbv[t] - 2] : -1;
+    }
+    long long off = base0 + before;
+#pragma unroll
+    for (int t = 0; t < kRollbackCached; ++t) {
+        const int b = lo + t;
+        if (b >= hi) continue;
+        if (cnt[t] < 0) {
+            if (r.row_status) r.row_status[b] = RB_INVALID;
+            continue;
+        }
+        int32_t* table = r.block_tables + static_cast<long long>(b) * r.max_blocks;
+        if (cnt[t] >= 1) r.free_list[off] = v0[t];
+        if (cnt[t] >= 2) r.free_list[off + 1] = v1[t];
+        for (int i = 2; i < cnt[t]; ++i) r.free_list[off + i] = table[nbv[t] - 1 - i];
+        for (int i = 0; i < cnt[t]; ++i) table[nbv[t] - 1 - i] = -1;
+        off += cnt[t];
+        r.num_blocks[b] = nbv[t] - cnt[t];
+        r.seq_lens[b] = tgt[t];
+        if (r.row_status) r.row_status[b] = 0;
+    }
+    if (threadIdx.x == 0) *r.free_count = static_cast<int32_t>(base0 + total);
+}
+
 __global__ void __launch_bounds__(kRollbackThreads, 1) rollback_kernel(const RollbackArgs r) {
     __shared__ long long warp_sums[32];
     // thread t owns rows [lo, hi): contiguous runs in thread order keep batch order
@@ -71,6 +131,10 @@ __global__ void __launch_bounds__(kRollbackThreads, 1) rollback_kernel(const Rol
     const long long lo0 = static_cast<long long>(threadIdx.x) * per;
     const int lo = static_cast<int>(lo0 < r.B ? lo0 : r.B);
     const int hi = static_cast<int>(lo0 + per < r.B ? lo0 + per : r.B);
+    if (per <= kRollbackCached) {  // uniform over the block
+        rollback_cached(r, lo, hi, warp_sums);
+        return;
+    }
     // 1. the run's count, its place in the free list, and the total
     long long mine = 0;
     for (int b = lo; b < hi; ++b) {

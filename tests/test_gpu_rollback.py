@@ -55,6 +55,25 @@ def test_rollback_matches_oracle(h, B, k, bs, mb):
     _same(got, ref)
 
 
+@pytest.mark.parametrize("B,k,bs,mb", [(4097, 6, 4, 10), (9000, 8, 2, 12)])
+def test_rollback_large_batches(B, k, bs, mb):
+    """Batches past 4096 rows (more than four rows a thread)."""
+    import speculative_decoding_verification_57_gb300 as sv
+
+    hl = sv.specv_create(0, max_batch=B, max_k=k, vocab=1000)
+    try:
+        rng = np.random.default_rng(B)
+        na, lens, tables, nb = _random_batch(rng, B, k, bs, mb)
+        na[::11] = -1  # some invalid rows
+        cap = B * mb
+        free = np.full(cap, -5, np.int32)
+        ref = oracle.rollback(na, k, lens, tables, nb, bs, free, 0)
+        got = _gpu(hl, na, k, lens, tables, nb, bs, free, 0)
+        _same(got, ref)
+    finally:
+        sv.specv_destroy(hl)
+
+
 def test_rollback_no_room(h):
     rng = np.random.default_rng(1)
     na, lens, tables, nb = _random_batch(rng, 64, 4, 2, 10)
