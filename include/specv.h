@@ -116,7 +116,9 @@ typedef struct {
 } specv_debug;
 
 /* Create a handle on CUDA device `device` for batches up to max_batch rows,
- * 1 <= k <= max_k (max_k <= 32) and vocabularies up to `vocab` entries.
+ * 1 <= k <= max_k (1 <= max_k <= 31: positions 0..k fit one warp) and
+ * vocabularies up to `vocab` entries (1 <= vocab <= 262144: at most 16 CTAs
+ * of 16384 entries a position).  Other values: SPECV_ERR_INVALID_ARGUMENT.
  * Queries the device; allocates no device memory.  Returns
  * SPECV_ERR_UNSUPPORTED if the device is not compute capability 10.3. */
 specv_status specv_create(specv_handle *out, int device, int max_batch, int max_k, int64_t vocab);

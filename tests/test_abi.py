@@ -60,6 +60,9 @@ def test_argument_errors_need_no_device(lib):
     assert lib.specv_create(None, 0, 1, 4, 100) == 1
     assert lib.specv_create(ctypes.byref(h), 0, 1, 0, 100) == 1  # k < 1
     assert lib.specv_create(ctypes.byref(h), 0, 1, 32, 100) == 1  # k above 31
+    assert lib.specv_create(ctypes.byref(h), 0, 1, 4, 0) == 1  # empty vocabulary
+    assert lib.specv_create(ctypes.byref(h), 0, 1, 4, 262145) == 1  # vocabulary above 16 x 16384
+    assert lib.specv_create(ctypes.byref(h), 0, -1, 4, 100) == 1  # negative batch
 
 
 def test_kernels_are_built_for_sm_103a():
