@@ -147,11 +147,11 @@ specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const
  * bonus are drawn over the kept set in vocabulary order; q is read (and
  * checked, bit 32) only there and at the draft tokens.  draft_probs may be
  * NULL (one-hot drafts), device memory, or page-locked host memory, read in
- * place (pageable host memory: SPECV_ERR_INVALID_ARGUMENT).  A row whose top_k or top_p is out of range gets
- * row_status bit 1024 and emits nothing.  Rows with temperature 0 take the
- * greedy rule (the filters keep the argmax).  Other arguments and bits as
- * for specv_verify_sample; no debug outputs.  One thread-block cluster of
- * min(k + 1, 8) CTAs per row. */
+ * place (pageable host memory: SPECV_ERR_INVALID_ARGUMENT).  A row whose
+ * top_k or top_p is out of range gets row_status bit 1024 and emits
+ * nothing.  Rows with temperature 0 take the greedy rule (the filters keep
+ * the argmax).  Other arguments and bits as for specv_verify_sample; no
+ * debug outputs.  One thread-block cluster of min(k + 1, 8) CTAs per row. */
 specv_status specv_verify_sample_filtered(specv_handle h, specv_dtype logits_dtype, const void *target_logits,
                                           const float *draft_probs, const int32_t *draft_tokens,
                                           const float *uniforms, const float *temperature, const int32_t *top_k,
