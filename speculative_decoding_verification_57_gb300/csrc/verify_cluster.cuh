@@ -224,6 +224,46 @@ __device__ __forceinline__ df exact_weight(float l, float qv, int md, const RowC
     return (r.hi + r.lo > 0.0f) ? r : df_make(0.0f);
 }
 
+// precise_e for two entries at once: the same steps and roundings, lane by
+// lane, with the f32x2 instructions where a step has one.  Returns the pairs
+// as (EH, EL) = ((e0.hi, e1.hi), (e0.lo, e1.lo)).
+__device__ __forceinline__ void precise_e_x2(f2 L, const RowConst& rc, const float2* tab, f2& EH, f2& EL) {
+    // two-sum L - M
+    const f2 NM = pack2(-rc.M, -rc.M);
+    const f2 DH = add2(L, NM);
+    const f2 BB = sub2(DH, L);
+    const f2 DL = add2(sub2(L, sub2(DH, BB)), sub2(NM, BB));
+    // x = (DH + DL) (ch + cl): NX = -xh exactly (round to nearest is symmetric)
+    const f2 CH = pack2(rc.ch, rc.ch);
+    const f2 NX = mul2(DH, pack2(-rc.ch, -rc.ch));
+    const f2 XL = fma2(DL, CH, fma2(DH, pack2(rc.cl, rc.cl), fma2(DH, CH, NX)));
+    // exp2dd, both lanes
+    float n0, n1;
+    unpack2(NX, n0, n1);
+    const float xh0 = fmaxf(-n0, -125.0f), xh1 = fmaxf(-n1, -125.0f);
+    const float kf0 = rintf(xh0 * 128.0f), kf1 = rintf(xh1 * 128.0f);
+    const int K0 = static_cast<int>(kf0), K1 = static_cast<int>(kf1);
+    const f2 F = add2(fma2(pack2(kf0, kf1), pack2(-0.0078125f, -0.0078125f), pack2(xh0, xh1)), XL);
+    const f2 T = mul2(F, pack2(kLn2, kLn2));
+    const f2 H = fma2(T, pack2(0.16666667f, 0.16666667f), pack2(0.5f, 0.5f));
+    const f2 P = fma2(mul2(T, T), H, T);  // e^t - 1
+    const float2 t0 = tab[K0 & 127], t1 = tab[K1 & 127];
+    const f2 TH = pack2(t0.x, t1.x);
+    const f2 LO = fma2(TH, P, pack2(t0.y, t1.y));
+    const f2 SC = pack2(__int_as_float(((K0 >> 7) + 127) << 23), __int_as_float(((K1 >> 7) + 127) << 23));
+    EH = mul2(TH, SC);
+    EL = mul2(LO, SC);
+}
+
+// (H, L) += (XH, XL) for two pair sums advanced together, lane by lane.
+__device__ __forceinline__ void df2_add_pair(f2& H, f2& L, f2 XH, f2 XL) {
+    const f2 S = add2(H, XH);
+    const f2 BB = sub2(S, H);
+    const f2 E = add2(sub2(H, sub2(S, BB)), sub2(XH, BB));
+    H = S;
+    L = add2(L, add2(E, XL));
+}
+
 // ------------------------------------------------------------------ stop-row sweep
 // Constants of the stop-row sweep, packed for the f32x2 instructions.
 struct SweepConst {
@@ -1059,23 +1099,62 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                         sweep_lane<BF16, true>(A, ls, qs, sh.lpad, sh.qpad, rot, nvl, K);
                     else
                         sweep_lane<BF16, false>(A, ls, qs, sh.lpad, sh.qpad, rot, nvl, K);
-                    // large entries, each lane its own in entry order (the warp
-                    // runs as many rounds as its busiest lane has entries)
-                    for (uint32_t m = A.large; m; m &= m - 1) {
-                        const int bit = __ffs(m) - 1;
-                        const float l = BF16 ? bf16_lo(reinterpret_cast<const uint16_t*>(ls)[bit])
-                                             : reinterpret_cast<const float*>(ls)[bit];
-                        const df e = precise_e<BF16>(l, rc, sh.exp2tab);
-                        if (mode == MODE_RESIDUAL) {
-                            const float q = qs[bit];
-                            const df r = minus_sq(e, df_make(rc.s1), q);
-                            const bool pos = r.hi + r.lo > 0.0f;
-                            bw = df_sum(bw, pos ? r : df_make(0.0f));
-                            A.q += pos ? q : 0.0f;
-                            be = df_sum(be, e);
+                    // large entries, each lane its own, two at a time in packed
+                    // arithmetic (the warp runs as many rounds as its busiest
+                    // lane needs); two interleaved pair sums, joined at the end
+                    f2 BWH = pack2(0.0f, 0.0f), BWL = BWH, BEH = BWH, BEL = BWH;
+                    for (uint32_t m = A.large; m;) {
+                        const int bit0 = __ffs(m) - 1;
+                        m &= m - 1;
+                        const bool two = m != 0;
+                        const int bit1 = two ? __ffs(m) - 1 : bit0;
+                        m &= m - 1;
+                        f2 L;
+                        if (BF16) {
+                            const uint16_t* l16 = reinterpret_cast<const uint16_t*>(ls);
+                            L = pack2(bf16_lo(l16[bit0]), bf16_lo(l16[bit1]));
                         } else {
-                            bw = df_sum(bw, e);
+                            const float* l32 = reinterpret_cast<const float*>(ls);
+                            L = pack2(l32[bit0], l32[bit1]);
                         }
+                        f2 EH, EL;
+                        precise_e_x2(L, rc, sh.exp2tab, EH, EL);
+                        if (!two) {  // a lone last entry: the second lane weighs nothing
+                            float h0, h1, l0, l1;
+                            unpack2(EH, h0, h1);
+                            unpack2(EL, l0, l1);
+                            EH = pack2(h0, 0.0f);
+                            EL = pack2(l0, 0.0f);
+                        }
+                        if (mode == MODE_RESIDUAL) {
+                            // e - s1 q: the product exact through one fma, then a two-sum
+                            const float q0 = qs[bit0], q1 = two ? qs[bit1] : 0.0f;
+                            const f2 Q = pack2(q0, q1);
+                            const f2 NP = mul2(pack2(-rc.s1, -rc.s1), Q);
+                            const f2 PL = fma2(pack2(rc.s1, rc.s1), Q, NP);
+                            const f2 RH = add2(EH, NP);
+                            const f2 BB = sub2(RH, EH);
+                            const f2 RL = add2(add2(sub2(EH, sub2(RH, BB)), sub2(NP, BB)), sub2(EL, PL));
+                            float rh0, rh1, rl0, rl1;
+                            unpack2(RH, rh0, rh1);
+                            unpack2(RL, rl0, rl1);
+                            const bool pos0 = rh0 + rl0 > 0.0f, pos1 = rh1 + rl1 > 0.0f;
+                            df2_add_pair(BWH, BWL, pack2(pos0 ? rh0 : 0.0f, pos1 ? rh1 : 0.0f),
+                                         pack2(pos0 ? rl0 : 0.0f, pos1 ? rl1 : 0.0f));
+                            A.q += (pos0 ? q0 : 0.0f) + (pos1 ? q1 : 0.0f);
+                            df2_add_pair(BEH, BEL, EH, EL);
+                        } else {
+                            df2_add_pair(BWH, BWL, EH, EL);
+                        }
+                    }
+                    {
+                        float h0, h1, l0, l1;
+                        unpack2(BWH, h0, h1);
+                        unpack2(BWL, l0, l1);
+                        bw = df_sum(df{h0, l0}, df{h1, l1});
+                        unpack2(BEH, h0, h1);
+                        unpack2(BEL, l0, l1);
+                        be = df_sum(df{h0, l0}, df{h1, l1});
                     }
                     __syncwarp();
                     if (mode == MODE_RESIDUAL) {
