@@ -229,6 +229,14 @@ __device__ __forceinline__ float max_nan_f32(float a, float b) {
     return d;
 }
 
+// Maximum over the 32 lanes of a converged warp, in one instruction (NaN
+// inputs are ignored unless every input is NaN).
+__device__ __forceinline__ float warp_max_f32(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 

@@ -166,6 +166,14 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2,
     s = a + b2;
 }
 
+// One partial's sum at the common maximum M >= m, for a merge of several
+// partials at once (the sums are then added): a partial whose maximum is
+// -inf adds nothing, a NaN sum stays NaN.
+__device__ __forceinline__ float ms_term(float m, float s, float M, float c) {
+    if (m == -INFINITY) return (s != s) ? s : 0.0f;
+    return s * ex2((m - M) * c);
+}
+
 // Greedy partial merge: larger value wins, equal values keep the lower index.
 __device__ __forceinline__ void merge_arg(float& v, int& a, float v2, int a2) {
     if (v2 > v || (v2 == v && a2 < a)) {
@@ -515,6 +523,11 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         sh.lpad[tid] = BF16 ? 0xff80ff80u : 0xff800000u;
         sh.qpad[tid] = 0.0f;
     }
+    if (tid == 32 && !greedy && t_ok) {  // log2(e) / T as a pair, for the exact exponentials
+        const df c2 = log2e_over(T);
+        sh.c_hi = c2.hi;
+        sh.c_lo = c2.lo;
+    }
     // One pass-1 tile: tile tt of the CTA's slices, position by position.
     auto issue_p1 = [&](int tt, int it) {
         int i = 0;
@@ -805,11 +818,12 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 }
                 nan_seen = __any_sync(0xffffffffu, nan_seen);
             } else {
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-                    merge_ms(m, s, m2, s2, c);
-                }
+                // the warp's maximum, every lane's sum brought to it, then the total
+                const float Mw = warp_max_f32(m);
+                float sw = ms_term(m, s, Mw, c);
+                for (int off = 16; off > 0; off >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, off);
+                m = Mw;
+                s = sw;
             }
             if (lane == 0) wpart[warp * pk + i] = Partial{m, s, arg, nan_seen ? 1 : 0};
         }
@@ -824,14 +838,17 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     const bool timed_out = sh.timeout != 0;
     if (tid <= k && t_ok) {
         Partial p = wpart[tid];
-        for (int w = 1; w < kConsumerWarps; ++w) {
-            const Partial o = wpart[w * pk + tid];
-            if (greedy) {
+        if (greedy) {
+            for (int w = 1; w < kConsumerWarps; ++w) {
+                const Partial o = wpart[w * pk + tid];
                 merge_arg(p.m, p.arg, o.m, o.arg);
                 p.flags |= o.flags;
-            } else {
-                merge_ms(p.m, p.s, o.m, o.s, c);
             }
+        } else {
+            for (int w = 1; w < kConsumerWarps; ++w) p.m = fmaxf(p.m, wpart[w * pk + tid].m);
+            float S = 0.0f;
+            for (int w = 0; w < kConsumerWarps; ++w) S += ms_term(wpart[w * pk + tid].m, wpart[w * pk + tid].s, p.m, c);
+            p.s = S;
         }
         if (timed_out) p.flags |= 2;
         // push this CTA's partial of position tid into every CTA of the cluster
@@ -853,8 +870,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 if (greedy)
                     merge_arg(M, A, pr.m, pr.arg);
                 else
-                    merge_ms(M, S, pr.m, pr.s, c);
+                    M = fmaxf(M, pr.m);
             }
+            if (!greedy)
+                for (uint32_t r = 0; r < C; ++r) S += ms_term(allpart[r * pk + lane].m, allpart[r * pk + lane].s, M, c);
             if (greedy && A == 0x7fffffff) A = 0;  // every value is -inf: index 0
         }
         __syncwarp();
@@ -886,13 +905,12 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                         if (!err) {
                             // p_i(x_i) with the double-float exponential (a masked
                             // entry, logit -inf, has p = 0)
-                            const df c2 = log2e_over(T);
                             RowConst rc;
                             rc.M = M;
                             rc.s1 = S;
                             rc.thr = 0.0f;
-                            rc.ch = c2.hi;
-                            rc.cl = c2.lo;
+                            rc.ch = sh.c_hi;
+                            rc.cl = sh.c_lo;
                             p = df_val(exact_weight<BF16>(Lx, 0.0f, MODE_BONUS, rc, df_make(0.0f), sh.exp2tab)) / S;
                             const float rho = fminf(1.0f, p / fmaxf(qx, 1e-12f));
                             stop = !(u0 < rho);
@@ -923,6 +941,24 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 sh.Mj = Mj;
                 sh.sj = Sj;
                 sh.mode = (j < k) ? (a.q ? MODE_RESIDUAL : MODE_ONEHOT) : MODE_BONUS;
+                if (t_ok && !greedy && !(st & ST_ERRMASK)) {
+                    // the stop row's pass-2 geometry, set here so that one block
+                    // barrier publishes it with the decision
+                    const bool resid = j < k && a.q;
+                    const long long lrow_j = (static_cast<long long>(b) * (k + 1) + j) * V;
+                    const float* qrow_j = a.q ? a.q + (static_cast<long long>(b) * k + (j < k ? j : 0)) * V : nullptr;
+                    sh.thr = kLargeP * Sj;
+                    // bulk copies need 16-byte aligned starts and sizes: both rows
+                    // aligned at the slice start, and whole groups of 8 entries
+                    const bool la = (reinterpret_cast<uintptr_t>(lg + (lrow_j + v0) * esz) & 15) == 0;
+                    const bool qa = qrow_j && (reinterpret_cast<uintptr_t>(qrow_j + v0) & 15) == 0;
+                    sh.p2fast = la && (!resid || (qa && !a.q_host)) && (n % kChunk) == 0;
+                    sh.ntiles2 = (n + kP2Elems - 1) / kP2Elems;
+                    // pass-2 slots: [q (residual rows)][logits], one tile each
+                    sh.loff2 = resid ? kP2Elems * 4 : 0;
+                    sh.stride2 = sh.loff2 + kP2Elems * esz;
+                    sh.nslots2 = min(kStages2, kRingBytes / sh.stride2);  // at least 5: the consumers step 4 tiles at a time
+                }
             }
             if (lane <= k) sh.xs[lane] = xi;
             // rank 0 writes debug values and, for greedy or failed rows, the outputs
@@ -963,23 +999,6 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     const int j = sh.j;
     const long long lrow = (static_cast<long long>(b) * (k + 1) + j) * V;
     const float* qrow = a.q ? a.q + (static_cast<long long>(b) * k + (j < k ? j : 0)) * V : nullptr;
-    if (tid == 0) {
-        const df c2 = log2e_over(T);
-        sh.c_hi = c2.hi;
-        sh.c_lo = c2.lo;
-        sh.thr = kLargeP * sh.sj;
-        // bulk copies need 16-byte aligned starts and sizes: both rows
-        // aligned at the slice start, and whole groups of 8 entries
-        const bool la = (reinterpret_cast<uintptr_t>(lg + (lrow + v0) * esz) & 15) == 0;
-        const bool qa = qrow && (reinterpret_cast<uintptr_t>(qrow + v0) & 15) == 0;
-        sh.p2fast = la && (sh.mode != MODE_RESIDUAL || (qa && !a.q_host)) && (n % kChunk) == 0;
-        sh.ntiles2 = (n + kP2Elems - 1) / kP2Elems;
-        // pass-2 slots: [q (residual rows)][logits], one tile each
-        sh.loff2 = (sh.mode == MODE_RESIDUAL) ? kP2Elems * 4 : 0;
-        sh.stride2 = sh.loff2 + kP2Elems * esz;
-        sh.nslots2 = min(kStages2, kRingBytes / sh.stride2);  // at least 5: the consumers step 4 tiles at a time
-    }
-    __syncthreads();
     RowConst rc;
     rc.M = sh.Mj;
     rc.s1 = sh.sj;
@@ -1180,16 +1199,37 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 sh.lane_lo[t2][lane] = lw.lo;
                 sh.lane_q[t2][lane] = A.q;
                 te = df_sum(te, df_sum(df{eh, elo}, be));
-                const df tw = df_warp_total(lw);
-                float tq = A.q;
-                for (int off = 16; off > 0; off >>= 1) tq += __shfl_down_sync(0xffffffffu, tq, off);
-                if (lane == 0) {
-                    sh.tile_hi[t2] = tw.hi;
-                    sh.tile_lo[t2] = tw.lo;
-                    sh.tile_q[t2] = tq;
-                }
-                __syncwarp();
             }
+            // totals of this warp's tiles, four tiles at a time: lane 8 i + g
+            // adds lane sums 4 g .. 4 g + 3 of the group's tile i (in a
+            // lane-rotated order: conflict-free banks), then the tile's eight
+            // lanes combine over three shuffles
+            __syncwarp();
+            for (int tb = warp; tb < ntiles2; tb += 4 * kConsumerWarps) {
+                const int tt = tb + (lane >> 3) * kConsumerWarps;
+                const int g = lane & 7;
+                df v = df_make(0.0f);
+                float vq = 0.0f;
+                if (tt < ntiles2) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int e = 4 * g + ((i + (lane >> 3)) & 3);
+                        v = df_sum(v, df{sh.lane_hi[tt][e], sh.lane_lo[tt][e]});
+                        vq += sh.lane_q[tt][e];
+                    }
+                }
+#pragma unroll
+                for (int off = 1; off < 8; off <<= 1) {
+                    v = df_sum(v, df{__shfl_xor_sync(0xffffffffu, v.hi, off), __shfl_xor_sync(0xffffffffu, v.lo, off)});
+                    vq += __shfl_xor_sync(0xffffffffu, vq, off);
+                }
+                if (g == 0 && tt < ntiles2) {
+                    sh.tile_hi[tt] = v.hi;
+                    sh.tile_lo[tt] = v.lo;
+                    sh.tile_q[tt] = vq;
+                }
+            }
+            __syncwarp();
         }
         // CTA totals: weights, e (residual mode), q over positive residuals
         const df tw = df_warp_total(te);
