@@ -1026,6 +1026,32 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     K.NS1 = pack2(-rc.s1, -rc.s1);
     K.thr = rc.thr;
 
+    // Bf16 rows: the exact e of every bf16 value that can be a large entry,
+    // tabulated once in the ring's unused tail, so that large entries look
+    // it up instead of evaluating exp2dd.  Positive logits only (their bf16
+    // bit patterns order like the values); lmin sits below every logit whose
+    // estimate can exceed thr (a margin of 1/16 in the exponent).
+    int tab_base = 0, tab_n = 0;
+    const float2* etab = reinterpret_cast<const float2*>(ring + S2 * stride2);
+    if (BF16 && !producer) {
+        const int cap = (kRingBytes - S2 * stride2) / static_cast<int>(sizeof(float2));
+        const float lmin = rc.M + (__log2f(rc.thr) - 0.0625f) / rc.ch;
+        if (rc.M > 0.0f && lmin > 0.0f) {
+            const int hb = static_cast<int>(__float_as_uint(rc.M) >> 16);
+            const int lb = static_cast<int>(__float_as_uint(lmin) >> 16);
+            if (hb >= lb && hb - lb + 1 <= cap) {
+                tab_base = lb;
+                tab_n = hb - lb + 1;
+            }
+        }
+        float2* wtab = reinterpret_cast<float2*>(ring + S2 * stride2);
+        for (int i = tid; i < tab_n; i += kConsumers) {
+            const df e = precise_e<BF16>(__uint_as_float(static_cast<uint32_t>(tab_base + i) << 16), rc, sh.exp2tab);
+            wtab[i] = make_float2(e.hi, e.lo);
+        }
+        consumers_sync();
+    }
+
     for (;;) {
         df te = df_make(0.0f);  // this thread's sum of e (residual mode)
         bool qbad = false;
@@ -1128,16 +1154,25 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                         const bool two = m != 0;
                         const int bit1 = two ? __ffs(m) - 1 : bit0;
                         m &= m - 1;
-                        f2 L;
+                        f2 EH, EL;
+                        bool tabbed = false;
                         if (BF16) {
                             const uint16_t* l16 = reinterpret_cast<const uint16_t*>(ls);
-                            L = pack2(bf16_lo(l16[bit0]), bf16_lo(l16[bit1]));
+                            const uint32_t w0 = l16[bit0], w1 = l16[bit1];
+                            const uint32_t i0 = w0 - static_cast<uint32_t>(tab_base);
+                            const uint32_t i1 = w1 - static_cast<uint32_t>(tab_base);
+                            tabbed = i0 < static_cast<uint32_t>(tab_n) && i1 < static_cast<uint32_t>(tab_n);
+                            if (tabbed) {
+                                const float2 t0 = etab[i0], t1 = etab[i1];
+                                EH = pack2(t0.x, t1.x);
+                                EL = pack2(t0.y, t1.y);
+                            } else {
+                                precise_e_x2(pack2(bf16_lo(w0), bf16_lo(w1)), rc, sh.exp2tab, EH, EL);
+                            }
                         } else {
                             const float* l32 = reinterpret_cast<const float*>(ls);
-                            L = pack2(l32[bit0], l32[bit1]);
+                            precise_e_x2(pack2(l32[bit0], l32[bit1]), rc, sh.exp2tab, EH, EL);
                         }
-                        f2 EH, EL;
-                        precise_e_x2(L, rc, sh.exp2tab, EH, EL);
                         if (!two) {  // a lone last entry: the second lane weighs nothing
                             float h0, h1, l0, l1;
                             unpack2(EH, h0, h1);
