@@ -79,6 +79,24 @@ def test_odd_sizes(h, V, k, B, dtype):
     _acc(compare(w, got, check_debug=True))
 
 
+@pytest.mark.parametrize("offset,T", [(-40.0, 1.0), (0.0, 4.0), (40.0, 4.0), (40.0, 0.25), (200.0, 1.0)])
+def test_bf16_logit_offsets(h, offset, T):
+    """Softmax does not see a common offset, but the bf16 grid does: shifted
+    logits put the stop row's large entries in a positive range (their exact
+    e read from a per-row table), in a range reaching zero or below it (e
+    evaluated directly), or on a coarse grid with many equal logits (+200:
+    spacing 1)."""
+    base = W.make_random(name="offset", B=6, k=4, V=50000, dtype="bf16", seed=int(offset) + 1000,
+                         logit_sigma=3.0, draft_sigma=1.0, temperature=T, spike=6.0, spike_mode="position")
+    lf = W.bf16_bits_to_f32(base.logits) + np.float32(offset)
+    rng = np.random.default_rng(int(1000 + offset * 10 + T * 100))
+    for _ in range(10):
+        w = W.Workload("offset", "bf16", W.f32_to_bf16_bits(lf), base.q, base.x,
+                       rng.random(base.u.shape, dtype=np.float32), base.T)
+        got = run_gpu(h, w, debug=True)
+        _acc(compare(w, got, check_debug=True))
+
+
 @pytest.mark.parametrize("C", [None, 11, 16])
 def test_cluster_sizes_agree(h, C, monkeypatch):
     """Every split of the vocabulary over a cluster gives the same result."""
