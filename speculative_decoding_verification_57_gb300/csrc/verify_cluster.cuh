@@ -540,7 +540,8 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>(bytes));
         bulk_g2s(smem_u32(ring + slot * kTileBytes), lg + e0 * esz + off, static_cast<uint32_t>(bytes), bar);
     };
-    int it_prod = 0, it_cons = 0;
+    int it_prod = 0;
+    int c_slot = 0, c_phase = 0;  // the consumers' stage and its phase
     if (producer && lane == 0) {
         // the producer sets up the ring and the slice geometry, and starts the
         // first copies before the block's first barrier
@@ -583,13 +584,12 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         const int slot = it % kStages;
         return mbar_wait_bounded(smem_u32(&sh.empty[slot]), ((it / kStages) & 1) ^ 1, kWaitPolls);
     };
-    auto cons_wait = [&](int it) -> bool {
-        const int slot = it % kStages;
-        return mbar_wait_bounded(smem_u32(&sh.full[slot]), (it / kStages) & 1, kWaitPolls);
-    };
-    auto cons_release = [&](int it) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.empty[it % kStages]));
+    // the consumers' next stage: c_slot = it % kStages, c_phase = (it / kStages) & 1
+    auto next_stage = [&]() {
+        if (++c_slot == kStages) {
+            c_slot = 0;
+            c_phase ^= 1;
+        }
     };
 
     // ---------------------------------------------------------------- pass 1
@@ -631,36 +631,42 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 for (int e = 0; e < h; ++e) scalar_elem(e);
             __syncwarp();  // reconverge before the tile loop's warp-wide steps
 
-            for (int lt = 0; lt < ntiles; ++lt, ++t, ++it_cons) {
+            for (int lt = 0; lt < ntiles; ++lt, ++t, next_stage()) {
                 if (t == 2 && warp == 0 && lane < k && !greedy && xi >= 0 && xi < V) {
                     // the accept test's scalars; x_i has long arrived
                     const long long row = static_cast<long long>(b) * (k + 1) + lane;
                     Lx = load_logit(a.logits, row * V + xi, BF16);
                     qx = a.q ? __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi) : 1.0f;
                 }
-                const bool ok = !sh.timeout && cons_wait(it_cons);
+                const bool ok = !sh.timeout && mbar_wait_bounded(smem_u32(&sh.full[c_slot]), c_phase, kWaitPolls);
                 const int bytes = min(kTileBytes, sh.nbytes[i] - lt * kTileBytes);
                 const int nch = bytes >> 4;
-                const uint32_t tile = smem_u32(ring + (it_cons % kStages) * kTileBytes);
+                const uint32_t tile = smem_u32(ring + c_slot * kTileBytes);
                 if (!ok) {
                     atomicOr(&sh.timeout, 1);
                     continue;
                 }
                 constexpr int kPer = kTileBytes / 16 / kConsumers;  // 16-byte chunks per thread
                 uint4 w[kPer];
+                if (nch == kTileBytes / 16) {  // a full tile (all but a position's last)
 #pragma unroll
-                for (int r = 0; r < kPer; ++r) {
-                    const int ch = tid + r * kConsumers;
-                    if (ch < nch) {
-                        w[r] = ld_shared_v4(tile + ch * 16);
-                    } else if (BF16) {
-                        w[r] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-                    } else {
-                        const uint32_t ni = __float_as_uint(-INFINITY);
-                        w[r] = make_uint4(ni, ni, ni, ni);
+                    for (int r = 0; r < kPer; ++r) w[r] = ld_shared_v4(tile + (tid + r * kConsumers) * 16);
+                } else {
+#pragma unroll
+                    for (int r = 0; r < kPer; ++r) {
+                        const int ch = tid + r * kConsumers;
+                        if (ch < nch) {
+                            w[r] = ld_shared_v4(tile + ch * 16);
+                        } else if (BF16) {
+                            w[r] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+                        } else {
+                            const uint32_t ni = __float_as_uint(-INFINITY);
+                            w[r] = make_uint4(ni, ni, ni, ni);
+                        }
                     }
                 }
-                cons_release(it_cons);  // the data is in registers
+                __syncwarp();  // the data is in registers: release the stage
+                if (lane == 0) mbar_arrive(smem_u32(&sh.empty[c_slot]));
                 float lmax;
                 if (BF16) {
                     if (greedy) {
