@@ -16,6 +16,7 @@ on the data path) and the slowest rank's time counts.
 """
 import argparse
 import hashlib
+import re
 import glob
 import json
 import os
@@ -122,11 +123,19 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text):
+    """A source file without its comments and blank lines: edits to comments
+    leave a kernel, and so its profile, unchanged."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_hash(files):
     h = hashlib.sha256()
     for name in files:
-        with open(os.path.join(ROOT, "speculative_decoding_verification_57_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "speculative_decoding_verification_57_gb300", "csrc", name)) as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

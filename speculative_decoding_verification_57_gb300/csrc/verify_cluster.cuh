@@ -13,10 +13,14 @@
 // over distributed shared memory after a cluster barrier; every CTA then
 // evaluates the accept tests and the first rejection with one warp ballot,
 // identically.  Pass 2 streams only the stop position j (target logits and,
-// after a rejection, the draft row q_j): it weighs every entry by
-// max(0, p_j - q_j) (or p_k for the bonus), keeps sums per 256-entry block,
-// and after a second exchange of CTA totals the CTA whose slice holds u * W
-// rescans one block with one warp to find the token.
+// after a rejection, the draft row q_j), one 1024-entry tile per warp: it
+// weighs every entry by max(0, p_j - q_j) (or p_k for the bonus) in
+// double-float sums, evaluating the exponential exactly (a table-driven
+// 2^x, or a per-row table of bf16 values) for the entries whose probability
+// can move the draw, and keeps sums per tile and per 32-entry lane segment.
+// After a second exchange of CTA totals the CTA whose slice holds u * W finds
+// the tile, then the segment, and one warp recomputes the segment's 32
+// weights exactly to pick the token.
 //
 // Sources (page title, section): "LLM Inference & Speculative Decoding: From
 // Roofline Physics to Lossless Acceleration", s.2 (acceptance rule, residual,

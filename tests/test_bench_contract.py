@@ -33,3 +33,13 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert "workload" in d["config"]
+
+
+def test_profile_hash_ignores_comments():
+    """A committed profile stays valid across comment edits, not code edits."""
+    import bench
+
+    code = "int a = 1;  // note\n/* block\n comment */\nint b = 2;\n\n"
+    assert bench._code_only(code) == "int a = 1;\nint b = 2;"
+    assert bench._code_only(code.replace("note", "other note")) == bench._code_only(code)
+    assert bench._code_only(code.replace("b = 2", "b = 3")) != bench._code_only(code)
