@@ -37,6 +37,7 @@ def test_reference_arm_prints_one_contract_line():
 
 def test_profile_hash_ignores_comments():
     """A committed profile stays valid across comment edits, not code edits."""
+    sys.path.insert(0, ROOT)
     import bench
 
     code = "int a = 1;  // note\n/* block\n comment */\nint b = 2;\n\n"
