@@ -55,7 +55,7 @@ constexpr int kChunk = 8;          // pass-2 entries per chunk
 constexpr int kLaneEntries = 32;   // pass-2 entries per lane and tile (four chunks)
 constexpr int kP2Elems = kLaneEntries * 32;  // pass-2 tile: 1024 entries, one warp
 constexpr int kMaxP2Tiles = kMaxSlice / kP2Elems;
-constexpr float kLargeP = 1e-5f;   // pass-2 entries with p above this use exp2dd
+constexpr float kLargeP = 1e-5f;   // pass-2 entries with p above this take the exact e (exp2dd or the bf16 table)
 constexpr uint32_t kWaitPolls = 1u << 22;
 constexpr float kLog2e = 1.44269504088896341f;
 
