@@ -244,6 +244,32 @@ def test_host_buffer_entry(h, q_pinned):
     _acc(compare(w, {kk: v.numpy() for kk, v in out.items()}))
 
 
+@pytest.mark.parametrize("case", ["benchmark pinned q", "13 rows pageable q", "10 rows fp32 pinned q"])
+def test_host_buffer_entry_large(h, case):
+    """The host-buffer entry at full sizes: the benchmark workload with q read
+    in place, a bf16 batch whose q is copied, and an fp32 batch at V = 151936."""
+    import torch
+
+    import speculative_decoding_verification_57_gb300 as sv
+
+    if case == "benchmark pinned q":
+        w, pinned = W.make_workload("benchmark"), True
+    elif case == "13 rows pageable q":
+        w = W.make_random(name="host", B=13, k=5, V=128256, dtype="bf16", seed=13, logit_sigma=3.0,
+                          draft_sigma=1.0, temperature=1.0, spike=8.0, spike_mode="position", greedy_rows=2)
+        pinned = False
+    else:
+        w = W.make_random(name="host", B=10, k=15, V=151936, dtype="f32", seed=10, logit_sigma=4.0,
+                          draft_sigma=2.0, temperature=1.0)
+        pinned = True
+    L = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16) if w.dtype == "bf16" else torch.from_numpy(w.logits)
+    q = torch.from_numpy(w.q)
+    out = sv.specv_verify_sample_host(h, L.pin_memory(), q.pin_memory() if pinned else q.clone(),
+                                      torch.from_numpy(w.x).pin_memory(), torch.from_numpy(w.u).pin_memory(),
+                                      torch.from_numpy(w.T).pin_memory())
+    _acc(compare(w, {kk: v.numpy() for kk, v in out.items()}))
+
+
 def test_empty_batch(h):
     import torch
 
