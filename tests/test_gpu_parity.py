@@ -67,6 +67,7 @@ ODD = [
     (1, 1, 3, "f32"), (7, 2, 3, "bf16"), (8, 4, 2, "f32"), (13, 16, 3, "bf16"), (1001, 5, 3, "f32"),
     (2047, 3, 2, "bf16"), (2048, 31, 2, "f32"), (2049, 2, 3, "bf16"), (4099, 1, 3, "f32"),
     (32003, 16, 3, "bf16"), (65537, 2, 2, "f32"), (128257, 3, 2, "bf16"), (262144, 2, 2, "bf16"),
+    (50000, 31, 3, "bf16"), (20000, 31, 2, "f32"),
 ]
 
 
