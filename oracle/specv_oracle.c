@@ -26,8 +26,8 @@
  *  [D] "Speculative Decoding: Draft, Verify, Accept" -- demo script part B
  *      (residual with a zero-mass fallback to p, inverse-CDF sampling).
  *
- * Readings where the pages leave a step open (each one is listed, with its
- * reason, in the design notes of the repository):
+ * Readings where the pages leave a step open (the plainest reading that the
+ * rest of the pages support, with the reason beside each):
  *  - accept iff u < min(1, p(x)/max(q(x), 1e-12))  (strict '<' and the clamp
  *    follow the code of [A] s.2 and [D]);
  *  - inverse CDF: the token is the smallest v, in vocabulary order, with
