@@ -1,5 +1,6 @@
-"""bench.py's command line and the reference arm's JSON line (CPU: the
-reference arm times the oracle on the host)."""
+"""bench.py on the CPU: its command line, the reference arm's JSON line
+(the reference arm times the oracle on the host), the profile keys and the
+clock sampler's reading of nvidia-smi."""
 import json
 import os
 import subprocess
@@ -44,3 +45,42 @@ def test_profile_hash_ignores_comments():
     assert bench._code_only(code) == "int a = 1;\nint b = 2;"
     assert bench._code_only(code.replace("note", "other note")) == bench._code_only(code)
     assert bench._code_only(code.replace("b = 2", "b = 3")) != bench._code_only(code)
+
+
+def test_clock_sampler_keeps_the_timed_window_and_reasons(monkeypatch):
+    """nvidia-smi rows outside the timed window are left out, the median SM
+    clock and the active throttle reasons come from the rows inside it."""
+    import time
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    rows = [
+        "2026/12/02 15:00:00.000, 0, 1500, 2070, 500.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 15:00:01.000, 0, 2070, 2070, 900.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "2026/12/02 15:00:01.100, 0, 2055, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 15:00:01.200, 0, 2070, 2070, 960.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "2026/12/02 15:00:03.000, 0, 1000, 2070, 300.0, 0x8, Active, Not Active, Not Active, Not Active",
+        "not a sample",
+    ]
+
+    class FakeSmi:
+        def terminate(self):
+            pass
+
+        def kill(self):
+            pass
+
+        def communicate(self, timeout=None):
+            return "\n".join(rows), ""
+
+    monkeypatch.setattr(bench.subprocess, "Popen", lambda *a, **k: FakeSmi())
+    monkeypatch.setattr(bench.time, "sleep", lambda s: None)
+    cs = bench.ClockSampler(0)
+    cs.start()
+    cs.t0 = time.mktime(time.strptime("2026/12/02 15:00:01", "%Y/%m/%d %H:%M:%S"))
+    cs.t1 = cs.t0 + 0.2
+    d = cs.stop()
+    assert d["in_window"] and d["samples"] == 3
+    assert d["sm_mhz"] == 2070.0 and d["sm_max_mhz"] == 2070.0
+    assert d["reasons"] == ["sw_power_cap"]  # the hw_slowdown row lies outside the window
