@@ -464,7 +464,7 @@ int specv_oracle_verify(int dtype, const void *logits, const float *q, const int
 
 /* ---------------------------------------------------------------- rollback
  * Paged KV-cache bookkeeping after verification, row by row in batch order
- * ([A] s.6 "PagedKVCacheManager", rollback_to): a row whose cache holds
+ * ([A] s.1 "PagedKVCacheManager", rollback_to): a row whose cache holds
  * seq_len positions, the last k of them the drafts, keeps
  *   target_len = seq_len - (k - num_accepted)
  * positions; its block table keeps ceil(target_len / block_size) blocks

@@ -2,7 +2,7 @@
 // device: for every row, drop the cache positions of the rejected drafts,
 // pop the blocks the shorter sequence no longer needs and append them to the
 // free list ("LLM Inference & Speculative Decoding: From Roofline Physics to
-// Lossless Acceleration", s.6, PagedKVCacheManager.rollback_to).
+// Lossless Acceleration", s.1, PagedKVCacheManager.rollback_to).
 //
 // The result equals rolling the rows back one at a time in batch order: row
 // b's popped blocks land in the free list after those of rows 0..b-1, each

@@ -1,6 +1,6 @@
 """GPU parity of the paged KV-cache rollback with the oracle (integer work:
 bit-exact).  "LLM Inference & Speculative Decoding: From Roofline Physics to
-Lossless Acceleration", s.6, PagedKVCacheManager.rollback_to."""
+Lossless Acceleration", s.1, PagedKVCacheManager.rollback_to."""
 import numpy as np
 import pytest
 

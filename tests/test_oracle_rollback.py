@@ -1,5 +1,5 @@
 """Pins of the oracle's paged KV-cache rollback ("LLM Inference & Speculative
-Decoding: From Roofline Physics to Lossless Acceleration", s.6,
+Decoding: From Roofline Physics to Lossless Acceleration", s.1,
 PagedKVCacheManager.rollback_to)."""
 import numpy as np
 
