@@ -209,7 +209,7 @@ specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, 
                                       int32_t *row_status, void *stream);
 
 /* Paged KV-cache bookkeeping after a verification ("LLM Inference &
- * Speculative Decoding: From Roofline Physics to Lossless Acceleration", s.6,
+ * Speculative Decoding: From Roofline Physics to Lossless Acceleration", s.1,
  * PagedKVCacheManager.rollback_to), all pointers device memory:
  *   num_accepted [B]               int32, as returned by a verify call
  *   seq_lens     [B]               int32 in/out: positions held in the cache,
@@ -230,7 +230,8 @@ specv_status specv_verify_sample_host(specv_handle h, specv_dtype logits_dtype, 
  *                                  (then nothing changes)
  * The result equals rolling the rows back one at a time in batch order,
  * each row's blocks popped last-first.  Asynchronous on `stream`; argument
- * errors are returned before launch. */
+ * errors are returned before launch (SPECV_ERR_INVALID_ARGUMENT, among them
+ * free_capacity outside [0, INT32_MAX]: free_count is an int32). */
 specv_status specv_rollback(specv_handle h, const int32_t *num_accepted, int batch, int k, int32_t *seq_lens,
                             int32_t *block_tables, int max_blocks, int32_t *num_blocks, int block_size,
                             int32_t *free_list, int64_t free_capacity, int32_t *free_count, int32_t *row_status,
@@ -239,6 +240,17 @@ specv_status specv_rollback(specv_handle h, const int32_t *num_accepted, int bat
 /* Number of CTAs per sequence (thread-block cluster size, 1..16) that the
  * next call with these sizes would use; 0 if the sizes are invalid. */
 int specv_plan_cluster(specv_handle h, specv_dtype logits_dtype, int batch, int k, int64_t V);
+
+/* Test hook, off unless called: arms the next launch of the split-vocabulary
+ * kernel (V > 2048) on this handle so that CTA 0 of the grid never issues
+ * the bulk copy of its pass-1 stage use number `stage_use` (counted from 0
+ * in issue order) nor signals it, and every wait of that launch gives up
+ * after `polls` polls.  The waits that run out end the row's work: it
+ * reports row_status bit 64 (num_accepted 0, out_tokens -1) and the call
+ * still returns SPECV_OK; the other rows and the next call run normally.  No
+ * copy is in flight when a CTA exits (it waits, bounded, for every copy it
+ * issued).  SPECV_ERR_INVALID_ARGUMENT for stage_use < 0 or polls < 1. */
+specv_status specv_test_withhold_stage(specv_handle h, int stage_use, int polls);
 
 /* Kernel launches issued by this handle since it was created. */
 int64_t specv_launch_count(specv_handle h);

@@ -23,6 +23,7 @@ __all__ = [
     "specv_verify_greedy",
     "specv_verify_sample_host",
     "specv_plan_cluster",
+    "specv_test_withhold_stage",
     "specv_launch_count",
     "ST_ERROR_MASK",
     "ST_NONFINITE",
@@ -299,6 +300,13 @@ def specv_rollback(h: Handle, num_accepted, k, seq_lens, block_tables, num_block
 
 def specv_plan_cluster(h: Handle, logits_dtype, B, k, V) -> int:
     return int(_lib.load().specv_plan_cluster(h.ptr, logits_dtype, B, k, V))
+
+
+def specv_test_withhold_stage(h: Handle, stage_use: int, polls: int) -> None:
+    """Test hook: the next split-vocabulary launch on ``h`` never fills
+    pass-1 stage use ``stage_use`` of CTA 0 and its waits give up after
+    ``polls`` polls (see include/specv.h)."""
+    _check(_lib.load().specv_test_withhold_stage(h.ptr, int(stage_use), int(polls)), "specv_test_withhold_stage")
 
 
 def specv_launch_count(h: Handle) -> int:

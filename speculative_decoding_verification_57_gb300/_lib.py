@@ -71,6 +71,8 @@ def load(build_if_missing=True):
     lib.specv_rollback.argtypes = [vp, vp, i32, i32, vp, vp, i32, vp, i32, vp, i64, vp, vp, vp]
     lib.specv_plan_cluster.restype = i32
     lib.specv_plan_cluster.argtypes = [vp, i32, i32, i32, i64]
+    lib.specv_test_withhold_stage.restype = i32
+    lib.specv_test_withhold_stage.argtypes = [vp, i32, i32]
     lib.specv_launch_count.restype = i64
     lib.specv_launch_count.argtypes = [vp]
     lib.specv_destroy.restype = None

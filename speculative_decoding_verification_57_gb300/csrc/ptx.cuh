@@ -51,6 +51,43 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
     return ok != 0;
 }
 
+// Non-blocking tests of a phase (mbarrier.test_wait never suspends the
+// thread, unlike try_wait): for a loop that polls several things in turn.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
+// The same with acquire at cluster scope: once it returns true, what other
+// CTAs of the cluster stored before their (release) arrivals on `bar` is
+// visible to the calling thread.
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t phase) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase)
+        : "memory");
+    return ok != 0;
+}
+
+// Arrival on an mbarrier of any CTA of the cluster (`bar` is a
+// shared::cluster address, e.g. from map_rank), with release at cluster
+// scope: the caller's earlier stores into that CTA are visible to whoever
+// observes the phase complete with an acquire at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Nanoseconds of the global timer.
 __device__ __forceinline__ unsigned long long gtimer() {
     unsigned long long t;

@@ -33,6 +33,10 @@ struct specv_ctx {
     // device staging for specv_verify_sample_host
     void* stage = nullptr;
     size_t stage_bytes = 0;
+    // one-shot test hook: the next cluster-kernel launch withholds one
+    // pass-1 stage of CTA 0 and waits at most `test_polls` polls
+    int test_withhold = -1;
+    uint32_t test_polls = 0;
 };
 
 static thread_local char g_last_error[256] = "";
@@ -173,6 +177,11 @@ specv_status run(specv_ctx* h, specv_dtype dt, const VerifyArgs& a, void* stream
     VerifyArgs args = a;
     args.slice = p.slice;
     args.pk = h->max_k + 1;
+    if (!p.warp && h->test_withhold >= 0) {  // the test hook arms one launch
+        args.withhold = h->test_withhold;
+        args.polls = h->test_polls;
+        h->test_withhold = -1;
+    }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (p.warp)
@@ -456,6 +465,13 @@ void specv_destroy(specv_handle h) {
     delete h;
 }
 
+specv_status specv_test_withhold_stage(specv_handle h, int stage_use, int polls) {
+    if (!h || stage_use < 0 || polls < 1) return SPECV_ERR_INVALID_ARGUMENT;
+    h->test_withhold = stage_use;
+    h->test_polls = static_cast<uint32_t>(polls);
+    return SPECV_OK;
+}
+
 const char* specv_status_string(specv_status s) {
     switch (s) {
         case SPECV_OK: return "ok";
@@ -473,7 +489,9 @@ specv_status specv_rollback(specv_handle h, const int32_t* num_accepted, int bat
                             int32_t* block_tables, int max_blocks, int32_t* num_blocks, int block_size,
                             int32_t* free_list, int64_t free_capacity, int32_t* free_count, int32_t* row_status,
                             void* stream) {
-    if (!h || batch < 0 || k < 0 || k > h->max_k || max_blocks < 0 || block_size < 1 || free_capacity < 0)
+    // free_count is an int32: a list longer than INT32_MAX entries could not be counted
+    if (!h || batch < 0 || k < 0 || k > h->max_k || max_blocks < 0 || block_size < 1 || free_capacity < 0 ||
+        free_capacity > INT32_MAX)
         return SPECV_ERR_INVALID_ARGUMENT;
     if (!free_count || (free_capacity > 0 && !free_list)) return SPECV_ERR_INVALID_ARGUMENT;
     if (batch > 0 && (!num_accepted || !seq_lens || !num_blocks || (max_blocks > 0 && !block_tables)))

@@ -57,6 +57,7 @@ constexpr int kP2Elems = kLaneEntries * 32;  // pass-2 tile: 1024 entries, one w
 constexpr int kMaxP2Tiles = kMaxSlice / kP2Elems;
 constexpr float kLargeP = 1e-5f;   // pass-2 entries with p above this take the exact e (exp2dd or the bf16 table)
 constexpr uint32_t kWaitPolls = 1u << 22;
+constexpr int kLook = 1;           // pass 1 reads at most this many positions past the first undecided one
 constexpr float kLog2e = 1.44269504088896341f;
 
 enum : int {
@@ -100,6 +101,8 @@ struct VerifyArgs {
     int slice;               // elements per CTA, a multiple of 64
     int pk;                  // positions per partial array in shared memory (>= k + 1)
     int q_host;              // q is page-locked host memory read in place: plain loads only, no bulk copies
+    int withhold = -1;       // test only: pass-1 stage use of CTA 0 that is never filled (-1: none)
+    uint32_t polls = kWaitPolls;  // poll limit of every wait
 };
 
 struct Partial {
@@ -110,7 +113,7 @@ struct Partial {
 };
 
 // Dynamic shared memory: the ring (kRingBytes), then the per-warp partials
-// [kConsumerWarps][pk], then every cluster CTA's partials [C][pk] (pushed by
+// [pk][kConsumerWarps], then every cluster CTA's partials [pk][C] (pushed by
 // each CTA of the cluster).
 inline size_t cluster_dyn_smem(int C, int pk) {
     return static_cast<size_t>(kRingBytes) + static_cast<size_t>(kConsumerWarps + C) * pk * sizeof(Partial);
@@ -137,6 +140,17 @@ struct alignas(16) ClusterSmem {
     alignas(16) uint32_t lpad[4];  // one masked piece of logits (-inf)
     alignas(16) float qpad[4];     // and of q (zero)
     int xs[kMaxK + 1];          // draft tokens, for whoever writes the outputs
+    unsigned long long pbar[kMaxK + 1];  // position i: one arrival per cluster CTA once its partial is pushed here
+    int pcnt[kMaxK + 1];        // position i: consumer warps of this CTA that have reported it
+    float posM[kMaxK + 1];      // merged per position: maximum, sum of exponentials (sampled),
+    float posS[kMaxK + 1];
+    int posA[kMaxK + 1];        // argmax (greedy), partial flags,
+    int posF[kMaxK + 1];
+    int posE[kMaxK + 1];        // error bits of its test,
+    float posP[kMaxK + 1];      // p(x_i)
+    int2 views[16];             // every cluster CTA's outcome (stop position, status), pushed by it
+    int p1_end;                 // pass-1 stage uses issued in all, once the producer stops issuing
+    int stop_pos;               // the first stopping position, once decided (-1 before)
     int j, status, mode, owner, p2fast, ntiles2, timeout, stride2, nslots2, loff2;
     float Mj, sj, thr, c_hi, c_lo, uj;
     float delta, sp_hi, sp_lo, t_hi, t_lo;
@@ -481,11 +495,168 @@ __device__ __forceinline__ void write_sampled(const VerifyArgs& a, int b, int k,
     if (a.row_status) a.row_status[b] = st;
 }
 
+// Fold one pass-1 tile into a consumer thread's online state.  The tile is
+// NT * 64 bytes of one position's logits; thread tid (0 .. NT-1) holds its
+// four 16-byte chunks r = 0 .. 3 in w[r], chunk r covering the tile's
+// elements (tid + r * NT) * (16 / esz) onward; tile_e0 is the index, within
+// the row, of the tile's first element.  Sampled rows keep (m, s): the
+// running maximum and the sum of exp((l - m) / T) (c = log2(e) / T); greedy
+// rows keep the maximum m, its lowest index arg and whether a NaN was seen.
+// Elements past the end of a short tile must hold -inf.
+template <bool BF16, int NT = kConsumers>
+__device__ __forceinline__ void p1_fold_tile(const uint4 (&w)[4], bool greedy, float c, long long tile_e0, int tid,
+                                             float& m, float& s, int& arg, bool& nan_seen) {
+    constexpr int kPer = 4;
+    constexpr int kConsumers = NT;  // the chunk stride of this tile layout
+    float lmax;
+    if (BF16) {
+        if (greedy) {
+            // one NaN-propagating maximum: a NaN only flags the row (its
+            // argmax is undefined), so it may hide the tile's other values
+            uint32_t mx = 0xff80ff80u;
+#pragma unroll
+            for (int r = 0; r < kPer; ++r)
+                mx = max_nan_bf16x2(max_nan_bf16x2(mx, w[r].x),
+                                    max_nan_bf16x2(w[r].y, max_nan_bf16x2(w[r].z, w[r].w)));
+            lmax = max_nan_f32(bf16_lo(mx), bf16_hi(mx));
+            if (lmax != lmax) nan_seen = true;
+        } else {
+            uint32_t mx = 0xff80ff80u;
+#pragma unroll
+            for (int r = 0; r < kPer; ++r)
+                mx = max_bf16x2(max_bf16x2(mx, w[r].x), max_bf16x2(w[r].y, max_bf16x2(w[r].z, w[r].w)));
+            lmax = fmaxf(bf16_lo(mx), bf16_hi(mx));
+        }
+    } else {
+        float mx = -INFINITY, mn = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+            const float f0 = __uint_as_float(w[r].x), f1 = __uint_as_float(w[r].y);
+            const float f2v = __uint_as_float(w[r].z), f3 = __uint_as_float(w[r].w);
+            mx = fmaxf(fmaxf(mx, f0), fmaxf(f1, fmaxf(f2v, f3)));
+            if (greedy) mn = max_nan_f32(max_nan_f32(mn, f0), max_nan_f32(f1, max_nan_f32(f2v, f3)));
+        }
+        lmax = mx;
+        if (greedy && mn != mn) nan_seen = true;
+    }
+    if (greedy) {
+        if (BF16 && lmax > m) {
+            // lowest tile-local index holding the new maximum: the first
+            // chunk whose maximum equals it (chunk r covers elements
+            // ch*8 .. ch*8+7, ch = tid + r*128), then the first such
+            // element in it; the packed compare takes -0 == +0
+            const uint32_t h16 = __float_as_uint(lmax) >> 16;
+            const uint32_t lmw = h16 | (h16 << 16);
+            const __nv_bfloat162 lm2 = *reinterpret_cast<const __nv_bfloat162*>(&lmw);
+            int rs = kPer - 1;
+#pragma unroll
+            for (int r = kPer - 2; r >= 0; --r) {
+                const uint32_t cmr = max_bf16x2(max_bf16x2(w[r].x, w[r].y), max_bf16x2(w[r].z, w[r].w));
+                if (__heq2_mask(*reinterpret_cast<const __nv_bfloat162*>(&cmr), lm2)) rs = r;
+            }
+            uint4 wc = w[kPer - 1];
+#pragma unroll
+            for (int r = kPer - 2; r >= 0; --r)
+                if (r == rs) wc = w[r];
+            const uint32_t ws[4] = {wc.x, wc.y, wc.z, wc.w};
+            int q8 = 7;
+#pragma unroll
+            for (int q4 = 3; q4 >= 0; --q4) {
+                const uint32_t eqm = __heq2_mask(*reinterpret_cast<const __nv_bfloat162*>(&ws[q4]), lm2);
+                if (eqm) q8 = q4 * 2 + ((eqm & 0xffffu) ? 0 : 1);
+            }
+            arg = static_cast<int>(tile_e0 + (tid + rs * kConsumers) * 8 + q8);
+            m = lmax;
+        } else if (!BF16 && lmax > m) {
+            // lowest tile-local index holding the new maximum: the
+            // candidates reduced by min in a tree (chunk r of this
+            // thread covers elements ch*4+..., ch = tid + r*128)
+            constexpr int kPerWord = BF16 ? 2 : 1;
+            constexpr int kCand = kPer * 4 * kPerWord;
+            int cand[kCand];
+#pragma unroll
+            for (int r = 0; r < kPer; ++r) {
+                const int ch = tid + r * kConsumers;
+                const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    if (BF16) {
+                        cand[(r * 4 + q4) * 2] = bf16_lo(ws[q4]) == lmax ? ch * 8 + q4 * 2 : 0x7fffffff;
+                        cand[(r * 4 + q4) * 2 + 1] =
+                            bf16_hi(ws[q4]) == lmax ? ch * 8 + q4 * 2 + 1 : 0x7fffffff;
+                    } else {
+                        cand[r * 4 + q4] = __uint_as_float(ws[q4]) == lmax ? ch * 4 + q4 : 0x7fffffff;
+                    }
+                }
+            }
+#pragma unroll
+            for (int half = kCand / 2; half > 0; half >>= 1)
+#pragma unroll
+                for (int i2 = 0; i2 < half; ++i2) cand[i2] = min(cand[i2], cand[i2 + half]);
+            arg = static_cast<int>(tile_e0 + cand[0]);
+            m = lmax;
+        }
+    } else if (lmax == -INFINITY) {
+        // the max ignores NaN: look for one among -inf entries
+        bool has_nan = false;
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+            const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                if (BF16)
+                    has_nan |= ((ws[q4] & 0x7fffu) > 0x7f80u) || ((ws[q4] & 0x7fff0000u) > 0x7f800000u);
+                else
+                    has_nan |= (ws[q4] & 0x7fffffffu) > 0x7f800000u;
+            }
+        }
+        if (has_nan) s = __uint_as_float(0x7fc00000u);
+    } else {
+        if (lmax > m) {
+            s = (m == -INFINITY) ? s * 0.0f : s * ex2((m - lmax) * c);
+            m = lmax;
+        }
+        // exponents as one fma a pair: l c - r with r = m c rounded; the
+        // rounding error of r (err = m c - r, exact through an fma) scales
+        // every term of the tile alike and is taken out once, to first
+        // order (|err| <= ulp(m c) / 2, so the neglected term is ~1e-12)
+        const float rr = m * c;
+        const float err = fmaf(m, c, -rr);
+        const f2 cc = pack2(c, c), nr = pack2(-rr, -rr);
+        f2 acc = pack2(0.0f, 0.0f);
+#pragma unroll
+        for (int r = 0; r < kPer; ++r) {
+            const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+            if (BF16) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const f2 d = fma2(pack2(bf16_lo(ws[q4]), bf16_hi(ws[q4])), cc, nr);
+                    float d0, d1;
+                    unpack2(d, d0, d1);
+                    acc = add2(acc, pack2(ex2(d0), ex2(d1)));
+                }
+            } else {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; q4 += 2) {
+                    const f2 d = fma2(pack2(__uint_as_float(ws[q4]), __uint_as_float(ws[q4 + 1])), cc, nr);
+                    float d0, d1;
+                    unpack2(d, d0, d1);
+                    acc = add2(acc, pack2(ex2(d0), ex2(d1)));
+                }
+            }
+        }
+        float a0, a1;
+        unpack2(acc, a0, a1);
+        s += (a0 + a1) * fmaf(-err, kLn2, 1.0f);  // back to the scale of m
+    }
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ __align__(16) ClusterSmem sh;
     constexpr int esz = BF16 ? 2 : 4;
+    const unsigned full = 0xffffffffu;
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -500,9 +671,13 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     const int n = static_cast<int>(max(0LL, min(static_cast<long long>(a.slice), V - v0)));
     const unsigned char* lg = reinterpret_cast<const unsigned char*>(a.logits);
     unsigned char* ring = dyn_smem;
-    const int pk = a.pk;
-    Partial* wpart = reinterpret_cast<Partial*>(dyn_smem + kRingBytes);  // [kConsumerWarps][pk]
-    Partial* allpart = wpart + kConsumerWarps * pk;                       // [C][pk]
+    const uint32_t polls = a.polls;
+    Partial* wpart = reinterpret_cast<Partial*>(dyn_smem + kRingBytes);  // [pk][kConsumerWarps]
+    Partial* allpart = wpart + kConsumerWarps * a.pk;                     // [pk][C]: every CTA's, pushed by it
+    // Positions after the first stop are never read: the rule does not look
+    // at them.  Draft trees (every node counts) and calls that ask for every
+    // position's debug values read them all.
+    const bool early = !a.parents && !(a.dbg_p || a.dbg_q || a.dbg_max || a.dbg_sumexp);
 
     // ---------------------------------------------------------------- row setup
     const float T = a.temp ? __ldg(a.temp + b) : 0.0f;
@@ -510,23 +685,12 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     const bool t_ok = greedy || (T >= FLT_MIN && T <= FLT_MAX);
     const float c = greedy || !t_ok ? 0.0f : kLog2e / T;
 
-    // per-position scalars, lane i of warp 0 holds position i
-    int xi = -1, pi = lane - 1;
-    float u0 = 0.0f, u1 = 0.0f, Lx = 0.0f, qx = 0.0f;
-    if (warp == 0 && lane <= k && t_ok) {
-        if (lane < k) xi = __ldg(a.x + static_cast<long long>(b) * k + lane);
-        if (lane < k && a.parents) pi = __ldg(a.parents + static_cast<long long>(b) * k + lane);
-        if (!greedy) {
-            const long long ub = (static_cast<long long>(b) * (k + 1) + lane) * 2;
-            u0 = __ldg(a.u + ub);
-            u1 = __ldg(a.u + ub + 1);
-        }
-    }
     if (tid < 128) sh.exp2tab[tid] = g_exp2_table[tid];
     if (tid < 4) {
         sh.lpad[tid] = BF16 ? 0xff80ff80u : 0xff800000u;
         sh.qpad[tid] = 0.0f;
     }
+    if (tid <= kMaxK) sh.pcnt[tid] = 0;
     if (tid == 32 && !greedy && t_ok) {  // log2(e) / T as a pair, for the exact exponentials
         const df c2 = log2e_over(T);
         sh.c_hi = c2.hi;
@@ -541,14 +705,15 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + v0 + sh.head[i];
         const int slot = it % kStages;
         const uint32_t bar = smem_u32(&sh.full[slot]);
+        if (blockIdx.x == 0 && it == a.withhold) return;  // test hook: this stage is never filled
         mbar_arrive_expect_tx(bar, static_cast<uint32_t>(bytes));
         bulk_g2s(smem_u32(ring + slot * kTileBytes), lg + e0 * esz + off, static_cast<uint32_t>(bytes), bar);
     };
     int it_prod = 0;
     int c_slot = 0, c_phase = 0;  // the consumers' stage and its phase
     if (producer && lane == 0) {
-        // the producer sets up the ring and the slice geometry, and starts the
-        // first copies before the block's first barrier
+        // the producer sets up the ring, the position barriers and the slice
+        // geometry, and starts the first copies before the block's first barrier
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
             mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
@@ -557,7 +722,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             mbar_init(smem_u32(&sh.full2[s]), 1);
             mbar_init(smem_u32(&sh.empty2[s]), 1);
         }
+        for (int i = 0; i <= k; ++i) mbar_init(smem_u32(&sh.pbar[i]), C);  // one arrival per CTA of the cluster
         sh.timeout = 0;
+        sh.p1_end = 0x7fffffff;
+        sh.stop_pos = -1;
         fence_mbar_init();
         fence_proxy_async_smem();
         int acc = 0;
@@ -573,21 +741,18 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             acc += (nb + kTileBytes - 1) / kTileBytes;
         }
         sh.tstart[k + 1] = acc;
-        if (t_ok)
-            for (; it_prod < min(kStages, acc); ++it_prod) issue_p1(it_prod, it_prod);
+        if (t_ok) {
+            const int lim = early ? sh.tstart[min(k, kLook) + 1] : acc;  // the first positions the rule may need
+            for (; it_prod < min(kStages, lim); ++it_prod) issue_p1(it_prod, it_prod);
+        }
     }
     __syncthreads();
+    // Every CTA's position barriers are initialised before any CTA arrives on
+    // them: each thread waits on this cluster barrier before its first remote
+    // arrival (and before the next cluster barrier).
+    cluster_arrive();
     const int total1 = t_ok ? sh.tstart[k + 1] : 0;
 
-    // Ring protocol.  Stage use number `it` (counted identically by producer
-    // and consumers across both passes) occupies slot it % kStages; its full
-    // barrier completes phase (it / kStages) & 1 when the copies land, its
-    // empty barrier when the four consumer warps have released it.
-    auto prod_acquire = [&](int it) -> bool {
-        if (it < kStages) return true;
-        const int slot = it % kStages;
-        return mbar_wait_bounded(smem_u32(&sh.empty[slot]), ((it / kStages) & 1) ^ 1, kWaitPolls);
-    };
     // the consumers' next stage: c_slot = it % kStages, c_phase = (it / kStages) & 1
     auto next_stage = [&]() {
         if (++c_slot == kStages) {
@@ -596,21 +761,228 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         }
     };
 
-    // ---------------------------------------------------------------- pass 1
+    // per-position scalars, lane i of the producer warp holds position i
+    int xi = -1, pi = lane - 1;
+    float u0 = 0.0f, u1 = 0.0f, Lx = 0.0f, qx = 0.0f;
+    int stop = -1;  // the first position that stops the chain (producer warp)
+
+    // ---------------------------------------------------------------- pass 1 and the decisions
     if (producer) {
-        if (lane == 0) {
-            for (int tt = it_prod; tt < total1; ++tt, ++it_prod) {
-                if (sh.timeout || !prod_acquire(it_prod)) {
-                    atomicOr(&sh.timeout, 1);
-                    break;
+        if (lane <= k && t_ok) {
+            if (lane < k) xi = __ldg(a.x + static_cast<long long>(b) * k + lane);
+            if (lane < k && a.parents) pi = __ldg(a.parents + static_cast<long long>(b) * k + lane);
+            if (!greedy) {
+                const long long ub = (static_cast<long long>(b) * (k + 1) + lane) * 2;
+                u0 = __ldg(a.u + ub);
+                u1 = __ldg(a.u + ub + 1);
+                if (lane < k && xi >= 0 && xi < V) {  // the accept test's scalars
+                    const long long row = static_cast<long long>(b) * (k + 1) + lane;
+                    Lx = load_logit(a.logits, row * V + xi, BF16);
+                    qx = a.q ? __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi) : 1.0f;
                 }
-                issue_p1(tt, it_prod);
             }
         }
-        it_prod = __shfl_sync(0xffffffffu, it_prod, 0);
+        it_prod = __shfl_sync(full, it_prod, 0);
+        int ipos = 0;  // the position of tile it_prod
+        while (ipos <= k && sh.tstart[ipos + 1] <= it_prod) ++ipos;
+        const int ndec = t_ok ? k + 1 : 0;
+        int dpos = 0;  // positions decided so far
+        uint32_t idle = 0;
+        unsigned long long t0 = 0;
+        bool gave_up = false;
+        // One loop issues the tiles (lane 0) and takes the decisions (the
+        // whole warp), in position order, as the CTAs' partials come in.  A
+        // tile is issued only when its position is at most kLook beyond the
+        // first undecided one, so that at most kLook positions past the stop
+        // are read.
+        while (dpos < ndec && (stop < 0 || !early)) {
+            bool progress = false;
+            if (it_prod < total1 && (!early || ipos <= dpos + kLook) && !*reinterpret_cast<volatile int*>(&sh.timeout)) {
+                int room = 1;
+                if (lane == 0 && it_prod >= kStages)
+                    room = mbar_test_wait(smem_u32(&sh.empty[it_prod % kStages]), ((it_prod / kStages) & 1) ^ 1);
+                if (__shfl_sync(full, room, 0)) {
+                    if (lane == 0) issue_p1(it_prod, it_prod);
+                    ++it_prod;
+                    while (ipos <= k && sh.tstart[ipos + 1] <= it_prod) ++ipos;
+                    progress = true;
+                }
+            }
+            if (__all_sync(full, mbar_test_wait_cluster(smem_u32(&sh.pbar[dpos]), 0))) {
+                // position i: merge the C partials (lane r holds CTA r's), then its test
+                const int i = dpos;
+                const Partial pr = lane < static_cast<int>(C) ? allpart[i * C + lane]
+                                                             : Partial{-INFINITY, 0.0f, 0x7fffffff, 0};
+                const int F = static_cast<int>(__reduce_or_sync(full, static_cast<unsigned>(pr.flags)));
+                float M, S = 0.0f;
+                int A = 0x7fffffff;
+                if (greedy) {
+                    float mv = pr.m;
+                    int ar = pr.arg;
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const float m2 = __shfl_xor_sync(full, mv, off);
+                        const int a2 = __shfl_xor_sync(full, ar, off);
+                        merge_arg(mv, ar, m2, a2);
+                    }
+                    M = __shfl_sync(full, mv, 0);
+                    A = __shfl_sync(full, ar, 0);
+                    if (A == 0x7fffffff) A = 0;  // every value is -inf: index 0
+                } else {
+                    M = warp_max_f32(pr.m);
+                    float tt = ms_term(pr.m, pr.s, M, c);
+                    for (int off = 16; off > 0; off >>= 1) tt += __shfl_xor_sync(full, tt, off);
+                    S = tt;
+                }
+                const int x = __shfl_sync(full, xi, i);
+                const float uu = __shfl_sync(full, u0, i), lx = __shfl_sync(full, Lx, i), qq = __shfl_sync(full, qx, i);
+                int err = 0;
+                bool stp = true;
+                float p = 0.0f;
+                if (F & 2) err |= ST_TIMEOUT;
+                if (a.parents) {
+                    stp = false;  // a tree: every node is decided at the end
+                } else if (greedy) {
+                    if (F & 1) err |= ST_NONFINITE;
+                    if (i < k && (x < 0 || x >= V)) err |= ST_TOKEN;
+                    stp = (err != 0) || i == k || x != A;
+                } else {
+                    if (!(isfinite(M) && isfinite(S))) err |= ST_NONFINITE;
+                    if (i < k) {
+                        if (x < 0 || x >= V) err |= ST_TOKEN;
+                        if (!(uu >= 0.0f && uu < 1.0f)) err |= ST_UNIFORM;
+                        if (x >= 0 && x < V && !(qq >= 0.0f && qq <= FLT_MAX)) err |= ST_QBAD;
+                        if (!err) {
+                            // p_i(x_i) with the double-float exponential (a masked
+                            // entry, logit -inf, has p = 0)
+                            RowConst rc;
+                            rc.M = M;
+                            rc.s1 = S;
+                            rc.thr = 0.0f;
+                            rc.ch = sh.c_hi;
+                            rc.cl = sh.c_lo;
+                            p = df_val(exact_weight<BF16>(lx, 0.0f, MODE_BONUS, rc, df_make(0.0f), sh.exp2tab)) / S;
+                            const float rho = fminf(1.0f, p / fmaxf(qq, 1e-12f));
+                            stp = !(uu < rho);
+                        }
+                    }
+                }
+                if (lane == 0) {
+                    sh.posM[i] = M;
+                    sh.posS[i] = S;
+                    sh.posA[i] = A;
+                    sh.posF[i] = F;
+                    sh.posE[i] = err;
+                    sh.posP[i] = p;
+                }
+                if (stp && stop < 0) stop = i;
+                ++dpos;
+                progress = true;
+            }
+            if (progress) {
+                idle = 0;
+                t0 = 0;
+                continue;
+            }
+            bool give = ++idle >= polls;
+            if ((idle & 255) == 255) {
+                const unsigned long long tn = gtimer();
+                if (t0 == 0)
+                    t0 = tn;
+                else if (tn - t0 > kWaitNs)
+                    give = true;
+            }
+            if (__any_sync(full, give)) {
+                gave_up = true;
+                break;
+            }
+        }
+        if (gave_up) {
+            // a CTA's partials never came: the undecided positions end the row
+            if (lane == 0) atomicOr(&sh.timeout, 1);
+            if (lane >= dpos && lane <= k) {
+                sh.posM[lane] = -INFINITY;
+                sh.posS[lane] = 0.0f;
+                sh.posA[lane] = 0;
+                sh.posF[lane] = 2;
+                sh.posE[lane] = ST_TIMEOUT;
+                sh.posP[lane] = 0.0f;
+            }
+            if (stop < 0) stop = dpos;
+        }
+        if (lane == 0) {
+            *reinterpret_cast<volatile int*>(&sh.p1_end) = it_prod;  // no pass-1 copy is issued after this
+            __threadfence_block();
+            *reinterpret_cast<volatile int*>(&sh.stop_pos) = stop >= 0 ? stop : k;
+            if (!gave_up && it_prod < total1) {
+                // The consumers go on to stage use it_prod, which is never filled:
+                // complete its phase without data (once its slot's previous use
+                // is released, so that the phase is that use's), which wakes
+                // them at once; they see it_prod >= p1_end and stop.
+                const int slot = it_prod % kStages;
+                if (it_prod < kStages ||
+                    mbar_wait_bounded(smem_u32(&sh.empty[slot]), ((it_prod / kStages) & 1) ^ 1, polls))
+                    mbar_arrive(smem_u32(&sh.full[slot]));
+            }
+        }
+        __syncwarp();
+        cluster_wait();
     } else {
         int t = 0;
+        bool waited = false;  // this warp has waited on the cluster barrier above
+        bool bail = false;    // a wait gave up
+        int reported = 0;     // positions this warp has reported
+        // Report this warp's partial of position i; the CTA's last warp to
+        // report it merges the four and pushes the CTA's partial into every
+        // CTA of the cluster, then arrives on their barriers of position i.
+        auto report = [&](int i, Partial P) {
+            int last = 0;
+            if (lane == 0) {
+                wpart[i * kConsumerWarps + warp] = P;
+                __threadfence_block();
+                last = atomicAdd(&sh.pcnt[i], 1) == kConsumerWarps - 1;
+            }
+            if (!__shfl_sync(full, last, 0)) return;
+            __threadfence_block();
+            const volatile Partial* wp = wpart + i * kConsumerWarps;
+            Partial q{-INFINITY, 0.0f, 0x7fffffff, 0};
+            if (lane < kConsumerWarps) {
+                q.m = wp[lane].m;
+                q.s = wp[lane].s;
+                q.arg = wp[lane].arg;
+                q.flags = wp[lane].flags;
+            }
+            const int F = static_cast<int>(__reduce_or_sync(full, static_cast<unsigned>(q.flags)));
+            float M, S = 0.0f;
+            int A = 0x7fffffff;
+            if (greedy) {
+                float mv = q.m;
+                int ar = q.arg;
+                for (int off = 2; off > 0; off >>= 1) {
+                    const float m2 = __shfl_xor_sync(full, mv, off);
+                    const int a2 = __shfl_xor_sync(full, ar, off);
+                    merge_arg(mv, ar, m2, a2);
+                }
+                M = __shfl_sync(full, mv, 0);
+                A = __shfl_sync(full, ar, 0);
+            } else {
+                M = warp_max_f32(q.m);
+                float tt = ms_term(q.m, q.s, M, c);
+                for (int off = 2; off > 0; off >>= 1) tt += __shfl_xor_sync(full, tt, off);
+                S = __shfl_sync(full, tt, 0);  // lanes 0..3 hold the sum
+            }
+            if (!waited) {
+                cluster_wait();
+                waited = true;
+            }
+            if (lane < static_cast<int>(C)) {
+                st_cluster_v4(map_rank(smem_u32(&allpart[i * C + rank]), lane), __float_as_uint(M), __float_as_uint(S),
+                              static_cast<uint32_t>(A), static_cast<uint32_t>(F));
+                mbar_arrive_cluster(map_rank(smem_u32(&sh.pbar[i]), lane));
+            }
+        };
         for (int i = 0; i <= k && t_ok; ++i) {
+            const int sp = *reinterpret_cast<volatile int*>(&sh.stop_pos);
+            const bool skip = early && sp >= 0 && i > sp;  // past the stop: copies landed are let go unread
             float m = -INFINITY, s = 0.0f;  // sampled state
             int arg = 0x7fffffff;           // greedy state (m holds the best value)
             bool nan_seen = false;
@@ -631,190 +1003,82 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                     online_add(m, s, l, c);
                 }
             };
-            if (tid == 0)
+            if (tid == 0 && !skip)
                 for (int e = 0; e < h; ++e) scalar_elem(e);
             __syncwarp();  // reconverge before the tile loop's warp-wide steps
 
+            bool ended = false;
             for (int lt = 0; lt < ntiles; ++lt, ++t, next_stage()) {
-                if (t == 2 && warp == 0 && lane < k && !greedy && xi >= 0 && xi < V) {
-                    // the accept test's scalars; x_i has long arrived
-                    const long long row = static_cast<long long>(b) * (k + 1) + lane;
-                    Lx = load_logit(a.logits, row * V + xi, BF16);
-                    qx = a.q ? __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi) : 1.0f;
+                // 0: the stage is full; 1: pass 1 ended before issuing it; 2: a wait gave up
+                int r = 2;
+                {
+                    unsigned long long w0 = 0;
+                    for (uint32_t it = 0; it < polls; ++it) {
+                        if (mbar_try_wait(smem_u32(&sh.full[c_slot]), c_phase)) {
+                            // a phase completed without data marks the end of pass 1
+                            r = t >= *reinterpret_cast<volatile int*>(&sh.p1_end) ? 1 : 0;
+                            break;
+                        }
+                        if (t >= *reinterpret_cast<volatile int*>(&sh.p1_end)) {
+                            r = 1;
+                            break;
+                        }
+                        if (*reinterpret_cast<volatile int*>(&sh.timeout)) break;
+                        if ((it & 255) == 255) {
+                            const unsigned long long tn = gtimer();
+                            if (w0 == 0)
+                                w0 = tn;
+                            else if (tn - w0 > kWaitNs)
+                                break;
+                        }
+                    }
                 }
-                const bool ok = !sh.timeout && mbar_wait_bounded(smem_u32(&sh.full[c_slot]), c_phase, kWaitPolls);
+                // the warp agrees on the outcome: lanes that went different ways
+                // here would meet the full-mask shuffles below apart
+                r = __reduce_max_sync(full, r);
+                if (r == 1) {
+                    ended = true;
+                    break;
+                }
+                if (r == 2) {
+                    if (lane == 0) atomicOr(&sh.timeout, 1);
+                    bail = true;
+                    break;
+                }
                 const int bytes = min(kTileBytes, sh.nbytes[i] - lt * kTileBytes);
                 const int nch = bytes >> 4;
                 const uint32_t tile = smem_u32(ring + c_slot * kTileBytes);
-                if (!ok) {
-                    atomicOr(&sh.timeout, 1);
+                if (skip) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&sh.empty[c_slot]));
                     continue;
                 }
                 constexpr int kPer = kTileBytes / 16 / kConsumers;  // 16-byte chunks per thread
                 uint4 w[kPer];
                 if (nch == kTileBytes / 16) {  // a full tile (all but a position's last)
 #pragma unroll
-                    for (int r = 0; r < kPer; ++r) w[r] = ld_shared_v4(tile + (tid + r * kConsumers) * 16);
+                    for (int r2 = 0; r2 < kPer; ++r2) w[r2] = ld_shared_v4(tile + (tid + r2 * kConsumers) * 16);
                 } else {
 #pragma unroll
-                    for (int r = 0; r < kPer; ++r) {
-                        const int ch = tid + r * kConsumers;
+                    for (int r2 = 0; r2 < kPer; ++r2) {
+                        const int ch = tid + r2 * kConsumers;
                         if (ch < nch) {
-                            w[r] = ld_shared_v4(tile + ch * 16);
+                            w[r2] = ld_shared_v4(tile + ch * 16);
                         } else if (BF16) {
-                            w[r] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+                            w[r2] = make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
                         } else {
                             const uint32_t ni = __float_as_uint(-INFINITY);
-                            w[r] = make_uint4(ni, ni, ni, ni);
+                            w[r2] = make_uint4(ni, ni, ni, ni);
                         }
                     }
                 }
                 __syncwarp();  // the data is in registers: release the stage
                 if (lane == 0) mbar_arrive(smem_u32(&sh.empty[c_slot]));
-                float lmax;
-                if (BF16) {
-                    if (greedy) {
-                        // one NaN-propagating maximum: a NaN only flags the row (its
-                        // argmax is undefined), so it may hide the tile's other values
-                        uint32_t mx = 0xff80ff80u;
-#pragma unroll
-                        for (int r = 0; r < kPer; ++r)
-                            mx = max_nan_bf16x2(max_nan_bf16x2(mx, w[r].x),
-                                                max_nan_bf16x2(w[r].y, max_nan_bf16x2(w[r].z, w[r].w)));
-                        lmax = max_nan_f32(bf16_lo(mx), bf16_hi(mx));
-                        if (lmax != lmax) nan_seen = true;
-                    } else {
-                        uint32_t mx = 0xff80ff80u;
-#pragma unroll
-                        for (int r = 0; r < kPer; ++r)
-                            mx = max_bf16x2(max_bf16x2(mx, w[r].x), max_bf16x2(w[r].y, max_bf16x2(w[r].z, w[r].w)));
-                        lmax = fmaxf(bf16_lo(mx), bf16_hi(mx));
-                    }
-                } else {
-                    float mx = -INFINITY, mn = -INFINITY;
-#pragma unroll
-                    for (int r = 0; r < kPer; ++r) {
-                        const float f0 = __uint_as_float(w[r].x), f1 = __uint_as_float(w[r].y);
-                        const float f2v = __uint_as_float(w[r].z), f3 = __uint_as_float(w[r].w);
-                        mx = fmaxf(fmaxf(mx, f0), fmaxf(f1, fmaxf(f2v, f3)));
-                        if (greedy) mn = max_nan_f32(max_nan_f32(mn, f0), max_nan_f32(f1, max_nan_f32(f2v, f3)));
-                    }
-                    lmax = mx;
-                    if (greedy && mn != mn) nan_seen = true;
-                }
-                if (greedy) {
-                    if (BF16 && lmax > m) {
-                        // lowest tile-local index holding the new maximum: the first
-                        // chunk whose maximum equals it (chunk r covers elements
-                        // ch*8 .. ch*8+7, ch = tid + r*128), then the first such
-                        // element in it; the packed compare takes -0 == +0
-                        const uint32_t h16 = __float_as_uint(lmax) >> 16;
-                        const uint32_t lmw = h16 | (h16 << 16);
-                        const __nv_bfloat162 lm2 = *reinterpret_cast<const __nv_bfloat162*>(&lmw);
-                        int rs = kPer - 1;
-#pragma unroll
-                        for (int r = kPer - 2; r >= 0; --r) {
-                            const uint32_t cmr = max_bf16x2(max_bf16x2(w[r].x, w[r].y), max_bf16x2(w[r].z, w[r].w));
-                            if (__heq2_mask(*reinterpret_cast<const __nv_bfloat162*>(&cmr), lm2)) rs = r;
-                        }
-                        uint4 wc = w[kPer - 1];
-#pragma unroll
-                        for (int r = kPer - 2; r >= 0; --r)
-                            if (r == rs) wc = w[r];
-                        const uint32_t ws[4] = {wc.x, wc.y, wc.z, wc.w};
-                        int q8 = 7;
-#pragma unroll
-                        for (int q4 = 3; q4 >= 0; --q4) {
-                            const uint32_t eqm = __heq2_mask(*reinterpret_cast<const __nv_bfloat162*>(&ws[q4]), lm2);
-                            if (eqm) q8 = q4 * 2 + ((eqm & 0xffffu) ? 0 : 1);
-                        }
-                        const long long tile_e0 = v0 + h + static_cast<long long>(lt) * (kTileBytes / esz);
-                        arg = static_cast<int>(tile_e0 + (tid + rs * kConsumers) * 8 + q8);
-                        m = lmax;
-                    } else if (!BF16 && lmax > m) {
-                        // lowest tile-local index holding the new maximum: the
-                        // candidates reduced by min in a tree (chunk r of this
-                        // thread covers elements ch*4+..., ch = tid + r*128)
-                        constexpr int kPerWord = BF16 ? 2 : 1;
-                        constexpr int kCand = kPer * 4 * kPerWord;
-                        int cand[kCand];
-#pragma unroll
-                        for (int r = 0; r < kPer; ++r) {
-                            const int ch = tid + r * kConsumers;
-                            const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                if (BF16) {
-                                    cand[(r * 4 + q4) * 2] = bf16_lo(ws[q4]) == lmax ? ch * 8 + q4 * 2 : 0x7fffffff;
-                                    cand[(r * 4 + q4) * 2 + 1] =
-                                        bf16_hi(ws[q4]) == lmax ? ch * 8 + q4 * 2 + 1 : 0x7fffffff;
-                                } else {
-                                    cand[r * 4 + q4] = __uint_as_float(ws[q4]) == lmax ? ch * 4 + q4 : 0x7fffffff;
-                                }
-                            }
-                        }
-#pragma unroll
-                        for (int half = kCand / 2; half > 0; half >>= 1)
-#pragma unroll
-                            for (int i2 = 0; i2 < half; ++i2) cand[i2] = min(cand[i2], cand[i2 + half]);
-                        const long long tile_e0 = v0 + h + static_cast<long long>(lt) * (kTileBytes / esz);
-                        arg = static_cast<int>(tile_e0 + cand[0]);
-                        m = lmax;
-                    }
-                } else if (lmax == -INFINITY) {
-                    // the max ignores NaN: look for one among -inf entries
-                    bool has_nan = false;
-#pragma unroll
-                    for (int r = 0; r < kPer; ++r) {
-                        const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
-#pragma unroll
-                        for (int q4 = 0; q4 < 4; ++q4) {
-                            if (BF16)
-                                has_nan |= ((ws[q4] & 0x7fffu) > 0x7f80u) || ((ws[q4] & 0x7fff0000u) > 0x7f800000u);
-                            else
-                                has_nan |= (ws[q4] & 0x7fffffffu) > 0x7f800000u;
-                        }
-                    }
-                    if (has_nan) s = __uint_as_float(0x7fc00000u);
-                } else {
-                    if (lmax > m) {
-                        s = (m == -INFINITY) ? s * 0.0f : s * ex2((m - lmax) * c);
-                        m = lmax;
-                    }
-                    // exponents as one fma a pair: l c - r with r = m c rounded; the
-                    // rounding error of r (err = m c - r, exact through an fma) scales
-                    // every term of the tile alike and is taken out once, to first
-                    // order (|err| <= ulp(m c) / 2, so the neglected term is ~1e-12)
-                    const float rr = m * c;
-                    const float err = fmaf(m, c, -rr);
-                    const f2 cc = pack2(c, c), nr = pack2(-rr, -rr);
-                    f2 acc = pack2(0.0f, 0.0f);
-#pragma unroll
-                    for (int r = 0; r < kPer; ++r) {
-                        const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
-                        if (BF16) {
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; ++q4) {
-                                const f2 d = fma2(pack2(bf16_lo(ws[q4]), bf16_hi(ws[q4])), cc, nr);
-                                float d0, d1;
-                                unpack2(d, d0, d1);
-                                acc = add2(acc, pack2(ex2(d0), ex2(d1)));
-                            }
-                        } else {
-#pragma unroll
-                            for (int q4 = 0; q4 < 4; q4 += 2) {
-                                const f2 d = fma2(pack2(__uint_as_float(ws[q4]), __uint_as_float(ws[q4 + 1])), cc, nr);
-                                float d0, d1;
-                                unpack2(d, d0, d1);
-                                acc = add2(acc, pack2(ex2(d0), ex2(d1)));
-                            }
-                        }
-                    }
-                    float a0, a1;
-                    unpack2(acc, a0, a1);
-                    s += (a0 + a1) * fmaf(-err, kLn2, 1.0f);  // back to the scale of m
-                }
+                const long long tile_e0 = v0 + h + static_cast<long long>(lt) * (kTileBytes / esz);
+                p1_fold_tile<BF16>(w, greedy, c, tile_e0, tid, m, s, arg, nan_seen);
             }
+            if (ended || bail) break;
+            if (skip) continue;
             if (tid == 0)
                 for (int e = h + interior; e < n; ++e) scalar_elem(e);
             __syncwarp();  // a diverged warp makes every shuffle below slow
@@ -822,128 +1086,82 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             // warp reduction of this position's partial
             if (greedy) {
                 for (int off = 16; off > 0; off >>= 1) {
-                    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                    const int a2 = __shfl_xor_sync(0xffffffffu, arg, off);
+                    const float m2 = __shfl_xor_sync(full, m, off);
+                    const int a2 = __shfl_xor_sync(full, arg, off);
                     merge_arg(m, arg, m2, a2);
                 }
-                nan_seen = __any_sync(0xffffffffu, nan_seen);
+                nan_seen = __any_sync(full, nan_seen);
             } else {
                 // the warp's maximum, every lane's sum brought to it, then the total
                 const float Mw = warp_max_f32(m);
                 float sw = ms_term(m, s, Mw, c);
-                for (int off = 16; off > 0; off >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, off);
+                for (int off = 16; off > 0; off >>= 1) sw += __shfl_xor_sync(full, sw, off);
                 m = Mw;
                 s = sw;
             }
-            if (lane == 0) wpart[warp * pk + i] = Partial{m, s, arg, nan_seen ? 1 : 0};
+            report(i, Partial{m, s, arg, nan_seen ? 1 : 0});
+            reported = i + 1;
         }
-        // rows too short to reach the third tile load the scalars here
-        if (t_ok && total1 <= 2 && warp == 0 && lane < k && !greedy && xi >= 0 && xi < V) {
-            const long long row = static_cast<long long>(b) * (k + 1) + lane;
-            Lx = load_logit(a.logits, row * V + xi, BF16);
-            qx = a.q ? __ldg(a.q + (static_cast<long long>(b) * k + lane) * V + xi) : 1.0f;
-        }
+        // a wait that gave up: the positions this warp has not reported are
+        // reported as timed out, so that no CTA of the cluster waits for them
+        if (bail)
+            for (int i = reported; i <= k; ++i) report(i, Partial{-INFINITY, 0.0f, 0x7fffffff, 2});
+        if (!waited) cluster_wait();
     }
-    __syncthreads();
-    const bool timed_out = sh.timeout != 0;
-    if (tid <= k && t_ok) {
-        Partial p = wpart[tid];
-        if (greedy) {
-            for (int w = 1; w < kConsumerWarps; ++w) {
-                const Partial o = wpart[w * pk + tid];
-                merge_arg(p.m, p.arg, o.m, o.arg);
-                p.flags |= o.flags;
-            }
-        } else {
-            for (int w = 1; w < kConsumerWarps; ++w) p.m = fmaxf(p.m, wpart[w * pk + tid].m);
-            float S = 0.0f;
-            for (int w = 0; w < kConsumerWarps; ++w) S += ms_term(wpart[w * pk + tid].m, wpart[w * pk + tid].s, p.m, c);
-            p.s = S;
-        }
-        if (timed_out) p.flags |= 2;
-        // push this CTA's partial of position tid into every CTA of the cluster
-        const uint32_t local = smem_u32(&allpart[rank * pk + tid]);
-        for (uint32_t r = 0; r < C; ++r)
-            st_cluster_v4(map_rank(local, r), __float_as_uint(p.m), __float_as_uint(p.s), static_cast<uint32_t>(p.arg),
-                          static_cast<uint32_t>(p.flags));
+    __syncthreads();  // pass 1 is over: no stage is read any more
+    if (sh.timeout != 0 && producer && lane == 0) {
+        // no bulk copy may outlive the wait that gave up on it: wait (bounded)
+        // for the last use of every stage that was issued
+        for (int it = max(0, it_prod - kStages); it < it_prod; ++it)
+            mbar_wait_bounded(smem_u32(&sh.full[it % kStages]), (it / kStages) & 1, polls);
     }
-    cluster_sync();  // #1: every CTA's partials are visible
 
-    // ---------------------------------------------------------------- decisions
-    if (warp == 0) {
-        float M = -INFINITY, S = 0.0f;
-        int A = 0x7fffffff, flags = 0;
-        if (lane <= k && t_ok) {
-            for (uint32_t r = 0; r < C; ++r) {
-                const Partial pr = allpart[r * pk + lane];
-                flags |= pr.flags;
-                if (greedy)
-                    merge_arg(M, A, pr.m, pr.arg);
-                else
-                    M = fmaxf(M, pr.m);
+    // ---------------------------------------------------------------- the row's outcome
+    // Every CTA decided from the same partials, so all reach the same
+    // outcome unless a wait gave up somewhere; each pushes its own to every
+    // CTA, and a disagreement ends the row with a timeout.  After the cluster
+    // barrier below no CTA touches another's shared memory on this path.
+    int oj = 0, ost = ST_TEMP;  // this CTA's outcome: stop position and status
+    if (producer) {
+        if (a.parents) {
+            ost = 0;
+            if (lane <= k && (sh.posF[lane] & 2)) ost = ST_TIMEOUT;
+            ost = static_cast<int>(__reduce_or_sync(full, static_cast<unsigned>(ost)));
+        } else if (t_ok) {
+            oj = stop;
+            ost = sh.posE[oj];
+            if (!greedy && !(ost & ST_ERRMASK)) {
+                const float uj = __shfl_sync(full, u1, oj);
+                if (!(uj >= 0.0f && uj < 1.0f)) ost |= ST_UNIFORM;
             }
-            if (!greedy)
-                for (uint32_t r = 0; r < C; ++r) S += ms_term(allpart[r * pk + lane].m, allpart[r * pk + lane].s, M, c);
-            if (greedy && A == 0x7fffffff) A = 0;  // every value is -inf: index 0
         }
-        __syncwarp();
+        if (lane < static_cast<int>(C))
+            st_cluster_v2(map_rank(smem_u32(&sh.views[rank]), lane), static_cast<uint32_t>(oj), static_cast<uint32_t>(ost));
+    }
+    cluster_sync();  // #1: every CTA's outcome is visible
+    if (producer) {
+        const bool same = lane >= static_cast<int>(C) || (sh.views[lane].x == oj && sh.views[lane].y == ost);
+        const bool agreed = __all_sync(full, same);
+        const bool have = lane <= k && t_ok;
+        const float M = have ? sh.posM[lane] : 0.0f;
+        const float S = have ? sh.posS[lane] : 0.0f;
+        const int A = have ? sh.posA[lane] : 0;
         if (a.parents) {
             // a draft tree (all rows greedy): rank 0 writes the outputs
-            const int terr = tree_greedy_warp(a, b, k, lane, xi, pi, A, flags, rank == 0);
+            const int F = (have ? sh.posF[lane] : 0) | (agreed ? 0 : 2);
+            const int terr = tree_greedy_warp(a, b, k, lane, xi, pi, A, F, rank == 0);
             if (lane == 0) {
                 sh.status = terr;
                 sh.j = 0;
             }
             if (rank == 0 && lane <= k && a.dbg_max) a.dbg_max[static_cast<long long>(b) * (k + 1) + lane] = M;
-        }
-        if (!a.parents) {  // a chain of drafts
-            int err = 0;
-            bool stop = false;
-            float p = 0.0f;
-            if (lane <= k && t_ok) {
-                if (flags & 2) err |= ST_TIMEOUT;
-                if (greedy) {
-                    if (flags & 1) err |= ST_NONFINITE;
-                    if (lane < k && (xi < 0 || xi >= V)) err |= ST_TOKEN;
-                    stop = (err != 0) || lane == k || xi != A;
-                } else {
-                    if (!(isfinite(M) && isfinite(S))) err |= ST_NONFINITE;
-                    if (lane < k) {
-                        if (xi < 0 || xi >= V) err |= ST_TOKEN;
-                        if (!(u0 >= 0.0f && u0 < 1.0f)) err |= ST_UNIFORM;
-                        if (xi >= 0 && xi < V && !(qx >= 0.0f && qx <= FLT_MAX)) err |= ST_QBAD;
-                        if (!err) {
-                            // p_i(x_i) with the double-float exponential (a masked
-                            // entry, logit -inf, has p = 0)
-                            RowConst rc;
-                            rc.M = M;
-                            rc.s1 = S;
-                            rc.thr = 0.0f;
-                            rc.ch = sh.c_hi;
-                            rc.cl = sh.c_lo;
-                            p = df_val(exact_weight<BF16>(Lx, 0.0f, MODE_BONUS, rc, df_make(0.0f), sh.exp2tab)) / S;
-                            const float rho = fminf(1.0f, p / fmaxf(qx, 1e-12f));
-                            stop = !(u0 < rho);
-                        } else {
-                            stop = true;
-                        }
-                    } else {
-                        stop = true;
-                    }
-                }
-            }
-            __syncwarp();
-            const unsigned mask = __ballot_sync(0xffffffffu, lane <= k && stop);
-            const int j = t_ok ? (__ffs(mask) - 1) : 0;
-            int st = t_ok ? __shfl_sync(0xffffffffu, err, j) : ST_TEMP;
-            if (t_ok && !greedy && !(st & ST_ERRMASK)) {
-                const float uj = __shfl_sync(0xffffffffu, u1, j);
-                if (!(uj >= 0.0f && uj < 1.0f)) st |= ST_UNIFORM;
-            }
-            const float Mj = __shfl_sync(0xffffffffu, M, j);
-            const float Sj = __shfl_sync(0xffffffffu, S, j);
-            const int Aj = __shfl_sync(0xffffffffu, A, j);
-            const float ujj = __shfl_sync(0xffffffffu, u1, j);
+        } else {
+            const int j = agreed ? oj : 0;
+            const int st = agreed ? ost : ST_TIMEOUT;
+            const float Mj = __shfl_sync(full, M, j);
+            const float Sj = __shfl_sync(full, S, j);
+            const int Aj = __shfl_sync(full, A, j);
+            const float ujj = __shfl_sync(full, u1, j);
             if (lane == 0) {
                 sh.uj = ujj;
                 sh.j = j;
@@ -973,12 +1191,12 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             if (lane <= k) sh.xs[lane] = xi;
             // rank 0 writes debug values and, for greedy or failed rows, the outputs
             if (rank == 0) {
-                if (lane <= k && t_ok) {
+                if (have) {
                     if (a.dbg_max) a.dbg_max[static_cast<long long>(b) * (k + 1) + lane] = M;
                     if (a.dbg_sumexp) a.dbg_sumexp[static_cast<long long>(b) * (k + 1) + lane] = greedy ? 0.0f : S;
                     if (lane < k) {
                         const bool xok = xi >= 0 && xi < V;
-                        if (a.dbg_p) a.dbg_p[static_cast<long long>(b) * k + lane] = (greedy || !xok) ? 0.0f : p;
+                        if (a.dbg_p) a.dbg_p[static_cast<long long>(b) * k + lane] = (greedy || !xok) ? 0.0f : sh.posP[lane];
                         if (a.dbg_q) a.dbg_q[static_cast<long long>(b) * k + lane] = (greedy || !xok) ? 0.0f : qx;
                     }
                 }
@@ -1000,10 +1218,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     }
     __syncthreads();
     const bool sample = t_ok && !greedy && !(sh.status & ST_ERRMASK);
-    if (!sample) {
-        cluster_sync();  // no CTA leaves while a peer may still read its partials
-        return;
-    }
+    if (!sample) return;
 
     // ---------------------------------------------------------------- pass 2
     const int j = sh.j;
@@ -1074,7 +1289,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 for (int t2 = 0; t2 < ntiles2; ++t2) {
                     const int g = g2 + t2;
                     if (sh.timeout ||
-                        (g >= S2 && !mbar_wait_bounded(smem_u32(&sh.empty2[slot]), phase ^ 1, kWaitPolls))) {
+                        (g >= S2 && !mbar_wait_bounded(smem_u32(&sh.empty2[slot]), phase ^ 1, polls))) {
                         atomicOr(&sh.timeout, 1);
                         break;
                     }
@@ -1113,7 +1328,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 bool ok = true;
                 if (p2fast) {
                     ok = __all_sync(0xffffffffu, !sh.timeout &&
-                                                     mbar_wait_bounded(smem_u32(&sh.full2[my_slot]), my_phase, kWaitPolls));
+                                                     mbar_wait_bounded(smem_u32(&sh.full2[my_slot]), my_phase, polls));
                     if (!ok && lane == 0) atomicOr(&sh.timeout, 1);
                 } else {
                     // unaligned rows: the warp stages its own tiles in slot

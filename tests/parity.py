@@ -42,11 +42,26 @@ def _outcome(res, b):
     return (int(res["num_accepted"][b]), tuple(int(t) for t in res["out_tokens"][b]), int(res["row_status"][b]))
 
 
-def compare(w, got, ref=None, *, check_debug=False):
+def plain_rows(w):
+    """The oracle of the plain rule on rows ``sl`` of workload ``w`` with
+    uniforms ``u`` for those rows."""
+    def run(sl, u, debug=False):
+        return oracle.verify(w.logits[sl], None if w.q is None else w.q[sl], w.x[sl], u, w.T[sl], debug=debug,
+                             nthreads=8)
+    return run
+
+
+def compare(w, got, ref=None, *, check_debug=False, oracle_rows=None):
     """Assert parity of ``got`` (GPU outputs as numpy) with the oracle on
-    workload ``w``; return counts {rows, flagged, mismatched}."""
-    if ref is None:
-        ref = oracle.verify(w.logits, w.q, w.x, w.u, w.T, debug=check_debug, nthreads=8)
+    workload ``w``; return counts {rows, flagged, mismatched}.
+    ``oracle_rows(sl, u)`` evaluates the oracle on rows ``sl`` with uniforms
+    ``u`` (default: the plain rule)."""
+    if oracle_rows is None:
+        oracle_rows = plain_rows(w)
+        if ref is None:
+            ref = oracle_rows(slice(None), w.u, debug=check_debug)
+    elif ref is None:
+        ref = oracle_rows(slice(None), w.u)
     B = w.B
     same = ((got["num_accepted"] == ref["num_accepted"]) & (got["row_status"] == ref["row_status"])
             & (got["out_tokens"] == ref["out_tokens"]).all(1))
@@ -59,13 +74,12 @@ def compare(w, got, ref=None, *, check_debug=False):
     for b in mism:
         idx = int(ref["boundary"][b]) - 1
         i, slot = idx // 2, idx % 2
-        sub = (w.logits[b:b + 1], None if w.q is None else w.q[b:b + 1], w.x[b:b + 1], w.T[b:b + 1])
         top = np.nextafter(np.float32(1), np.float32(0))
 
         def outcome_at(u_val):
             uu = w.u[b:b + 1].copy()
             uu[0, i, slot] = np.float32(np.clip(u_val, 0.0, top))
-            return _outcome(oracle.verify(sub[0], sub[1], sub[2], uu, sub[3]), 0)
+            return _outcome(oracle_rows(slice(b, b + 1), uu), 0)
 
         want = _outcome(got, b)
         have = _outcome(ref, b)

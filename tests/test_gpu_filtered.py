@@ -1,7 +1,9 @@
 """GPU parity of top-k / top-p verification with the oracle ("Speculative
 decoding." lesson, "Why the output is exactly p": the filters are applied to
-p before the rule).  Integer outputs must match on every row whose uniforms
-lie away from the decision edges (the oracle's boundary flag)."""
+p before the rule).  Integer outputs must match the oracle's on every row;
+a row whose uniform lies within 1e-6 of a decision edge of the oracle may
+differ only as parity.compare allows: its outcome must be the oracle's
+outcome for that uniform moved by at most 1e-6."""
 import numpy as np
 import pytest
 
@@ -35,14 +37,20 @@ def _run(h, w, top_k, top_p, onehot=False):
 
 
 def _check(w, got, top_k, top_p, onehot=False):
-    ref = oracle.verify_warped(w.logits, None if onehot else w.q, w.x, w.u, w.T, top_k, top_p)
-    same = ((got["num_accepted"] == ref["num_accepted"]) & (got["row_status"] == ref["row_status"])
-            & (got["out_tokens"] == ref["out_tokens"]).all(1))
-    flagged = ref["boundary"] != 0
-    bad = np.nonzero(~same & ~flagged)[0]
-    assert len(bad) == 0, (bad[:5], got["out_tokens"][bad[:3]], ref["out_tokens"][bad[:3]],
-                           got["row_status"][bad[:3]], ref["row_status"][bad[:3]])
-    return int((~same).sum()), ref
+    from parity import compare
+
+    if onehot:
+        w = W.Workload(w.name, w.dtype, w.logits, None, w.x, w.u, w.T)
+    tk = np.asarray(top_k, np.int32)
+    tp = np.asarray(top_p, np.float32)
+
+    def rows(sl, u):
+        return oracle.verify_warped(w.logits[sl], None if w.q is None else w.q[sl], w.x[sl], u, w.T[sl], tk[sl],
+                                    tp[sl])
+
+    ref = rows(slice(None), w.u)
+    stats = compare(w, got, ref, oracle_rows=rows)
+    return stats["mismatched"], ref
 
 
 @pytest.mark.parametrize("B,k,V,dtype,K,p", [(64, 5, 128256, "bf16", 50, 0.9), (16, 4, 32000, "bf16", 20, 1.0),
