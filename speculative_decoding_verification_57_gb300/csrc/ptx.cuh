@@ -51,6 +51,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t phase) {
     return ok != 0;
 }
 
+// try_wait with an explicit bound on how long the thread may be suspended
+// (nanoseconds) before it polls again.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t phase, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(phase), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Non-blocking tests of a phase (mbarrier.test_wait never suspends the
 // thread, unlike try_wait): for a loop that polls several things in turn.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t phase) {
@@ -78,14 +92,6 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t ph
         : "r"(bar), "r"(phase)
         : "memory");
     return ok != 0;
-}
-
-// Arrival on an mbarrier of any CTA of the cluster (`bar` is a
-// shared::cluster address, e.g. from map_rank), with release at cluster
-// scope: the caller's earlier stores into that CTA are visible to whoever
-// observes the phase complete with an acquire at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 // Nanoseconds of the global timer.
@@ -187,6 +193,17 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 // it after the next cluster barrier); they do not wait for a reply.
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// A 16-byte store into the shared memory of a CTA of the cluster whose
+// completion is counted, in bytes, on an mbarrier of that CTA (both
+// addresses shared::cluster): the sender does not wait for it, and a thread
+// that sees the barrier's phase complete sees the data.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+                 "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
                  : "memory");
 }
 

@@ -58,6 +58,7 @@ constexpr int kMaxP2Tiles = kMaxSlice / kP2Elems;
 constexpr float kLargeP = 1e-5f;   // pass-2 entries with p above this take the exact e (exp2dd or the bf16 table)
 constexpr uint32_t kWaitPolls = 1u << 22;
 constexpr int kLook = 1;           // pass 1 reads at most this many positions past the first undecided one
+constexpr uint32_t kNapNs = 1000;  // longest sleep of a producer loop that found nothing to do
 constexpr float kLog2e = 1.44269504088896341f;
 
 enum : int {
@@ -140,8 +141,8 @@ struct alignas(16) ClusterSmem {
     alignas(16) uint32_t lpad[4];  // one masked piece of logits (-inf)
     alignas(16) float qpad[4];     // and of q (zero)
     int xs[kMaxK + 1];          // draft tokens, for whoever writes the outputs
-    unsigned long long pbar[kMaxK + 1];  // position i: one arrival per cluster CTA once its partial is pushed here
-    int pcnt[kMaxK + 1];        // position i: consumer warps of this CTA that have reported it
+    unsigned long long pbar[kMaxK + 1];  // position i: complete once every cluster CTA's partial has landed here
+    unsigned long long cbar[kMaxK + 1];  // position i: complete once this CTA's four consumer warps have reported it
     float posM[kMaxK + 1];      // merged per position: maximum, sum of exponentials (sampled),
     float posS[kMaxK + 1];
     int posA[kMaxK + 1];        // argmax (greedy), partial flags,
@@ -521,10 +522,11 @@ __device__ __forceinline__ void p1_fold_tile(const uint4 (&w)[4], bool greedy, f
             lmax = max_nan_f32(bf16_lo(mx), bf16_hi(mx));
             if (lmax != lmax) nan_seen = true;
         } else {
-            uint32_t mx = 0xff80ff80u;
+            uint32_t mr[kPer];  // a tree: each chunk's maximum, then theirs
 #pragma unroll
-            for (int r = 0; r < kPer; ++r)
-                mx = max_bf16x2(max_bf16x2(mx, w[r].x), max_bf16x2(w[r].y, max_bf16x2(w[r].z, w[r].w)));
+            for (int r = 0; r < kPer; ++r) mr[r] = max_bf16x2(max_bf16x2(w[r].x, w[r].y), max_bf16x2(w[r].z, w[r].w));
+            // (with -inf: a tile of NaN alone yields -inf, and the NaN search below)
+            const uint32_t mx = max_bf16x2(max_bf16x2(max_bf16x2(mr[0], mr[1]), max_bf16x2(mr[2], mr[3])), 0xff80ff80u);
             lmax = fmaxf(bf16_lo(mx), bf16_hi(mx));
         }
     } else {
@@ -623,17 +625,18 @@ __device__ __forceinline__ void p1_fold_tile(const uint4 (&w)[4], bool greedy, f
         const float rr = m * c;
         const float err = fmaf(m, c, -rr);
         const f2 cc = pack2(c, c), nr = pack2(-rr, -rr);
-        f2 acc = pack2(0.0f, 0.0f);
+        f2 acc[kPer];  // one sum per chunk: four short chains instead of one long one
 #pragma unroll
         for (int r = 0; r < kPer; ++r) {
             const uint32_t ws[4] = {w[r].x, w[r].y, w[r].z, w[r].w};
+            acc[r] = pack2(0.0f, 0.0f);
             if (BF16) {
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4) {
                     const f2 d = fma2(pack2(bf16_lo(ws[q4]), bf16_hi(ws[q4])), cc, nr);
                     float d0, d1;
                     unpack2(d, d0, d1);
-                    acc = add2(acc, pack2(ex2(d0), ex2(d1)));
+                    acc[r] = add2(acc[r], pack2(ex2(d0), ex2(d1)));
                 }
             } else {
 #pragma unroll
@@ -641,12 +644,12 @@ __device__ __forceinline__ void p1_fold_tile(const uint4 (&w)[4], bool greedy, f
                     const f2 d = fma2(pack2(__uint_as_float(ws[q4]), __uint_as_float(ws[q4 + 1])), cc, nr);
                     float d0, d1;
                     unpack2(d, d0, d1);
-                    acc = add2(acc, pack2(ex2(d0), ex2(d1)));
+                    acc[r] = add2(acc[r], pack2(ex2(d0), ex2(d1)));
                 }
             }
         }
         float a0, a1;
-        unpack2(acc, a0, a1);
+        unpack2(add2(add2(acc[0], acc[1]), add2(acc[2], acc[3])), a0, a1);
         s += (a0 + a1) * fmaf(-err, kLn2, 1.0f);  // back to the scale of m
     }
 }
@@ -690,7 +693,6 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         sh.lpad[tid] = BF16 ? 0xff80ff80u : 0xff800000u;
         sh.qpad[tid] = 0.0f;
     }
-    if (tid <= kMaxK) sh.pcnt[tid] = 0;
     if (tid == 32 && !greedy && t_ok) {  // log2(e) / T as a pair, for the exact exponentials
         const df c2 = log2e_over(T);
         sh.c_hi = c2.hi;
@@ -713,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     int c_slot = 0, c_phase = 0;  // the consumers' stage and its phase
     if (producer && lane == 0) {
         // the producer sets up the ring, the position barriers and the slice
-        // geometry, and starts the first copies before the block's first barrier
+        // geometry
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(&sh.full[s]), 1);
             mbar_init(smem_u32(&sh.empty[s]), kConsumerWarps);
@@ -722,12 +724,18 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             mbar_init(smem_u32(&sh.full2[s]), 1);
             mbar_init(smem_u32(&sh.empty2[s]), 1);
         }
-        for (int i = 0; i <= k; ++i) mbar_init(smem_u32(&sh.pbar[i]), C);  // one arrival per CTA of the cluster
+        for (int i = 0; i <= k; ++i) {
+            mbar_init(smem_u32(&sh.pbar[i]), 1);
+            mbar_init(smem_u32(&sh.cbar[i]), kConsumerWarps);
+        }
         sh.timeout = 0;
         sh.p1_end = 0x7fffffff;
         sh.stop_pos = -1;
         fence_mbar_init();
         fence_proxy_async_smem();
+        // position i is complete once every CTA of the cluster has stored its
+        // 16-byte partial here
+        for (int i = 0; i <= k; ++i) mbar_arrive_expect_tx(smem_u32(&sh.pbar[i]), C * sizeof(Partial));
         int acc = 0;
         for (int i = 0; i <= k; ++i) {
             const long long e0 = (static_cast<long long>(b) * (k + 1) + i) * V + v0;
@@ -741,10 +749,13 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
             acc += (nb + kTileBytes - 1) / kTileBytes;
         }
         sh.tstart[k + 1] = acc;
-        if (t_ok) {
-            const int lim = early ? sh.tstart[min(k, kLook) + 1] : acc;  // the first positions the rule may need
-            for (; it_prod < min(kStages, lim); ++it_prod) issue_p1(it_prod, it_prod);
-        }
+    }
+    if (producer) {
+        // the first copies, one a lane, before the block's first barrier
+        __syncwarp();
+        const int lim = t_ok ? (early ? sh.tstart[min(k, kLook) + 1] : sh.tstart[k + 1]) : 0;  // positions the rule may need
+        it_prod = min(kStages, lim);
+        if (lane < it_prod) issue_p1(lane, lane);
     }
     __syncthreads();
     // Every CTA's position barriers are initialised before any CTA arrives on
@@ -782,11 +793,12 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 }
             }
         }
-        it_prod = __shfl_sync(full, it_prod, 0);
         int ipos = 0;  // the position of tile it_prod
         while (ipos <= k && sh.tstart[ipos + 1] <= it_prod) ++ipos;
         const int ndec = t_ok ? k + 1 : 0;
         int dpos = 0;  // positions decided so far
+        int ppos = 0;  // positions of this CTA pushed to the cluster
+        cluster_wait();  // the peers' position barriers are set up: pushes may start
         uint32_t idle = 0;
         unsigned long long t0 = 0;
         bool gave_up = false;
@@ -798,17 +810,65 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         while (dpos < ndec && (stop < 0 || !early)) {
             bool progress = false;
             if (it_prod < total1 && (!early || ipos <= dpos + kLook) && !*reinterpret_cast<volatile int*>(&sh.timeout)) {
-                int room = 1;
-                if (lane == 0 && it_prod >= kStages)
-                    room = mbar_test_wait(smem_u32(&sh.empty[it_prod % kStages]), ((it_prod / kStages) & 1) ^ 1);
-                if (__shfl_sync(full, room, 0)) {
-                    if (lane == 0) issue_p1(it_prod, it_prod);
-                    ++it_prod;
+                // lane l looks at tile it_prod + l; the leading run of tiles that
+                // may be read and whose slots are free is issued at once
+                const int tt = it_prod + lane;
+                bool ok = lane < kStages && tt < total1;
+                if (ok && early) {
+                    int p = ipos;
+                    while (p <= k && sh.tstart[p + 1] <= tt) ++p;
+                    ok = p <= dpos + kLook;
+                }
+                if (ok && tt >= kStages) ok = mbar_test_wait(smem_u32(&sh.empty[tt % kStages]), ((tt / kStages) & 1) ^ 1);
+                const int nn = __ffs(~__ballot_sync(full, ok)) - 1;
+                if (lane < nn) issue_p1(tt, tt);
+                if (nn > 0) {
+                    it_prod += nn;
                     while (ipos <= k && sh.tstart[ipos + 1] <= it_prod) ++ipos;
                     progress = true;
                 }
             }
-            if (__all_sync(full, mbar_test_wait_cluster(smem_u32(&sh.pbar[dpos]), 0))) {
+            if (ppos < ndec && __all_sync(full, mbar_test_wait(smem_u32(&sh.cbar[ppos]), 0))) {
+                // the CTA's four consumer warps have folded position ppos:
+                // merge their partials and push the CTA's into every CTA
+                const volatile Partial* wp = wpart + ppos * kConsumerWarps;
+                Partial q{-INFINITY, 0.0f, 0x7fffffff, 0};
+                if (lane < kConsumerWarps) {
+                    q.m = wp[lane].m;
+                    q.s = wp[lane].s;
+                    q.arg = wp[lane].arg;
+                    q.flags = wp[lane].flags;
+                }
+                const int F = static_cast<int>(__reduce_or_sync(full, static_cast<unsigned>(q.flags)));
+                float M, S = 0.0f;
+                int A = 0x7fffffff;
+                if (greedy) {
+                    float mv = q.m;
+                    int ar = q.arg;
+                    for (int off = 2; off > 0; off >>= 1) {
+                        const float m2 = __shfl_xor_sync(full, mv, off);
+                        const int a2 = __shfl_xor_sync(full, ar, off);
+                        merge_arg(mv, ar, m2, a2);
+                    }
+                    M = __shfl_sync(full, mv, 0);
+                    A = __shfl_sync(full, ar, 0);
+                } else {
+                    M = warp_max_f32(q.m);
+                    float tt = ms_term(q.m, q.s, M, c);
+                    for (int off = 2; off > 0; off >>= 1) tt += __shfl_xor_sync(full, tt, off);
+                    S = __shfl_sync(full, tt, 0);  // lanes 0..3 hold the sum
+                }
+                if (lane < static_cast<int>(C))
+                    st_async_v4(map_rank(smem_u32(&allpart[ppos * C + rank]), lane), __float_as_uint(M),
+                                __float_as_uint(S), static_cast<uint32_t>(A), static_cast<uint32_t>(F),
+                                map_rank(smem_u32(&sh.pbar[ppos]), lane));
+                ++ppos;
+                progress = true;
+            }
+            // (a plain test first: the cluster-scope acquire is taken only once
+            // the phase is seen complete)
+            if (__all_sync(full, mbar_test_wait(smem_u32(&sh.pbar[dpos]), 0)) &&
+                __all_sync(full, mbar_test_wait_cluster(smem_u32(&sh.pbar[dpos]), 0))) {
                 // position i: merge the C partials (lane r holds CTA r's), then its test
                 const int i = dpos;
                 const Partial pr = lane < static_cast<int>(C) ? allpart[i * C + lane]
@@ -928,61 +988,23 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         cluster_wait();
     } else {
         int t = 0;
-        bool waited = false;  // this warp has waited on the cluster barrier above
         bool bail = false;    // a wait gave up
         int reported = 0;     // positions this warp has reported
-        // Report this warp's partial of position i; the CTA's last warp to
-        // report it merges the four and pushes the CTA's partial into every
-        // CTA of the cluster, then arrives on their barriers of position i.
+        // Report this warp's partial of position i to the producer warp, which
+        // merges the CTA's four and pushes the result to the cluster.
         auto report = [&](int i, Partial P) {
-            int last = 0;
             if (lane == 0) {
                 wpart[i * kConsumerWarps + warp] = P;
-                __threadfence_block();
-                last = atomicAdd(&sh.pcnt[i], 1) == kConsumerWarps - 1;
+                mbar_arrive(smem_u32(&sh.cbar[i]));  // release: the store above is seen with the phase
             }
-            if (!__shfl_sync(full, last, 0)) return;
-            __threadfence_block();
-            const volatile Partial* wp = wpart + i * kConsumerWarps;
-            Partial q{-INFINITY, 0.0f, 0x7fffffff, 0};
-            if (lane < kConsumerWarps) {
-                q.m = wp[lane].m;
-                q.s = wp[lane].s;
-                q.arg = wp[lane].arg;
-                q.flags = wp[lane].flags;
-            }
-            const int F = static_cast<int>(__reduce_or_sync(full, static_cast<unsigned>(q.flags)));
-            float M, S = 0.0f;
-            int A = 0x7fffffff;
-            if (greedy) {
-                float mv = q.m;
-                int ar = q.arg;
-                for (int off = 2; off > 0; off >>= 1) {
-                    const float m2 = __shfl_xor_sync(full, mv, off);
-                    const int a2 = __shfl_xor_sync(full, ar, off);
-                    merge_arg(mv, ar, m2, a2);
-                }
-                M = __shfl_sync(full, mv, 0);
-                A = __shfl_sync(full, ar, 0);
-            } else {
-                M = warp_max_f32(q.m);
-                float tt = ms_term(q.m, q.s, M, c);
-                for (int off = 2; off > 0; off >>= 1) tt += __shfl_xor_sync(full, tt, off);
-                S = __shfl_sync(full, tt, 0);  // lanes 0..3 hold the sum
-            }
-            if (!waited) {
-                cluster_wait();
-                waited = true;
-            }
-            if (lane < static_cast<int>(C)) {
-                st_cluster_v4(map_rank(smem_u32(&allpart[i * C + rank]), lane), __float_as_uint(M), __float_as_uint(S),
-                              static_cast<uint32_t>(A), static_cast<uint32_t>(F));
-                mbar_arrive_cluster(map_rank(smem_u32(&sh.pbar[i]), lane));
-            }
+            __syncwarp();
         };
+        // the first stopping position, once the producer has decided it (-1
+        // before); the same value in every lane
+        auto stop_now = [&]() { return __shfl_sync(full, *reinterpret_cast<volatile int*>(&sh.stop_pos), 0); };
         for (int i = 0; i <= k && t_ok; ++i) {
-            const int sp = *reinterpret_cast<volatile int*>(&sh.stop_pos);
-            const bool skip = early && sp >= 0 && i > sp;  // past the stop: copies landed are let go unread
+            const int sp = stop_now();
+            bool skip = early && sp >= 0 && i > sp;  // past the stop: copies landed are let go unread
             float m = -INFINITY, s = 0.0f;  // sampled state
             int arg = 0x7fffffff;           // greedy state (m holds the best value)
             bool nan_seen = false;
@@ -1048,6 +1070,10 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 const int bytes = min(kTileBytes, sh.nbytes[i] - lt * kTileBytes);
                 const int nch = bytes >> 4;
                 const uint32_t tile = smem_u32(ring + c_slot * kTileBytes);
+                if (early && !skip) {
+                    const int sp2 = stop_now();
+                    skip = sp2 >= 0 && i > sp2;
+                }
                 if (skip) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&sh.empty[c_slot]));
@@ -1106,7 +1132,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         // reported as timed out, so that no CTA of the cluster waits for them
         if (bail)
             for (int i = reported; i <= k; ++i) report(i, Partial{-INFINITY, 0.0f, 0x7fffffff, 2});
-        if (!waited) cluster_wait();
+        cluster_wait();
     }
     __syncthreads();  // pass 1 is over: no stage is read any more
     if (sh.timeout != 0 && producer && lane == 0) {
@@ -1281,30 +1307,57 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         df te = df_make(0.0f);  // this thread's sum of e (residual mode)
         bool qbad = false;
         if (producer) {
-            if (p2fast && lane == 0) {
+            if (p2fast) {
                 // the ring's last generic-proxy reads (pass 1) are ordered
                 // before these async-proxy writes by the block barrier above
                 fence_proxy_async_smem();
-                int slot = g2 % S2, phase = (g2 / S2) & 1;  // tile g: slot g % S2, phase (g / S2) & 1
-                for (int t2 = 0; t2 < ntiles2; ++t2) {
-                    const int g = g2 + t2;
-                    if (sh.timeout ||
-                        (g >= S2 && !mbar_wait_bounded(smem_u32(&sh.empty2[slot]), phase ^ 1, polls))) {
-                        atomicOr(&sh.timeout, 1);
-                        break;
+                // Lane l looks at tile t2 + l (tile g = g2 + t2 + l: slot g % S2,
+                // phase (g / S2) & 1); the leading run of tiles whose slots are
+                // free is issued at once, one tile a lane: a lane waits about as
+                // long to issue one bulk copy as to issue several in one step.
+                uint32_t idle2 = 0;
+                unsigned long long w0 = 0;
+                for (int t2 = 0; t2 < ntiles2;) {
+                    if (*reinterpret_cast<volatile int*>(&sh.timeout)) break;
+                    const int tt = t2 + lane;
+                    const int g = g2 + tt;
+                    const bool ok = lane < S2 && tt < ntiles2 &&
+                                    (g < S2 || mbar_test_wait(smem_u32(&sh.empty2[g % S2]), ((g / S2) & 1) ^ 1));
+                    const int nn = __ffs(~__ballot_sync(full, ok)) - 1;
+                    if (lane < nn) {
+                        const int slot = g % S2;
+                        const int e0 = tt * kP2Elems;
+                        const int cnt = min(kP2Elems, n - e0);
+                        const uint32_t bar = smem_u32(&sh.full2[slot]);
+                        const uint32_t dst = smem_u32(ring + slot * stride2);
+                        const uint32_t lbytes = static_cast<uint32_t>(cnt * esz);
+                        const uint32_t qbytes = mode == MODE_RESIDUAL ? static_cast<uint32_t>(cnt * 4) : 0u;
+                        mbar_arrive_expect_tx(bar, lbytes + qbytes);
+                        bulk_g2s(dst + loff2, lg + (lrow + v0 + e0) * esz, lbytes, bar);
+                        if (qbytes) bulk_g2s(dst, qrow + v0 + e0, qbytes, bar);
                     }
-                    const int e0 = t2 * kP2Elems;
-                    const int cnt = min(kP2Elems, n - e0);
-                    const uint32_t bar = smem_u32(&sh.full2[slot]);
-                    const uint32_t dst = smem_u32(ring + slot * stride2);
-                    const uint32_t lbytes = static_cast<uint32_t>(cnt * esz);
-                    const uint32_t qbytes = mode == MODE_RESIDUAL ? static_cast<uint32_t>(cnt * 4) : 0u;
-                    mbar_arrive_expect_tx(bar, lbytes + qbytes);
-                    bulk_g2s(dst + loff2, lg + (lrow + v0 + e0) * esz, lbytes, bar);
-                    if (qbytes) bulk_g2s(dst, qrow + v0 + e0, qbytes, bar);
-                    if (++slot == S2) {
-                        slot = 0;
-                        phase ^= 1;
+                    t2 += nn;
+                    if (nn > 0) {
+                        idle2 = 0;
+                        w0 = 0;
+                        continue;
+                    }
+                    if (lane == 0) {  // sleep until the next tile's slot is free (briefly)
+                        const int g = g2 + t2;
+                        mbar_try_wait_hint(smem_u32(&sh.empty2[g % S2]), ((g / S2) & 1) ^ 1, kNapNs);
+                    }
+                    __syncwarp();
+                    bool give = ++idle2 >= kWaitPolls;
+                    if ((idle2 & 255) == 255) {
+                        const unsigned long long tn = gtimer();
+                        if (w0 == 0)
+                            w0 = tn;
+                        else if (tn - w0 > kWaitNs)
+                            give = true;
+                    }
+                    if (__any_sync(full, give)) {
+                        if (lane == 0) atomicOr(&sh.timeout, 1);
+                        break;
                     }
                 }
             }
@@ -1328,7 +1381,7 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 bool ok = true;
                 if (p2fast) {
                     ok = __all_sync(0xffffffffu, !sh.timeout &&
-                                                     mbar_wait_bounded(smem_u32(&sh.full2[my_slot]), my_phase, polls));
+                                                     mbar_wait_bounded(smem_u32(&sh.full2[my_slot]), my_phase, kWaitPolls));
                     if (!ok && lane == 0) atomicOr(&sh.timeout, 1);
                 } else {
                     // unaligned rows: the warp stages its own tiles in slot
