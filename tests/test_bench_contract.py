@@ -36,6 +36,29 @@ def test_reference_arm_prints_one_contract_line():
     assert "workload" in d["config"]
 
 
+def test_every_workload_is_a_bench_option_and_reference_arm_covers_it():
+    """--workload takes each named workload; the reference arm's steps use
+    that workload's rows (all of them when they fit the time budget)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from speculative_decoding_verification_57_gb300 import workloads as W
+
+    assert set(bench.WORKLOADS_DESC) == set(W.WORKLOADS)
+    for name in W.WORKLOADS:
+        assert bench.parse_args(["--workload", name]).workload == name
+    assert bench.parse_args([]).workload == "benchmark"
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    for name in ("toy", "zipf"):
+        out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", name,
+                              "--steps", "3", "--warmup", "1"], capture_output=True, text=True, cwd=ROOT, env=env,
+                             timeout=600)
+        assert out.returncode == 0, out.stderr[-2000:]
+        d = json.loads([l for l in out.stdout.splitlines() if l.startswith("{")][0])
+        w = W.make_workload(name)
+        assert (d["config"]["B"], d["config"]["k"], d["config"]["V"]) == (w.B, w.k, w.V)
+        assert d["config"]["rows_per_step"] == w.B
+
+
 def test_profile_hash_ignores_comments():
     """A committed profile stays valid across comment edits, not code edits."""
     sys.path.insert(0, ROOT)
