@@ -68,7 +68,7 @@ struct DeviceGuard {
 
 
 struct Plan {
-    bool warp = false;
+    bool warp = false;  // V <= kWarpKernelMaxV: one warp per row
     int cluster = 1;
     int slice = 0;
 };

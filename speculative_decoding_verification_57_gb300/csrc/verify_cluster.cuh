@@ -57,7 +57,7 @@ constexpr int kP2Elems = kLaneEntries * 32;  // pass-2 tile: 1024 entries, one w
 constexpr int kMaxP2Tiles = kMaxSlice / kP2Elems;
 constexpr float kLargeP = 1e-5f;   // pass-2 entries with p above this take the exact e (exp2dd or the bf16 table)
 constexpr uint32_t kWaitPolls = 1u << 22;
-constexpr int kLook = 1;           // pass 1 reads at most this many positions past the first undecided one
+constexpr int kLookTiles = 5;      // pass 1 reads at most this many tiles past the first undecided position
 constexpr uint32_t kNapNs = 1000;  // longest sleep of a producer loop that found nothing to do
 constexpr float kLog2e = 1.44269504088896341f;
 
@@ -753,7 +753,8 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
     if (producer) {
         // the first copies, one a lane, before the block's first barrier
         __syncwarp();
-        const int lim = t_ok ? (early ? sh.tstart[min(k, kLook) + 1] : sh.tstart[k + 1]) : 0;  // positions the rule may need
+        // the tiles the rule may need: position 0's and kLookTiles more
+        const int lim = t_ok ? (early ? min(sh.tstart[k + 1], sh.tstart[1] + kLookTiles) : sh.tstart[k + 1]) : 0;
         it_prod = min(kStages, lim);
         if (lane < it_prod) issue_p1(lane, lane);
     }
@@ -793,8 +794,6 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
                 }
             }
         }
-        int ipos = 0;  // the position of tile it_prod
-        while (ipos <= k && sh.tstart[ipos + 1] <= it_prod) ++ipos;
         const int ndec = t_ok ? k + 1 : 0;
         int dpos = 0;  // positions decided so far
         int ppos = 0;  // positions of this CTA pushed to the cluster
@@ -802,29 +801,25 @@ __global__ void __launch_bounds__(kThreads, 4) verify_cluster_kernel(const Verif
         uint32_t idle = 0;
         unsigned long long t0 = 0;
         bool gave_up = false;
-        // One loop issues the tiles (lane 0) and takes the decisions (the
+        // One loop issues the tiles (lanes 0..4) and takes the decisions (the
         // whole warp), in position order, as the CTAs' partials come in.  A
-        // tile is issued only when its position is at most kLook beyond the
-        // first undecided one, so that at most kLook positions past the stop
-        // are read.
+        // tile is issued only while it lies at most kLookTiles past the last
+        // tile of the first undecided position, so that little is read past
+        // the stop (about one position of the benchmark's slices; several
+        // when a position's slice is a single tile).
         while (dpos < ndec && (stop < 0 || !early)) {
             bool progress = false;
-            if (it_prod < total1 && (!early || ipos <= dpos + kLook) && !*reinterpret_cast<volatile int*>(&sh.timeout)) {
+            const int lim_t = early ? min(total1, sh.tstart[dpos + 1] + kLookTiles) : total1;
+            if (it_prod < lim_t && !*reinterpret_cast<volatile int*>(&sh.timeout)) {
                 // lane l looks at tile it_prod + l; the leading run of tiles that
                 // may be read and whose slots are free is issued at once
                 const int tt = it_prod + lane;
-                bool ok = lane < kStages && tt < total1;
-                if (ok && early) {
-                    int p = ipos;
-                    while (p <= k && sh.tstart[p + 1] <= tt) ++p;
-                    ok = p <= dpos + kLook;
-                }
+                bool ok = lane < kStages && tt < lim_t;
                 if (ok && tt >= kStages) ok = mbar_test_wait(smem_u32(&sh.empty[tt % kStages]), ((tt / kStages) & 1) ^ 1);
                 const int nn = __ffs(~__ballot_sync(full, ok)) - 1;
                 if (lane < nn) issue_p1(tt, tt);
                 if (nn > 0) {
                     it_prod += nn;
-                    while (ipos <= k && sh.tstart[ipos + 1] <= it_prod) ++ipos;
                     progress = true;
                 }
             }

@@ -1,8 +1,16 @@
 // verify_warp.cuh -- verify kernel for small vocabularies: one warp per
-// sequence, lanes striding over V.  Same rule, same status bits and same
-// inverse-CDF convention as the split-vocabulary kernel; here the whole stop
-// row is weighted with the double-float exponential and summed as float pairs,
-// which costs little at small V.
+// sequence.  Same rule, same status bits and same inverse-CDF convention as
+// the split-vocabulary kernel.
+//
+// Pass 1 reads each position's logits with 16-byte loads (lane l takes
+// chunks l, l + 32, ...; an unaligned head and tail take scalar loads) and
+// folds each chunk into an online (max, sum of exponentials), or (max,
+// lowest argmax) for greedy rows.  Pass 2 evaluates the exact e of every
+// entry of the stop row once (the double-float exponential, cheap at small
+// V) into shared memory, recomputes the normaliser from them, turns them into
+// weights, and draws the token with a warp scan: each lane sums a contiguous
+// chunk of entries, an inclusive scan over the lanes finds the chunk holding
+// u * W, and that lane walks its chunk.
 #pragma once
 #include <cfloat>
 #include <cstdint>
@@ -14,18 +22,90 @@
 namespace specv {
 
 constexpr int kWarpKernelMaxV = 2048;
-constexpr int kWarpsPerBlock = 4;
+constexpr int kWarpsPerBlock = 2;  // each warp keeps its stop row's weights (16 KB at most) in shared memory
+
+// Fold one value into the online (max, sum) or (max, argmax) state.
+__device__ __forceinline__ void warp_fold1(bool greedy, float l, int v, float c, float& m, float& s, int& arg,
+                                           bool& nan_seen) {
+    if (greedy) {
+        if (l != l) nan_seen = true;
+        if (l > m) {
+            m = l;
+            arg = v;
+        }
+    } else {
+        online_add(m, s, l, c);
+    }
+}
+
+// One row of V logits starting at element row_e0: this lane's share of its
+// (max, sum of exp((l - max) c)) or (max, lowest argmax), before the warp
+// reduction.  The values of a 16-byte chunk are folded together: the chunk's
+// maximum first, then every value's exponential at the (possibly raised)
+// running maximum -- the same arithmetic as one value at a time, in another
+// order, and the same outcome for NaN and infinite logits.
+template <bool BF16>
+__device__ __forceinline__ void warp_row_fold(const void* logits, long long row_e0, int V, bool greedy, float c,
+                                              int lane, float& m, float& s, int& arg, bool& nan_seen) {
+    constexpr int esz = BF16 ? 2 : 4;
+    constexpr int vw = 16 / esz;  // values per 16-byte chunk
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(logits) + row_e0 * esz;
+    const int h = min(V, static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(p) & 15)) & 15) / esz));
+    const int nch = (V - h) / vw;
+    const int tail0 = h + nch * vw;
+    if (lane < h) warp_fold1(greedy, load_logit(logits, row_e0 + lane, BF16), lane, c, m, s, arg, nan_seen);
+    const uint4* cp = reinterpret_cast<const uint4*>(p + h * esz);
+    for (int ch = lane; ch < nch; ch += 32) {
+        const uint4 w = __ldg(cp + ch);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        float f[vw];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (BF16) {
+                f[2 * t] = bf16_lo(ws[t]);
+                f[2 * t + 1] = bf16_hi(ws[t]);
+            } else {
+                f[t] = __uint_as_float(ws[t]);
+            }
+        }
+        const int v0 = h + ch * vw;
+        if (greedy) {
+#pragma unroll
+            for (int t = 0; t < vw; ++t) warp_fold1(true, f[t], v0 + t, c, m, s, arg, nan_seen);
+        } else {
+            float cm = f[0];
+#pragma unroll
+            for (int t = 1; t < vw; ++t) cm = fmaxf(cm, f[t]);
+            if (cm > m) {
+                s = (m == -INFINITY) ? s * 0.0f : s * ex2((m - cm) * c);
+                m = cm;
+            }
+#pragma unroll
+            for (int t = 0; t < vw; ++t)
+                if (m != -INFINITY || f[t] != f[t]) s += ex2((f[t] - m) * c);
+        }
+    }
+    if (lane < V - tail0)
+        warp_fold1(greedy, load_logit(logits, row_e0 + tail0 + lane, BF16), tail0 + lane, c, m, s, arg, nan_seen);
+}
 
 template <bool BF16>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const VerifyArgs a) {
     __shared__ float2 tab[128];
+    // the stop row's e, then its weights (pairs); entry v at v + v / 32, so
+    // that lanes walking contiguous chunks fall in different banks
+    __shared__ float2 wbuf[kWarpsPerBlock][kWarpKernelMaxV + kWarpKernelMaxV / 32];
     for (int i = threadIdx.x; i < 128; i += blockDim.x) tab[i] = g_exp2_table[i];
     __syncthreads();
+    const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+    const int wib = threadIdx.x >> 5;
+    const int b = blockIdx.x * kWarpsPerBlock + wib;
     if (b >= a.B) return;
+    float2* wbase = wbuf[wib];
+    auto wv = [&](int v) -> float2& { return wbase[v + (v >> 5)]; };
     const int k = a.k;
-    const long long V = a.V;
+    const int V = static_cast<int>(a.V);
     const float T = a.temp ? __ldg(a.temp + b) : 0.0f;
     const bool greedy = (T == 0.0f);
     const bool t_ok = greedy || (T >= FLT_MIN && T <= FLT_MAX);
@@ -44,35 +124,25 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
             u1 = __ldg(a.u + (static_cast<long long>(b) * (k + 1) + lane) * 2 + 1);
         }
     }
-    // pass 1: per position, lanes stride over the vocabulary
+    // pass 1: per position, lanes over 16-byte chunks, then the warp reduction
     for (int i = 0; i <= k && t_ok; ++i) {
         float m = -INFINITY, s = 0.0f;
         int arg = 0x7fffffff;
         bool nan_seen = false;
-        for (long long v = lane; v < V; v += 32) {
-            const float l = load_logit(a.logits, base + i * V + v, BF16);
-            if (greedy) {
-                if (l != l) nan_seen = true;
-                if (l > m) {
-                    m = l;
-                    arg = static_cast<int>(v);
-                }
-            } else {
-                online_add(m, s, l, c);
-            }
-        }
+        warp_row_fold<BF16>(a.logits, base + static_cast<long long>(i) * V, V, greedy, c, lane, m, s, arg, nan_seen);
+        __syncwarp();
         if (greedy) {
             for (int off = 16; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                const int a2 = __shfl_xor_sync(0xffffffffu, arg, off);
+                const float m2 = __shfl_xor_sync(full, m, off);
+                const int a2 = __shfl_xor_sync(full, arg, off);
                 merge_arg(m, arg, m2, a2);
             }
-            nan_seen = __any_sync(0xffffffffu, nan_seen);
+            nan_seen = __any_sync(full, nan_seen);
             if (arg == 0x7fffffff) arg = 0;
         } else {
             for (int off = 16; off > 0; off >>= 1) {
-                const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-                const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+                const float m2 = __shfl_xor_sync(full, m, off);
+                const float s2 = __shfl_xor_sync(full, s, off);
                 merge_ms(m, s, m2, s2, c);
             }
         }
@@ -108,7 +178,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
                     if (!(qx >= 0.0f && qx <= FLT_MAX)) err |= ST_QBAD;
                 }
                 if (!err) {
-                    const float Lx = load_logit(a.logits, base + lane * V + xi, BF16);
+                    const float Lx = load_logit(a.logits, base + static_cast<long long>(lane) * V + xi, BF16);
                     RowConst rc;
                     rc.M = Mi;
                     rc.s1 = Si;
@@ -127,13 +197,13 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
         }
     }
     __syncwarp();
-    const unsigned mask = __ballot_sync(0xffffffffu, lane <= k && stop);
+    const unsigned mask = __ballot_sync(full, lane <= k && stop);
     const int j = t_ok ? __ffs(mask) - 1 : 0;
-    int st = t_ok ? __shfl_sync(0xffffffffu, err, j) : ST_TEMP;
-    const float uj = __shfl_sync(0xffffffffu, u1, j);
+    int st = t_ok ? __shfl_sync(full, err, j) : ST_TEMP;
+    const float uj = __shfl_sync(full, u1, j);
     if (t_ok && !greedy && !(st & ST_ERRMASK) && !(uj >= 0.0f && uj < 1.0f)) st |= ST_UNIFORM;
-    const float Mj = __shfl_sync(0xffffffffu, Mi, j);
-    const int Aj = __shfl_sync(0xffffffffu, Ai, j);
+    const float Mj = __shfl_sync(full, Mi, j);
+    const int Aj = __shfl_sync(full, Ai, j);
 
     if (lane <= k && t_ok) {
         if (a.dbg_max) a.dbg_max[static_cast<long long>(b) * (k + 1) + lane] = Mi;
@@ -150,70 +220,102 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
     const bool bad = (st & ST_ERRMASK) != 0;
     if (!bad && greedy) token = Aj;
     if (!bad && !greedy) {
-        // pass 2 on row j: every entry with exp2dd, sums as float pairs;
-        // weights r = max(0, e - s q) (residual, s recomputed exactly), or e
-        // (bonus, or empty residual)
-        const long long row = base + j * V;
+        // pass 2 on row j: the exact e of every entry, once (the draft token's
+        // entry of a one-hot row weighs nothing); s recomputed from them
+        const long long row = base + static_cast<long long>(j) * V;
         const float* qrow = a.q ? a.q + (static_cast<long long>(b) * k + (j < k ? j : 0)) * V : nullptr;
         int mode = (j < k) ? (a.q ? MODE_RESIDUAL : MODE_ONEHOT) : MODE_BONUS;
-        const int xj = __shfl_sync(0xffffffffu, xi, j < k ? j : 0);  // one-hot drafts: left out of the residual
+        const int xj = __shfl_sync(full, xi, j < k ? j : 0);
         RowConst rc;
         rc.M = Mj;
         rc.s1 = 0.0f;
         rc.thr = 0.0f;
         rc.ch = c2.hi;
         rc.cl = c2.lo;
-        df s_prec = df_make(0.0f);
-        if (mode == MODE_RESIDUAL) {
-            for (long long v = lane; v < V; v += 32)
-                s_prec = df_sum(s_prec, exact_weight<BF16>(load_logit(a.logits, row + v, BF16), 0.0f, MODE_BONUS, rc,
-                                                           df_make(0.0f), tab));
-            s_prec = df_shfl(df_warp_total(s_prec), 0);
-        }
-        auto weight = [&](long long v) -> df {
-            const float qq = mode == MODE_RESIDUAL ? __ldg(qrow + v) : 0.0f;
-            const float l = (mode == MODE_ONEHOT && v == xj) ? -INFINITY : load_logit(a.logits, row + v, BF16);
-            return exact_weight<BF16>(l, qq, mode, rc, s_prec, tab);
+        auto exact_e = [&](int v, bool drop_draft) -> df {
+            const float l = (drop_draft && v == xj) ? -INFINITY : load_logit(a.logits, row + v, BF16);
+            return l == -INFINITY ? df_make(0.0f) : precise_e<BF16>(l, rc, tab);
         };
-        bool qbad = false;
-        df W = df_make(0.0f);
-        for (long long v = lane; v < V; v += 32) {
-            W = df_sum(W, weight(v));
-            if (mode == MODE_RESIDUAL) {
+        df se = df_make(0.0f);
+        for (int v = lane; v < V; v += 32) {
+            const df e = exact_e(v, mode == MODE_ONEHOT);
+            wv(v) = make_float2(e.hi, e.lo);
+            se = df_sum(se, e);
+        }
+        const df s_prec = df_shfl(df_warp_total(se), 0);
+        df W = s_prec;  // bonus and one-hot rows: the weights are the e
+        if (mode == MODE_RESIDUAL) {
+            // w = max(0, e - s q), the product exact through one fma
+            bool qbad = false;
+            df Wl = df_make(0.0f);
+            for (int v = lane; v < V; v += 32) {
                 const float qq = __ldg(qrow + v);
                 qbad |= !(qq >= 0.0f && qq <= FLT_MAX);
+                const float2 e2 = wv(v);
+                df r = minus_sq(df{e2.x, e2.y}, s_prec, qq);
+                if (!(r.hi + r.lo > 0.0f)) r = df_make(0.0f);
+                wv(v) = make_float2(r.hi, r.lo);
+                Wl = df_sum(Wl, r);
             }
+            W = df_shfl(df_warp_total(Wl), 0);
+            if (__any_sync(full, qbad)) st |= ST_QBAD;
         }
-        W = df_shfl(df_warp_total(W), 0);
-        if (__any_sync(0xffffffffu, qbad)) st |= ST_QBAD;
         if ((mode == MODE_RESIDUAL || mode == MODE_ONEHOT) && !(st & ST_ERRMASK)) {
-            const float Sj = __shfl_sync(0xffffffffu, Si, j);
+            const float Sj = __shfl_sync(full, Si, j);
             if (lane == 0 && a.dbg_resid)
                 a.dbg_resid[b] = df_val(W) / (mode == MODE_RESIDUAL ? df_val(s_prec) : Sj);
             if (!(W.hi + W.lo > 0.0f)) {
+                // empty residual: sample p itself, every entry
                 mode = MODE_FALLBACK;
                 st |= ST_ZERO_RESIDUAL;
-                W = df_make(0.0f);
-                for (long long v = lane; v < V; v += 32) W = df_sum(W, weight(v));
-                W = df_shfl(df_warp_total(W), 0);
+                df se2 = df_make(0.0f);
+                for (int v = lane; v < V; v += 32) {
+                    const df e = exact_e(v, false);
+                    wv(v) = make_float2(e.hi, e.lo);
+                    se2 = df_sum(se2, e);
+                }
+                W = df_shfl(df_warp_total(se2), 0);
             }
         }
+        __syncwarp();  // every lane's weights are in shared memory
         if (!(st & ST_ERRMASK)) {
+            // inverse CDF: lane l sums entries [l cs, (l + 1) cs) in order; the
+            // first lane with a positive sum whose inclusive prefix exceeds
+            // u W holds the token, which it finds by walking its entries
             const df target = df_mul_f(W, uj);
-            df acc = df_make(0.0f);
+            const int cs = (V + 31) / 32;
+            const int c0 = min(V, lane * cs), c1 = min(V, c0 + cs);
+            df lsum = df_make(0.0f);
             int lastpos = -1;
-            for (long long v0 = 0; v0 < V && token < 0; v0 += 32) {
-                const long long v = v0 + lane;
-                const df w = v < V ? weight(v) : df_make(0.0f);
-                const bool pos = w.hi + w.lo > 0.0f;
-                const df incl = df_sum(acc, df_warp_incl_scan(w, lane));
-                const unsigned posm = __ballot_sync(0xffffffffu, pos);
-                if (posm) lastpos = static_cast<int>(v0 + 31 - __clz(posm));
-                const unsigned hit = __ballot_sync(0xffffffffu, pos && df_less(target, incl));
-                if (hit) token = static_cast<int>(v0 + __ffs(hit) - 1);
-                acc = df_shfl(incl, 31);
+            for (int v = c0; v < c1; ++v) {
+                const float2 w2 = wv(v);
+                if (w2.x + w2.y > 0.0f) {
+                    lsum = df_sum(lsum, df{w2.x, w2.y});
+                    lastpos = v;
+                }
             }
-            if (token < 0) token = lastpos;
+            const df incl = df_warp_incl_scan(lsum, lane);
+            const df excl = df_shfl_up(incl, 1);
+            const bool lpos = lastpos >= 0;
+            const unsigned hit = __ballot_sync(full, lpos && df_less(target, incl));
+            if (hit) {
+                const int L = __ffs(hit) - 1;
+                if (lane == L) {
+                    df acc = lane == 0 ? df_make(0.0f) : excl;
+                    for (int v = c0; v < c1 && token < 0; ++v) {
+                        const float2 w2 = wv(v);
+                        if (w2.x + w2.y > 0.0f) {
+                            acc = df_sum(acc, df{w2.x, w2.y});
+                            if (df_less(target, acc)) token = v;
+                        }
+                    }
+                    if (token < 0) token = lastpos;  // only through rounding at the chunk's end
+                }
+                token = __shfl_sync(full, token, L);
+            } else {
+                // only through rounding at the top edge: the last positive entry
+                token = __reduce_max_sync(full, static_cast<unsigned>(lastpos + 1)) - 1;
+            }
         }
     }
     const bool bad2 = (st & ST_ERRMASK) != 0;

@@ -342,3 +342,36 @@ def test_zz_summary():
     print("parity totals", TOTALS)
     if TOTALS["rows"]:
         assert TOTALS["mismatched"] <= max(1, 1e-4 * TOTALS["rows"])
+
+
+def test_small_vocabulary_kernel(h):
+    """V <= 2048 (one warp per row) matches the oracle on odd sizes, debug
+    outputs, one-hot drafts, masked entries and unaligned rows."""
+    import torch
+
+    import speculative_decoding_verification_57_gb300 as sv
+
+    cases = [(1, 1, 3, "f32"), (7, 2, 3, "bf16"), (13, 16, 3, "bf16"), (1000, 4, 5, "f32"), (1001, 5, 3, "f32"),
+             (2047, 3, 2, "bf16"), (2048, 31, 2, "f32"), (700, 6, 9, "bf16"), (33, 8, 40, "f32")]
+    for V, k, B, dtype in cases:
+        w = W.make_random(name="small", B=B, k=k, V=V, dtype=dtype, seed=V * 7 + k, logit_sigma=2.5,
+                          draft_sigma=0.7, temperature=0.9, spike=4.0, spike_mode="position",
+                          greedy_rows=1 if B > 2 else 0)
+        for debug in (False, True):
+            _acc(compare(w, run_gpu(h, w, debug=debug), check_debug=debug))
+        w1 = W.Workload(w.name, w.dtype, w.logits, None, w.x, w.u, w.T)
+        _acc(compare(w1, run_gpu(h, w1)))
+        wm = W.make_random(name="small-masked", B=B, k=k, V=V, dtype=dtype, seed=V + 5, logit_sigma=2.0,
+                           draft_sigma=0.8, temperature=1.1)
+        mask = np.random.default_rng(V).random((B, k + 1, V)) < 0.3
+        wm.logits[mask] = W.f32_to_bf16_bits(np.array([-np.inf], np.float32))[0] if dtype == "bf16" else -np.inf
+        _acc(compare(wm, run_gpu(h, wm, debug=True), check_debug=True))
+    # rows starting one element past an aligned address: unaligned heads and tails
+    w = W.make_random(name="small-unaligned", B=4, k=3, V=1500, dtype="bf16", seed=8, logit_sigma=3.0,
+                      draft_sigma=1.0, temperature=1.0)
+    L, q, x, u, T = to_device(w, "cuda:0")
+    Lb = torch.empty(L.numel() + 1, dtype=L.dtype, device="cuda:0")
+    Lb[1:].copy_(L.reshape(-1))
+    out = sv.specv_verify_sample(h, Lb[1:].view(L.shape), q, x, u, T)
+    torch.cuda.synchronize()
+    _acc(compare(w, {kk: v.cpu().numpy() for kk, v in out.items()}))
