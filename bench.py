@@ -4,7 +4,7 @@ One step = one verify call (one batch) of a named workload; the default is
 B=64, k=5, V=128256 (Llama-3 vocabulary), bf16 target logits, T=1.  Every
 call streams its inputs from HBM: large workloads cycle through enough
 copies of their inputs to exceed twice the L2 (replayed from a CUDA graph);
-workloads too small for that have the L2 flushed (a 2x-L2 write) before
+workloads too small for that have the L2 flushed (a 2x-L2 read) before
 every call, each call timed by its own pair of CUDA events.  Prints one JSON
 line (rank 0).
 
@@ -463,18 +463,21 @@ def run_ours(args):
     launches_before = sv.specv_launch_count(h)
     sampler = ClockSampler(local)
     if flushed:
-        # each call alone: a 2x-L2 write, then the call between its own events
-        flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+        # each call alone: a 2x-L2 read (the L2 then holds clean lines of
+        # another buffer, nothing to write back), then the call between its
+        # own events
+        flush = torch.ones(2 * l2 // 4, dtype=torch.int32, device=dev)
+        flush_out = torch.empty((), dtype=torch.int64, device=dev)
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
         with torch.cuda.stream(stream):
             for i in range(max(3, args.warmup)):
-                flush.zero_()
+                torch.sum(flush, dim=0, out=flush_out)
                 torch.cuda._sleep(200_000)
                 call(i)
         stream.synchronize()
-        launch_mode = f"direct launches, L2 flushed ({2 * l2 / 1e6:.0f} MB write) before each call"
-        l2_desc = (f"L2 flushed before every call ({2 * l2 / 1e6:.0f} MB write, outside the call's event pair); "
+        launch_mode = f"direct launches, L2 flushed ({2 * l2 / 1e6:.0f} MB read) before each call"
+        l2_desc = (f"L2 flushed before every call ({2 * l2 / 1e6:.0f} MB read, outside the call's event pair); "
                    "the sum of the per-call event times is the timed total")
         if rank == 0:
             sampler.start()
@@ -484,7 +487,7 @@ def run_ours(args):
         sampler.mark("t0")
         with torch.cuda.stream(stream):
             for i in range(args.steps):
-                flush.zero_()
+                torch.sum(flush, dim=0, out=flush_out)
                 # a ~100 us device-side pause after the flush: the host has
                 # queued the call before the GPU reaches its first event
                 torch.cuda._sleep(200_000)

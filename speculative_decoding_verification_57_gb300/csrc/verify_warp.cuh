@@ -55,8 +55,21 @@ __device__ __forceinline__ void warp_row_fold(const void* logits, long long row_
     const int tail0 = h + nch * vw;
     if (lane < h) warp_fold1(greedy, load_logit(logits, row_e0 + lane, BF16), lane, c, m, s, arg, nan_seen);
     const uint4* cp = reinterpret_cast<const uint4*>(p + h * esz);
-    for (int ch = lane; ch < nch; ch += 32) {
-        const uint4 w = __ldg(cp + ch);
+    // eight chunks a lane are loaded before any is folded: eight loads in flight
+    constexpr int kU = 8;
+    for (int ch0 = lane; ch0 < nch; ch0 += 32 * kU) {
+        uint4 wq[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int ch = ch0 + 32 * u;
+            const uint32_t ninf = BF16 ? 0xff80ff80u : 0xff800000u;
+            wq[u] = ch < nch ? __ldg(cp + ch) : make_uint4(ninf, ninf, ninf, ninf);
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+        const int ch = ch0 + 32 * u;
+        if (ch >= nch) break;
+        const uint4 w = wq[u];
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
         float f[vw];
 #pragma unroll
@@ -83,6 +96,7 @@ __device__ __forceinline__ void warp_row_fold(const void* logits, long long row_
 #pragma unroll
             for (int t = 0; t < vw; ++t)
                 if (m != -INFINITY || f[t] != f[t]) s += ex2((f[t] - m) * c);
+        }
         }
     }
     if (lane < V - tail0)
@@ -236,11 +250,26 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
             const float l = (drop_draft && v == xj) ? -INFINITY : load_logit(a.logits, row + v, BF16);
             return l == -INFINITY ? df_make(0.0f) : precise_e<BF16>(l, rc, tab);
         };
+        // entries v = lane + 32 t, eight at a time: their loads are issued
+        // together, before any of them is used
+        constexpr int kB = 8;
         df se = df_make(0.0f);
-        for (int v = lane; v < V; v += 32) {
-            const df e = exact_e(v, mode == MODE_ONEHOT);
-            wv(v) = make_float2(e.hi, e.lo);
-            se = df_sum(se, e);
+        for (int v0 = lane; v0 < V; v0 += 32 * kB) {
+            float lb[kB];
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int v = v0 + 32 * u;
+                lb[u] = v < V ? load_logit(a.logits, row + v, BF16) : -INFINITY;
+            }
+#pragma unroll
+            for (int u = 0; u < kB; ++u) {
+                const int v = v0 + 32 * u;
+                if (v >= V) break;
+                const float l = (mode == MODE_ONEHOT && v == xj) ? -INFINITY : lb[u];
+                const df e = l == -INFINITY ? df_make(0.0f) : precise_e<BF16>(l, rc, tab);
+                wv(v) = make_float2(e.hi, e.lo);
+                se = df_sum(se, e);
+            }
         }
         const df s_prec = df_shfl(df_warp_total(se), 0);
         df W = s_prec;  // bonus and one-hot rows: the weights are the e
@@ -248,14 +277,25 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) verify_warp_kernel(const 
             // w = max(0, e - s q), the product exact through one fma
             bool qbad = false;
             df Wl = df_make(0.0f);
-            for (int v = lane; v < V; v += 32) {
-                const float qq = __ldg(qrow + v);
-                qbad |= !(qq >= 0.0f && qq <= FLT_MAX);
-                const float2 e2 = wv(v);
-                df r = minus_sq(df{e2.x, e2.y}, s_prec, qq);
-                if (!(r.hi + r.lo > 0.0f)) r = df_make(0.0f);
-                wv(v) = make_float2(r.hi, r.lo);
-                Wl = df_sum(Wl, r);
+            for (int v0 = lane; v0 < V; v0 += 32 * kB) {
+                float qb[kB];
+#pragma unroll
+                for (int u = 0; u < kB; ++u) {
+                    const int v = v0 + 32 * u;
+                    qb[u] = v < V ? __ldg(qrow + v) : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < kB; ++u) {
+                    const int v = v0 + 32 * u;
+                    if (v >= V) break;
+                    const float qq = qb[u];
+                    qbad |= !(qq >= 0.0f && qq <= FLT_MAX);
+                    const float2 e2 = wv(v);
+                    df r = minus_sq(df{e2.x, e2.y}, s_prec, qq);
+                    if (!(r.hi + r.lo > 0.0f)) r = df_make(0.0f);
+                    wv(v) = make_float2(r.hi, r.lo);
+                    Wl = df_sum(Wl, r);
+                }
             }
             W = df_shfl(df_warp_total(Wl), 0);
             if (__any_sync(full, qbad)) st |= ST_QBAD;
