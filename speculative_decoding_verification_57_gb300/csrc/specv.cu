@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstring>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -68,7 +69,8 @@ struct DeviceGuard {
 
 
 struct Plan {
-    bool warp = false;  // V <= kWarpKernelMaxV: one warp per row
+    bool warp = false;  // V <= kWarpKernelMaxV: one warp per row, or (row) one CTA per row
+    bool row = false;
     int cluster = 1;
     int slice = 0;
 };
@@ -76,7 +78,14 @@ struct Plan {
 Plan make_plan(const specv_ctx* h, specv_dtype dt, int batch, int64_t V) {
     Plan p;
     if (V <= kWarpKernelMaxV) {
+        // a CTA per row while the batch leaves SMs idle (its positions and
+        // its stop row are then worked on in parallel), else a warp per row
         p.warp = true;
+        p.row = batch <= 2 * h->sm_count;
+        if (const char* env = getenv("SPECV_SMALLV")) {
+            if (!strcmp(env, "row")) p.row = true;
+            if (!strcmp(env, "warp")) p.row = false;
+        }
         return p;
     }
     const int cmin = static_cast<int>((V + kMaxSlice - 1) / kMaxSlice);
@@ -120,9 +129,13 @@ cudaError_t launch_cluster(const VerifyArgs& a, const Plan& p, cudaStream_t stre
 }
 
 template <bool BF16>
-cudaError_t launch_warp(const VerifyArgs& a, cudaStream_t stream) {
-    const unsigned blocks = static_cast<unsigned>((a.B + kWarpsPerBlock - 1) / kWarpsPerBlock);
-    verify_warp_kernel<BF16><<<blocks, 32 * kWarpsPerBlock, 0, stream>>>(a);
+cudaError_t launch_warp(const VerifyArgs& a, bool row, cudaStream_t stream) {
+    if (row) {
+        verify_row_kernel<BF16><<<static_cast<unsigned>(a.B), kRowThreads, 0, stream>>>(a);
+    } else {
+        const unsigned blocks = static_cast<unsigned>((a.B + kWarpsPerBlock - 1) / kWarpsPerBlock);
+        verify_warp_kernel<BF16><<<blocks, 32 * kWarpsPerBlock, 0, stream>>>(a);
+    }
     return cudaGetLastError();
 }
 
@@ -185,7 +198,7 @@ specv_status run(specv_ctx* h, specv_dtype dt, const VerifyArgs& a, void* stream
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (p.warp)
-        e = dt == SPECV_BF16 ? launch_warp<true>(args, s) : launch_warp<false>(args, s);
+        e = dt == SPECV_BF16 ? launch_warp<true>(args, p.row, s) : launch_warp<false>(args, p.row, s);
     else
         e = dt == SPECV_BF16 ? launch_cluster<true>(args, p, s) : launch_cluster<false>(args, p, s);
     if (e != cudaSuccess) return cuda_fail(e, "verify kernel launch");

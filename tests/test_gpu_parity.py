@@ -344,13 +344,16 @@ def test_zz_summary():
         assert TOTALS["mismatched"] <= max(1, 1e-4 * TOTALS["rows"])
 
 
-def test_small_vocabulary_kernel(h):
-    """V <= 2048 (one warp per row) matches the oracle on odd sizes, debug
-    outputs, one-hot drafts, masked entries and unaligned rows."""
+@pytest.mark.parametrize("kernel", ["row", "warp"])
+def test_small_vocabulary_kernels(h, kernel, monkeypatch):
+    """V <= 2048 has two kernels, a CTA per row (small batches) and a warp
+    per row (large ones); each, forced, matches the oracle on odd sizes,
+    debug outputs, one-hot drafts, masked entries and unaligned rows."""
     import torch
 
     import speculative_decoding_verification_57_gb300 as sv
 
+    monkeypatch.setenv("SPECV_SMALLV", kernel)
     cases = [(1, 1, 3, "f32"), (7, 2, 3, "bf16"), (13, 16, 3, "bf16"), (1000, 4, 5, "f32"), (1001, 5, 3, "f32"),
              (2047, 3, 2, "bf16"), (2048, 31, 2, "f32"), (700, 6, 9, "bf16"), (33, 8, 40, "f32")]
     for V, k, B, dtype in cases:
