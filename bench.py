@@ -149,7 +149,7 @@ _CLUSTER_SOURCES = ["verify_cluster.cuh", "ptx.cuh", "exp2dd.cuh", "specv.cu"]
 _WARP_SOURCES = ["verify_warp.cuh", "verify_cluster.cuh", "ptx.cuh", "exp2dd.cuh", "specv.cu"]
 KERNEL_SOURCES = {
     "verify_cluster_kernel_B64_k5_V128256_bf16": _CLUSTER_SOURCES,
-    "verify_warp_kernel_toy_B1_k4_V1000_f32": _WARP_SOURCES,
+    "verify_row_kernel_toy_B1_k4_V1000_f32": _WARP_SOURCES,
     "verify_cluster_kernel_zipf_B8_k4_V32000_bf16": _CLUSTER_SOURCES,
     "verify_cluster_kernel_mixed_B256_k8_V128256_bf16": _CLUSTER_SOURCES,
     "verify_cluster_kernel_split_v_B16_k16_V151936_f32": _CLUSTER_SOURCES,
@@ -179,6 +179,8 @@ def kernel_source_hash(files):
 def measured_traffic(name="verify_cluster_kernel_B64_k5_V128256_bf16"):
     """DRAM traffic per launch of a kernel from its committed ncu summary,
     if it was taken on the kernel's current sources."""
+    if name not in KERNEL_SOURCES:
+        return None
     path = os.path.join(ROOT, "profiles", name + ".json")
     try:
         with open(path) as f:
@@ -250,11 +252,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(used), "in_window": bool(inside)}
 
 
-def profile_name(workload, w, onehot=False):
+def small_v_kernel(B, sms):
+    """The kernel the library runs for a vocabulary of at most 2048: one CTA
+    of eight warps per row while the batch is at most twice the SM count,
+    else one warp per row; SPECV_SMALLV=row|warp forces either."""
+    env = os.environ.get("SPECV_SMALLV")
+    if env in ("row", "warp"):
+        return f"verify_{env}_kernel"
+    return "verify_row_kernel" if B <= 2 * sms else "verify_warp_kernel"
+
+
+def profile_name(workload, w, onehot=False, sms=152):
     """The committed ncu summary of a workload's verify kernel."""
     if workload == WORKLOAD_NAME:
         return "verify_cluster_kernel_onehot_B64_k5_V128256_bf16" if onehot else "verify_cluster_kernel_B64_k5_V128256_bf16"
-    kern = "verify_warp_kernel" if w.V <= 2048 else "verify_cluster_kernel"
+    kern = small_v_kernel(w.B, sms) if w.V <= 2048 else "verify_cluster_kernel"
     return f"{kern}_{workload}_B{w.B}_k{w.k}_V{w.V}_{'bf16' if w.dtype == 'bf16' else 'f32'}"
 
 
@@ -597,9 +609,15 @@ def run_ours(args):
     cpu_one, _, _, _ = time_oracle(w, budget_s=1.0, max_rows=8, nthreads=1)
     parity = compare_rows(ref, got)
     achieved = alg / per_call_s / 1e9
-    traffic = measured_traffic(profile_name(name, w, onehot))
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    traffic = measured_traffic(profile_name(name, w, onehot, sms))
     temps = sorted(set(float(t) for t in w.T))
-    launch_desc = ("one warp per row (verify_warp_kernel)" if V <= 2048 else specv_cluster_desc(sv, h, B, k, V))
+    if V > 2048:
+        launch_desc = specv_cluster_desc(sv, h, B, k, V)
+    elif small_v_kernel(B, sms) == "verify_row_kernel":
+        launch_desc = f"one CTA of 8 warps per row, {B} CTA{'' if B == 1 else 's'} (verify_row_kernel)"
+    else:
+        launch_desc = f"one warp per row, {(B + 1) // 2} CTAs of 2 warps (verify_warp_kernel)"
     line = {
         "metric": "verify rows/s",
         "value": value,
