@@ -61,6 +61,9 @@ def parse_args(argv=None):
     p.add_argument("--variant", choices=["sample", "onehot", "tree", "filtered", "rollback"], default="sample",
                    help="onehot: the same workload verified as one-hot drafts (q = None); tree: greedy "
                         "verification of 16-node draft trees over the same vocabulary")
+    p.add_argument("--top-k", type=int, default=None,
+                   help="filtered variant: top_k of every row (default 40; above 64 the radix-select kernel)")
+    p.add_argument("--top-p", type=float, default=None, help="filtered variant: top_p of every row (default 0.95)")
     p.add_argument("--workload", choices=list(WORKLOADS_DESC), default=WORKLOAD_NAME,
                    help="the named synthetic workload of the sample / onehot variants (and of the reference arm)")
     return p.parse_args(argv)
@@ -791,17 +794,20 @@ FILTER_TOP_K, FILTER_TOP_P = 40, 0.95
 
 
 def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
-    """Sampled verification with top-k 40 / top-p 0.95 on the target rows,
-    on the benchmark workload (B=64, k=5, V=128256 bf16)."""
+    """Sampled verification with top-k / top-p (default 40 / 0.95) on the
+    target rows, on the benchmark workload (B=64, k=5, V=128256 bf16)."""
     import numpy as np
     import torch
 
     from speculative_decoding_verification_57_gb300 import workloads as W
 
+    top_k = FILTER_TOP_K if args.top_k is None else args.top_k
+    top_p = FILTER_TOP_P if args.top_p is None else args.top_p
+    wide = top_k > 64
     w = W.make_workload(WORKLOAD_NAME, seed=W.WORKLOADS[WORKLOAD_NAME][1] + 1000 * rank)
     B, k, V = w.B, w.k, w.V
-    tk = np.full(B, FILTER_TOP_K, np.int32)
-    tp = np.full(B, FILTER_TOP_P, np.float32)
+    tk = np.full(B, top_k, np.int32)
+    tp = np.full(B, top_p, np.float32)
     h = sv.specv_create(local, max_batch=B, max_k=k, vocab=V)
     L0 = torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16)
     host = dict(L=L0, q=torch.from_numpy(w.q), x=torch.from_numpy(w.x), u=torch.from_numpy(w.u),
@@ -826,7 +832,7 @@ def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
     # every logit once; q read at the kept entries of the stop row (at most top_k per row); the
     # per-position q(x), x, u and T; top_k, top_p; outputs
     rejected = got["num_accepted"] < k
-    alg = (B * (k + 1) * V * 2 + int(rejected.sum()) * FILTER_TOP_K * 4 + B * k * 12 + B * 12 + B * 8
+    alg = (B * (k + 1) * V * 2 + int(rejected.sum()) * min(top_k, V) * 4 + B * k * 12 + B * 12 + B * 8
            + B * (k + 2) * 4)
     G = max(1, min(args.graph_calls, args.steps))
     g = torch.cuda.CUDAGraph()
@@ -883,7 +889,7 @@ def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
         stream.synchronize()
     e2e_s = reduce_max(time.perf_counter() - t0, ws, dev)
     assert np.array_equal(host_out["num_accepted"].numpy(), got["num_accepted"])
-    q_in_place = B * k * 4 + int(rejected.sum()) * FILTER_TOP_K * 4
+    q_in_place = B * k * 4 + int(rejected.sum()) * min(top_k, V) * 4
     if rank != 0:
         return 0
     import oracle  # the CPU-baseline leg
@@ -903,14 +909,18 @@ def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
         "metric": "filtered-verify rows/s", "value": B * steps * ws / (ms_max / 1e3), "unit": "rows/s",
         "n_gpus": ws, "steps": steps, "warmup": args.warmup, "ms_per_step": ms_max / steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD + f", top_k {FILTER_TOP_K}, top_p {FILTER_TOP_P}", "B": B, "k": k, "V": V,
+        "config": {"workload": WORKLOAD + f", top_k {top_k}, top_p {top_p}", "B": B, "k": k, "V": V,
                    "global_batch": B * ws, "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": f"rotating {N_SETS} input sets ({N_SETS * (w.logits.nbytes + w.q.nbytes) / 1e9:.2f} GB) "
                          "> 2x L2",
-                   "launch": f"CUDA graph of {G} calls, {B * min(k + 1, 8)} CTAs in clusters of {min(k + 1, 8)}"},
+                   "launch": f"CUDA graph of {G} calls, two launches a call: the top-64 kernel "
+                             f"({B * min(k + 1, 8)} CTAs in clusters of {min(k + 1, 8)}) and the radix-select "
+                             f"kernel ({B * min(k + 1, 16)} CTAs of 512 threads in clusters of {min(k + 1, 16)}); "
+                             f"the rows are the {'second' if wide else 'first'}'s, the other's CTAs exit at once"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak,
-                     "traffic": measured_traffic("verify_topk_kernel_B64_k5_V128256_bf16"),
+                     "traffic": measured_traffic(f"verify_topk_wide_kernel_B64_k5_V128256_bf16_K{top_k}" if wide
+                                                 else "verify_topk_kernel_B64_k5_V128256_bf16"),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, burst)",
                      "algorithmic_bytes_per_launch": alg},
         "cpu_baseline": {"value": cpu_value, "unit": "rows/s", "cores": cores, "kind": "oracle",
@@ -922,7 +932,7 @@ def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
                 "steps": e2e_steps,
                 "path": "pinned copies (logits, x, u, T, top_k, top_p) + specv_verify_sample_filtered with q read "
                         "in place from page-locked host memory + copies back, per step"},
-        "gpu_launches": steps, "mean_num_accepted": float(np.mean(got["num_accepted"])), "clocks": clocks,
+        "gpu_launches": 2 * steps, "mean_num_accepted": float(np.mean(got["num_accepted"])), "clocks": clocks,
     }
     print(json.dumps(line), flush=True)
     return 0

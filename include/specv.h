@@ -68,7 +68,7 @@
  *                              512  (tree verification) a parent index
  *                                   outside [-1, node)
  *                             1024  (top-k / top-p verification) top_k
- *                                   outside [1, 64] or top_p outside (0, 1]
+ *                                   outside [1, 4096] or top_p outside (0, 1]
  *                              The walk checks position 0, 1, ... in order and
  *                              stops at the first position with an error; a
  *                              row with any of the bits 1, 2, 4, 8, 32, 64, 512, 1024 set
@@ -137,8 +137,8 @@ specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const
  * temperature, top-k and top-p have to be applied to p before the rule, and
  * to q before drafting -- q is used as given).  The pages name the filters
  * without defining them; the readings here:
- *   top_k [B] int32, 1..64: keep the top_k largest logits, the lower index
- *         first among equal logits;
+ *   top_k [B] int32, 1..4096: keep the top_k largest logits (all V if
+ *         top_k >= V), the lower index first among equal logits;
  *   top_p [B] fp32, (0, 1]: within those, in the same order, keep the
  *         shortest prefix whose mass (renormalised over the top_k) reaches
  *         top_p (at least one entry; 1 keeps all top_k).
@@ -151,7 +151,11 @@ specv_status specv_verify_sample(specv_handle h, specv_dtype logits_dtype, const
  * top_k or top_p is out of range gets row_status bit 1024 and emits
  * nothing.  Rows with temperature 0 take the greedy rule (the filters keep
  * the argmax).  Other arguments and bits as for specv_verify_sample; no
- * debug outputs.  One thread-block cluster of min(k + 1, 8) CTAs per row. */
+ * debug outputs.  Two launches on the stream: rows with top_k up to 64 (and
+ * greedy or refused rows) take one thread-block cluster of min(k + 1, 8)
+ * CTAs per row that keeps each position's best 64 in registers; rows with
+ * top_k above 64 take a cluster of min(k + 1, 16) CTAs per row that selects
+ * each position's kept set exactly by a radix select on the logits' keys. */
 specv_status specv_verify_sample_filtered(specv_handle h, specv_dtype logits_dtype, const void *target_logits,
                                           const float *draft_probs, const int32_t *draft_tokens,
                                           const float *uniforms, const float *temperature, const int32_t *top_k,

@@ -185,7 +185,7 @@ def specv_verify_greedy(h: Handle, logits, x, *, out=None, stream=None):
 def specv_verify_sample_filtered(h: Handle, logits, q, x, u, T, top_k, top_p, *, out=None, stream=None):
     """Sampled verification with top-k / top-p applied to the target rows:
     as specv_verify_sample (q may be None: one-hot drafts, or a pinned CPU
-    tensor, read in place), plus top_k [B] int32 in 1..64 and top_p [B]
+    tensor, read in place), plus top_k [B] int32 in 1..4096 and top_p [B]
     fp32 in (0, 1], CUDA tensors."""
     torch = _torch()
     B, k1, V = logits.shape

@@ -18,6 +18,7 @@
 #include "verify_warp.cuh"
 #include "rollback.cuh"
 #include "verify_topk.cuh"
+#include "verify_topk_wide.cuh"
 
 using namespace specv;
 
@@ -168,6 +169,11 @@ cudaError_t set_attributes() {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(verify_topk_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(topk_dyn_smem(kMaxK)));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(verify_topk_wide_kernel<BF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(verify_topk_wide_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(wide_dyn_smem(kMaxK)));
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(verify_cluster_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(cluster_dyn_smem(16, kMaxK + 1)));
@@ -367,9 +373,22 @@ specv_status specv_verify_sample_filtered(specv_handle h, specv_dtype logits_dty
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = logits_dtype == SPECV_BF16 ? cudaLaunchKernelEx(&cfg, verify_topk_kernel<true>, a)
-                                                     : cudaLaunchKernelEx(&cfg, verify_topk_kernel<false>, a);
+    cudaError_t e = logits_dtype == SPECV_BF16 ? cudaLaunchKernelEx(&cfg, verify_topk_kernel<true>, a)
+                                               : cudaLaunchKernelEx(&cfg, verify_topk_kernel<false>, a);
     if (e != cudaSuccess) return cuda_fail(e, "verify_topk launch");
+    h->launches.fetch_add(1, std::memory_order_relaxed);
+    // Rows with top_k above 64 go to the wide kernel, rows up to 64 (and
+    // greedy or refused rows) to the one above: each kernel leaves the
+    // other's rows untouched, so the two launches share nothing but the
+    // stream.  top_k is on the device, so both are always launched.
+    const int Cw = wide_cluster(k);
+    cfg.gridDim = dim3(static_cast<unsigned>(batch) * Cw, 1, 1);
+    cfg.blockDim = dim3(kWideThreads, 1, 1);
+    cfg.dynamicSmemBytes = wide_dyn_smem(k);
+    attr[0].val.clusterDim.x = static_cast<unsigned>(Cw);
+    e = logits_dtype == SPECV_BF16 ? cudaLaunchKernelEx(&cfg, verify_topk_wide_kernel<true>, a)
+                                   : cudaLaunchKernelEx(&cfg, verify_topk_wide_kernel<false>, a);
+    if (e != cudaSuccess) return cuda_fail(e, "verify_topk_wide launch");
     h->launches.fetch_add(1, std::memory_order_relaxed);
     return SPECV_OK;
 }

@@ -70,7 +70,7 @@ enum : int {
     ST_QBAD = 32,
     ST_TIMEOUT = 64,
     ST_PARENT = 512,   // tree verification: a parent index outside [-1, node)
-    ST_FILTER = 1024,  // top-k / top-p verification: top_k outside [1, 64] or top_p outside (0, 1]
+    ST_FILTER = 1024,  // top-k / top-p verification: top_k outside [1, 4096] or top_p outside (0, 1]
     ST_ERRMASK = 1 | 2 | 4 | 8 | 32 | 64 | 512 | 1024,
 };
 

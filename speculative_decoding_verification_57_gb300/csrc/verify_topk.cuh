@@ -40,6 +40,13 @@
 namespace specv {
 
 constexpr int kTopKMax = 64;       // largest top_k this path takes
+constexpr int kWideKMax = 4096;    // largest top_k at all: rows above kTopKMax are verify_topk_wide_kernel's
+
+// Rows verify_topk_wide_kernel verifies (sampled, valid filters, top_k above
+// this path's 64); this kernel leaves them untouched.
+__device__ __forceinline__ bool wide_row(float T, int K, float top_p) {
+    return T >= FLT_MIN && T <= FLT_MAX && K > kTopKMax && K <= kWideKMax && top_p > 0.0f && top_p <= 1.0f;
+}
 constexpr int kTopkClusterMax = 8;  // CTAs per sequence
 constexpr int kTopkLocalMax = (kMaxK + 1 + kTopkClusterMax - 1) / kTopkClusterMax;  // positions per CTA
 constexpr int kTopkStages = 8;     // ring stages of kTileBytes: the four warps drift apart by a few tiles
@@ -284,7 +291,8 @@ __global__ void __launch_bounds__(kThreads, 3) verify_topk_kernel(const VerifyAr
     const bool t_ok = greedy || (T >= FLT_MIN && T <= FLT_MAX);
     const int K = a.top_k ? __ldg(a.top_k + b) : kTopKMax;
     const float top_p = a.top_p ? __ldg(a.top_p + b) : 1.0f;
-    const bool f_ok = greedy || (K >= 1 && K <= kTopKMax && top_p > 0.0f && top_p <= 1.0f);
+    if (wide_row(T, K, top_p)) return;  // the whole cluster leaves: the wide kernel has the row
+    const bool f_ok = greedy || (K >= 1 && K <= kWideKMax && top_p > 0.0f && top_p <= 1.0f);
     const bool run = t_ok && f_ok;
 
     // ---------------------------------------------------------------- setup

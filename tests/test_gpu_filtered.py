@@ -92,15 +92,50 @@ def test_filter_errors_and_bad_rows(h):
     w.logits[5, 0, 17] = np.nan
     w.logits[6, 1, 3] = np.inf
     w.x[7, 0] = 5000
-    K = [0, 65, 10, 10, 10, 10, 10, 10]
+    K = [0, 4097, 10, 10, 10, 10, 10, 10]
     P = np.array([1, 1, 0, 1.5, 1, 1, 1, 1], np.float32)
     got = _run(h, w, K, P)
-    keep = np.array([0, 2, 3, 4, 5, 6, 7])
-    sub = W.Workload(w.name, w.dtype, w.logits[keep], w.q[keep], w.x[keep], w.u[keep], w.T[keep])
-    _, ref = _check(sub, {kk: v[keep] for kk, v in got.items()}, np.asarray(K)[keep], P[keep])
-    ref = {kk: np.insert(v, 1, 0, axis=0) for kk, v in ref.items()}
-    assert ref["row_status"][[0, 2, 3, 5, 7]].tolist() == [1024, 1024, 1024, 1, 2]
-    assert got["row_status"][1] == 1024  # beyond this path's 64 (the oracle's definition takes it)
+    _, ref = _check(w, got, K, P)
+    assert ref["row_status"][[0, 1, 2, 3, 5, 7]].tolist() == [1024, 1024, 1024, 1024, 1, 2]
+    # the same bad rows with top_k above 64 (the wide kernel's)
+    K = [0, 4097, 100, 100, 3000, 4096, 200, 65]
+    assert _check(w, _run(h, w, K, P), K, P)[1]["row_status"][[0, 1, 2, 3, 5, 7]].tolist() == [1024, 1024, 1024,
+                                                                                               1024, 1, 2]
+
+
+@pytest.mark.parametrize("B,k,V,dtype,K,p", [(16, 5, 128256, "bf16", 4096, 1.0), (16, 5, 128256, "bf16", 4096, 0.9),
+                                             (24, 4, 32000, "bf16", 1000, 0.95), (8, 16, 151936, "f32", 300, 0.8),
+                                             (12, 3, 40003, "f32", 65, 1.0), (10, 2, 1000, "f32", 2000, 0.7),
+                                             (6, 31, 5001, "bf16", 100, 0.5)])
+def test_wide_top_k_matches_oracle(h, B, k, V, dtype, K, p):
+    """top_k above 64 (the radix-select kernel): up to the 4096 the oracle
+    takes, top-p alone within the 4096 at the full Llama-3 vocabulary, top_k
+    above V, 16 positions (two on one CTA) and 31."""
+    w = W.make_random(name="wide", B=B, k=k, V=V, dtype=dtype, seed=V + K + k, logit_sigma=3.0, draft_sigma=0.4,
+                      temperature=0.9, spike=4.0, spike_mode="position", greedy_rows=2)
+    mism, ref = _check(w, _run(h, w, [K] * B, [p] * B), [K] * B, [p] * B)
+    assert mism <= 1
+    assert (ref["row_status"] == 0).sum() >= B // 2
+    assert ref["num_accepted"].max() >= 1  # some rows get past position 0
+
+
+def test_wide_mixed_with_narrow_rows(h):
+    """One call whose rows go to both kernels (top_k up to 64 and above),
+    one-hot and full q, many uniform sets at the benchmark's shape."""
+    rng = np.random.default_rng(11)
+    w = W.make_random(name="wmix", B=48, k=4, V=50000, dtype="bf16", seed=12, logit_sigma=2.5, draft_sigma=0.5,
+                      temperature=1.1, spike=6.0, spike_mode="position", greedy_rows=4)
+    K = rng.choice([5, 64, 65, 300, 4096], size=48)
+    P = rng.choice([1.0, 0.95, 0.5], size=48).astype(np.float32)
+    assert _check(w, _run(h, w, K, P, onehot=True), K, P, onehot=True)[0] <= 1
+    assert _check(w, _run(h, w, K, P), K, P)[0] <= 1
+    base = W.make_workload("benchmark")
+    mism = 0
+    for r in range(3):
+        wr = W.Workload(base.name, base.dtype, base.logits[:16], base.q[:16], base.x[:16],
+                        rng.random(base.u[:16].shape, dtype=np.float32), base.T[:16])
+        mism += _check(wr, _run(h, wr, [1000] * 16, [0.95] * 16), [1000] * 16, [0.95] * 16)[0]
+    assert mism <= 1
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
@@ -122,12 +157,12 @@ def test_filtered_ties_and_degenerate_rows(h, dtype):
     w.x[0] = rng.integers(0, 64, size=k)           # inside the flat row's kept set
     logits = W.f32_to_bf16_bits(L.astype(np.float32)) if dtype == "bf16" else L.astype(np.float32)
     w = W.Workload(w.name, w.dtype, logits, w.q, w.x, w.u, w.T)
-    for K, p in [(64, 1.0), (13, 0.8), (1, 1.0)]:
+    for K, p in [(64, 1.0), (13, 0.8), (1, 1.0), (100, 0.8), (3001, 1.0), (2000, 0.3), (65, 0.99)]:
         _check(w, _run(h, w, [K] * B, [p] * B), [K] * B, [p] * B)
 
 
 def test_filtered_pinned_host_q(h):
-    """q in page-locked host memory is read in place."""
+    """q in page-locked host memory is read in place (by both kernels)."""
     import torch
 
     import speculative_decoding_verification_57_gb300 as sv
@@ -136,7 +171,7 @@ def test_filtered_pinned_host_q(h):
     w = W.make_random(name="fpin", B=16, k=4, V=32000, dtype="bf16", seed=21, logit_sigma=3.0, draft_sigma=0.7,
                       temperature=0.9, spike=4.0, spike_mode="position", greedy_rows=2)
     L, _, x, u, T = to_device(w, "cuda:0")
-    K, P = [40] * 16, [0.9] * 16
+    K, P = [40] * 8 + [500] * 8, [0.9] * 16
     out = sv.specv_verify_sample_filtered(h, L, torch.from_numpy(w.q).pin_memory(), x, u, T,
                                           torch.tensor(K, dtype=torch.int32, device="cuda:0"),
                                           torch.tensor(P, dtype=torch.float32, device="cuda:0"))
@@ -145,7 +180,8 @@ def test_filtered_pinned_host_q(h):
 
 
 @pytest.mark.parametrize("V,dtype,K,p,k", [(50, "f32", 64, 1.0, 3), (37, "bf16", 40, 0.5, 2), (2049, "bf16", 64, 0.05, 1),
-                                           (8, "f32", 3, 1.0, 6)])
+                                           (8, "f32", 3, 1.0, 6), (50, "f32", 100, 1.0, 3), (37, "bf16", 4096, 0.5, 2),
+                                           (2049, "bf16", 700, 0.05, 1), (8, "f32", 65, 0.9, 6)])
 def test_filtered_small_vocabularies(h, V, dtype, K, p, k):
     """V below the 64 kept entries (padded lists), top-p cutting to a single
     entry, one draft, tiny vocabularies."""
