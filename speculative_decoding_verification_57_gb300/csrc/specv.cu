@@ -173,7 +173,7 @@ cudaError_t set_attributes() {
     e = cudaFuncSetAttribute(verify_topk_wide_kernel<BF16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(verify_topk_wide_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(wide_dyn_smem(kMaxK)));
+                             static_cast<int>(wide_dyn_smem(kMaxK, 262144)));
     if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(verify_cluster_kernel<BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(cluster_dyn_smem(16, kMaxK + 1)));
@@ -384,7 +384,7 @@ specv_status specv_verify_sample_filtered(specv_handle h, specv_dtype logits_dty
     const int Cw = wide_cluster(k);
     cfg.gridDim = dim3(static_cast<unsigned>(batch) * Cw, 1, 1);
     cfg.blockDim = dim3(kWideThreads, 1, 1);
-    cfg.dynamicSmemBytes = wide_dyn_smem(k);
+    cfg.dynamicSmemBytes = wide_dyn_smem(k, V);
     attr[0].val.clusterDim.x = static_cast<unsigned>(Cw);
     e = logits_dtype == SPECV_BF16 ? cudaLaunchKernelEx(&cfg, verify_topk_wide_kernel<true>, a)
                                    : cudaLaunchKernelEx(&cfg, verify_topk_wide_kernel<false>, a);

@@ -16,16 +16,18 @@
 //   1. a radix select on the logits' order-preserving keys (bf16: 12 + 4
 //      bits, fp32: 12 + 12 + 8 bits), one pass over the row a digit, finds
 //      the key of the K-th largest entry, key*, and how many entries lie
-//      above it; the last digit's counts are kept per warp, each warp owning
-//      a contiguous stretch of the row, so that the ties at key* that fit
-//      (the lowest indices) are known per warp;
-//   2. one more pass marks the kept entries in a bitmap of the vocabulary,
-//      which a block scan turns into the kept list in vocabulary order
-//      (index and logit, at most 4096 entries, in shared memory);
-//   3. on the list: the maximum M, every weight e = exp((l - M) / T) with
-//      the double-float exponential, their sum, and (top_p < 1) the top-p
-//      cut by bisection on the key: the largest key whose entries and those
-//      above reach top_p of the sum, and how many of its ties are needed;
+//      above it.  The first pass counts every entry (two keys a 32-bit word
+//      for bf16); the later ones skip, with one packed maximum a 16-byte
+//      group, the groups whose entries all lie below the digit's range;
+//   2. one more pass marks the entries above key* and those equal to it in
+//      two bitmaps of the vocabulary; a block scan in vocabulary order turns
+//      them into the kept list (the ties up to the count that fits, the
+//      lowest indices first): index and logit, at most 4096 entries, in
+//      shared memory;
+//   3. on the list: the maximum M and, for top_p < 1, a bitonic sort of the
+//      list into rank order, a prefix sum of the weights e = exp((l - M) / T)
+//      (double-float exponential and sums) and the first rank where it
+//      reaches top_p of the total: that entry's (key, index) is the cut;
 //   4. p'(x_i) goes to the leader CTA over distributed shared memory.
 // After a cluster barrier the leader's warp 0 walks the positions, and the
 // CTA that owns the stop position draws from its kept list: weights in
@@ -35,6 +37,8 @@
 #include <cfloat>
 #include <climits>
 #include <cstdint>
+
+#include <cuda_bf16.h>
 
 #include "exp2dd.cuh"
 #include "ptx.cuh"
@@ -47,20 +51,25 @@ constexpr int kWideThreads = 512;
 constexpr int kWideWarps = kWideThreads / 32;
 constexpr int kWideEpt = kWideKMax / kWideThreads;  // kept-list entries per thread
 constexpr int kWideClusterMax = 16;                // CTAs per sequence
-constexpr int kWideWorkBytes = 32768;              // histograms, then the bitmap (V <= 262144), then the weights
 constexpr int kWideSlotBytes = kWideKMax * 8;      // one position's kept list: index and logit
 constexpr int kWideSlots = (kMaxK + kWideClusterMax) / kWideClusterMax;  // positions a CTA owns at most
+constexpr int kWideHistBins = 4096;                // 12-bit digits
 static_assert(kWideEpt * kWideThreads == kWideKMax, "the kept list is split evenly over the threads");
-static_assert(kWideKMax * 8 <= kWideWorkBytes, "the weights of a kept list fit the work area");
-static_assert(262144 / 8 <= kWideWorkBytes, "the bitmap of the largest vocabulary fits the work area");
 
 inline int wide_cluster(int k) { return k + 1 < kWideClusterMax ? k + 1 : kWideClusterMax; }
 
+// Work area: the histogram, then the two bitmaps, then the sort keys.
+__host__ __device__ inline int wide_work_bytes(long long V) {
+    const long long bitmaps = 2 * ((V + 31) / 32) * 4;
+    const long long least = kWideKMax * 8;  // the sort keys (and 4096 bins of 4 bytes)
+    return static_cast<int>(bitmaps > least ? bitmaps : least);
+}
+
 // Dynamic shared memory: the work area, then one kept list per owned position.
-inline size_t wide_dyn_smem(int k) {
+inline size_t wide_dyn_smem(int k, long long V) {
     const int C = wide_cluster(k);
     const int P = (k + C) / C;  // ceil((k + 1) / C)
-    return static_cast<size_t>(kWideWorkBytes) + static_cast<size_t>(P) * kWideSlotBytes;
+    return static_cast<size_t>(wide_work_bytes(V)) + static_cast<size_t>(P) * kWideSlotBytes;
 }
 
 // Order-preserving keys (a larger logit has a larger key; -0 is +0).  bf16:
@@ -76,9 +85,26 @@ __device__ __forceinline__ uint32_t key32(uint32_t f) {
     return (f & 0x80000000u) ? ~f : (f | 0x80000000u);
 }
 
+// key16 of both halves of a word at once: a set sign bit flips all 16 bits,
+// a clear one the sign bit only; -0 (which comes out 0x7fff) is moved to +0.
+__device__ __forceinline__ uint32_t key16x2(uint32_t w) {
+    const uint32_t k = w ^ 0x80008000u ^ (((w >> 15) & 0x00010001u) * 0x7fffu);
+    return k + (__vcmpeq2(k, 0x7fff7fffu) & 0x00010001u);
+}
+
 template <bool BF16>
 __device__ __forceinline__ uint32_t val_key(float v) {
     return BF16 ? key16(__float_as_uint(v) >> 16) : key32(__float_as_uint(v));
+}
+
+// The value of a key (NaN for the keys no logit has).
+template <bool BF16>
+__device__ __forceinline__ float key_val(uint32_t key) {
+    if (BF16) {
+        const uint32_t b = (key & 0x8000u) ? (key ^ 0x8000u) : (~key & 0xffffu);
+        return __uint_as_float(b << 16);
+    }
+    return __uint_as_float((key & 0x80000000u) ? (key ^ 0x80000000u) : ~key);
 }
 
 template <bool BF16>
@@ -87,86 +113,146 @@ __device__ __forceinline__ float ld_val(const unsigned char* rowp, int e) {
     return __ldg(reinterpret_cast<const float*>(rowp) + e);
 }
 
-// One logit's bit pattern: its key, whether it takes part (not NaN), and
-// whether it makes the row non-finite (NaN or +inf).
-template <bool BF16>
-__device__ __forceinline__ bool take_bits(uint32_t bits, uint32_t& key, bool& bad) {
-    if (BF16) {
-        const bool nan = (bits & 0x7fffu) > 0x7f80u;
-        bad |= nan || bits == 0x7f80u;
-        key = key16(bits);
-        return !nan;
-    }
-    const bool nan = (bits & 0x7fffffffu) > 0x7f800000u;
-    bad |= nan || bits == 0x7f800000u;
-    key = key32(bits);
-    return !nan;
+__device__ __forceinline__ __nv_bfloat162 as_bf2(uint32_t w) {
+    __nv_bfloat162 r;
+    memcpy(&r, &w, 4);
+    return r;
 }
 
-// Walks one warp's stretch of a row in vocabulary order: the scalar head
-// (entries before the first 16-byte boundary) belongs to warp 0, before its
-// groups; the scalar tail to the last warp, after its groups; the 16-byte
-// groups between are split evenly over the warps.  Every lane calls
-// f(e0, keys, vmask) once a round, the same number of times: keys[q] is
-// entry e0 + q's key, bit q of vmask says it exists (and is not NaN).
-// Within a round the lanes' entries follow lane order.
-template <bool BF16, typename F>
-__device__ __forceinline__ void wide_walk(const unsigned char* rowp, int n, int h, int ng, int warp, int lane,
-                                          bool& bad, F&& f) {
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 v) {
+    uint32_t r;
+    memcpy(&r, &v, 4);
+    return r;
+}
+
+// Level 0: every entry of the row counted by its key's top 12 bits; returns
+// whether this thread met a NaN or +inf (the row is then refused, and what
+// the counts hold does not matter).  Threads take 16-byte groups in turn.
+template <bool BF16>
+__device__ __forceinline__ bool wide_hist0(const unsigned char* rowp, int n, int h, int ng, uint32_t* hist) {
     constexpr int G = BF16 ? 8 : 4;
     constexpr int esz = BF16 ? 2 : 4;
-    uint32_t keys[G];
-    auto scalar_round = [&](int e) {
-        uint32_t vm = 0;
-        if (e >= 0) {
-            const uint32_t bits = BF16 ? static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(rowp) + e))
-                                       : __float_as_uint(__ldg(reinterpret_cast<const float*>(rowp) + e));
-            vm = take_bits<BF16>(bits, keys[0], bad) ? 1u : 0u;
+    const int tid = threadIdx.x;
+    bool bad = false;
+    auto scalar = [&](int e) {
+        uint32_t key;
+        if (BF16) {
+            const uint32_t b = __ldg(reinterpret_cast<const unsigned short*>(rowp) + e);
+            bad |= (b & 0x7fffu) > 0x7f80u || b == 0x7f80u;
+            key = key16(b);
+            atomicAdd(&hist[key >> 4], 1u);
+        } else {
+            const uint32_t f = __float_as_uint(__ldg(reinterpret_cast<const float*>(rowp) + e));
+            bad |= (f & 0x7fffffffu) > 0x7f800000u || f == 0x7f800000u;
+            key = key32(f);
+            atomicAdd(&hist[key >> 20], 1u);
         }
-        f(e < 0 ? 0 : e, keys, vm);
     };
-    if (warp == 0 && h > 0) scalar_round(lane < h ? lane : -1);
-    const int g0 = static_cast<int>(static_cast<long long>(ng) * warp / kWideWarps);
-    const int g1 = static_cast<int>(static_cast<long long>(ng) * (warp + 1) / kWideWarps);
-    for (int base = g0; base < g1; base += 128) {
+    if (tid < h) scalar(tid);
+    const int t0 = h + ng * G;
+    if (tid < n - t0) scalar(t0 + tid);
+    uint32_t mxb = BF16 ? 0xff80ff80u : __float_as_uint(-INFINITY);  // running maximum, NaN kept
+    for (int base = 0; base < ng; base += 4 * kWideThreads) {
         uint4 w[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int g = base + 32 * u + lane;
-            w[u] = g < g1 ? __ldg(reinterpret_cast<const uint4*>(rowp + (static_cast<long long>(h) + static_cast<long long>(g) * G) * esz))
+            const int g = base + u * kWideThreads + tid;
+            w[u] = g < ng ? __ldg(reinterpret_cast<const uint4*>(rowp + (static_cast<long long>(h) + static_cast<long long>(g) * G) * esz))
                           : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int g = base + 32 * u + lane;
-            uint32_t vm = 0;
-            if (g < g1) {
+            const int g = base + u * kWideThreads + tid;
+            if (g < ng) {
                 const uint32_t wd[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-                if (BF16) {
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        vm |= (take_bits<true>(wd[m] & 0xffffu, keys[2 * m], bad) ? 1u : 0u) << (2 * m);
-                        vm |= (take_bits<true>(wd[m] >> 16, keys[2 * m + 1], bad) ? 1u : 0u) << (2 * m + 1);
+                for (int m = 0; m < 4; ++m) {
+                    if (BF16) {
+                        mxb = bf2_bits(__hmax2_nan(as_bf2(mxb), as_bf2(wd[m])));
+                        const uint32_t k = key16x2(wd[m]);
+                        atomicAdd(&hist[(k >> 4) & 0xfffu], 1u);
+                        atomicAdd(&hist[k >> 20], 1u);
+                    } else {
+                        mxb = __float_as_uint(max_nan_f32(__uint_as_float(mxb), __uint_as_float(wd[m])));
+                        uint32_t k = wd[m] ^ (static_cast<uint32_t>(static_cast<int>(wd[m]) >> 31) | 0x80000000u);
+                        k += k == 0x7fffffffu ? 1u : 0u;
+                        atomicAdd(&hist[k >> 20], 1u);
                     }
-                } else {
-#pragma unroll
-                    for (int m = 0; m < 4; ++m) vm |= (take_bits<false>(wd[m], keys[m], bad) ? 1u : 0u) << m;
                 }
             }
-            f(h + g * G, keys, vm);
         }
     }
+    if (BF16) {
+        const uint32_t lo = mxb & 0xffffu, hi = mxb >> 16;
+        bad |= (lo & 0x7fffu) > 0x7f80u || lo == 0x7f80u || (hi & 0x7fffu) > 0x7f80u || hi == 0x7f80u;
+    } else {
+        bad |= (mxb & 0x7fffffffu) > 0x7f800000u || mxb == 0x7f800000u;
+    }
+    return bad;
+}
+
+// The later passes: f(e, key) for every entry of a 16-byte group whose
+// largest value is at least vmin (and for the scalar head and tail), so that
+// the groups entirely below the range of interest cost one packed maximum.
+// The row is finite here (level 0 refused it otherwise).
+template <bool BF16, typename F>
+__device__ __forceinline__ void wide_scan(const unsigned char* rowp, int n, int h, int ng, float vmin, F&& f) {
+    constexpr int G = BF16 ? 8 : 4;
+    constexpr int esz = BF16 ? 2 : 4;
+    const int tid = threadIdx.x;
+    if (tid < h) {
+        const float v = ld_val<BF16>(rowp, tid);
+        f(tid, val_key<BF16>(v));
+    }
     const int t0 = h + ng * G;
-    if (warp == kWideWarps - 1 && t0 < n) scalar_round(lane < n - t0 ? t0 + lane : -1);
+    if (tid < n - t0) {
+        const float v = ld_val<BF16>(rowp, t0 + tid);
+        f(t0 + tid, val_key<BF16>(v));
+    }
+    for (int base = 0; base < ng; base += 4 * kWideThreads) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int g = base + u * kWideThreads + tid;
+            w[u] = g < ng ? __ldg(reinterpret_cast<const uint4*>(rowp + (static_cast<long long>(h) + static_cast<long long>(g) * G) * esz))
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int g = base + u * kWideThreads + tid;
+            if (g >= ng) continue;
+            const uint32_t wd[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+            float gm;
+            if (BF16) {
+                const __nv_bfloat162 a = __hmax2(__hmax2(as_bf2(wd[0]), as_bf2(wd[1])), __hmax2(as_bf2(wd[2]), as_bf2(wd[3])));
+                gm = fmaxf(__low2float(a), __high2float(a));
+            } else {
+                gm = fmaxf(fmaxf(__uint_as_float(wd[0]), __uint_as_float(wd[1])),
+                           fmaxf(__uint_as_float(wd[2]), __uint_as_float(wd[3])));
+            }
+            if (!(gm >= vmin)) continue;
+            const int e0 = h + g * G;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                if (BF16) {
+                    const uint32_t k = key16x2(wd[m]);
+                    f(e0 + 2 * m, k & 0xffffu);
+                    f(e0 + 2 * m + 1, k >> 16);
+                } else {
+                    f(e0 + m, key32(wd[m]));
+                }
+            }
+        }
+    }
 }
 
 struct WideSlot {
-    df S;           // mass of the kept set P, in e-units
-    float M;        // the row maximum
-    uint32_t cut;   // P: list entries with a key above cut, and the first
-    int m_cut;      // m_cut (vocabulary order) whose key equals it (cut 0: every entry)
-    int n;          // kept-list entries: min(top_k, V)
-    int bad;        // a NaN or +inf logit, or every logit -inf
+    df S;             // mass of the kept set P, in e-units
+    float M;          // the row maximum
+    uint32_t cut;     // P: list entries with a key above cut, or equal to it
+    int cutidx;       // with an index up to cutidx (cut 0: every entry)
+    int n;            // kept-list entries: min(top_k, V)
+    int bad;          // a NaN or +inf logit, or every logit -inf
 };
 
 struct alignas(16) WideSmem {
@@ -175,34 +261,23 @@ struct alignas(16) WideSmem {
     df red_df[kWideWarps];
     uint32_t red_u[kWideWarps];
     float red_f[kWideWarps];
-    uint32_t quota[kWideWarps];  // ties at key* each warp keeps
     int xs[kMaxK + 1];
     float lpx[kMaxK + 1];        // this CTA's p'(x_i) and flags, pushed to the leader at the end
     int lbad[kMaxK + 1];
     float px[kMaxK + 1];         // the leader's copy of every position's
     int pbad[kMaxK + 1];
-    df e_cut;
     int dstar;
     uint32_t dabove;
-    int xr;
-    int m_cut;
     df S;
+    int mties;                   // ties at the top-p cut that are kept
+    int cutidx;
+    float xpx;
     int dj, dst;                 // the decision (written by the leader into every CTA)
     float du1;
 };
 
 // Block-wide helpers over the 512 threads; each ends with a barrier, so the
 // scratch may be reused at once.
-__device__ __forceinline__ uint32_t wide_sum_u32(uint32_t v, uint32_t* red) {
-    v = __reduce_add_sync(0xffffffffu, v);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    uint32_t t = 0;
-    for (int i = 0; i < kWideWarps; ++i) t += red[i];
-    __syncthreads();
-    return t;
-}
-
 __device__ __forceinline__ uint32_t wide_min_u32(uint32_t v, uint32_t* red) {
     v = __reduce_min_sync(0xffffffffu, v);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
@@ -265,15 +340,19 @@ __device__ __forceinline__ df wide_sum_df(df v, df* red) {
     return t;
 }
 
-// Exclusive prefix of pairs in thread order.
-__device__ __forceinline__ df wide_excl_scan_df(df v, df* red) {
+// Exclusive prefix of pairs in thread order, and the total.
+__device__ __forceinline__ df wide_excl_scan_df(df v, df* red, df& total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const df incl = df_warp_incl_scan(v, lane);
     if (lane == 31) red[w] = incl;
     __syncthreads();
-    df base = df_make(0.0f);
-    for (int i = 0; i < w; ++i) base = df_sum(base, red[i]);
+    df base = df_make(0.0f), tot = df_make(0.0f);
+    for (int i = 0; i < kWideWarps; ++i) {
+        if (i == w) base = tot;
+        tot = df_sum(tot, red[i]);
+    }
     __syncthreads();
+    total = tot;
     const df up = df_shfl_up(incl, 1);  // every lane takes part; lane 0 then drops it
     return lane == 0 ? base : df_sum(base, up);
 }
@@ -306,13 +385,32 @@ __device__ __forceinline__ void wide_find_digit(const uint32_t* hist, int nb, ui
     __syncthreads();
 }
 
+// Bitonic sort of n2 (a power of two, at most kWideKMax) 64-bit keys in
+// shared memory into descending order.
+__device__ __forceinline__ void wide_sort_desc(unsigned long long* s, int n2) {
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < (n2 >> 1); i += kWideThreads) {
+                const int a = ((i & ~(stride - 1)) << 1) | (i & (stride - 1));
+                const int c = a + stride;
+                const unsigned long long x = s[a], y = s[c];
+                const bool desc = (a & size) == 0;
+                if ((x < y) == desc) {
+                    s[a] = y;
+                    s[c] = x;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ WideSmem sh;
     constexpr int esz = BF16 ? 2 : 4;
     constexpr int G = 16 / esz;
-    constexpr int KB = BF16 ? 16 : 32;  // key bits
     const unsigned full = 0xffffffffu;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int C = static_cast<int>(cluster_size());
@@ -327,8 +425,12 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
     if (!wide_row(T, K, top_p)) return;  // the whole cluster leaves: verify_topk_kernel has the row
     cluster_arrive();                      // paired with the wait before the first remote store
 
+    const int work_bytes = wide_work_bytes(a.V);
     uint32_t* work = reinterpret_cast<uint32_t*>(dyn_smem);
-    df* ework = reinterpret_cast<df*>(dyn_smem);
+    const int nwords = (n + 31) >> 5;
+    uint32_t* strict_bm = work;         // entries above key*
+    uint32_t* tie_bm = work + nwords;   // entries equal to key*
+    unsigned long long* skeys = reinterpret_cast<unsigned long long*>(dyn_smem);
     if (tid < 128) sh.exp2tab[tid] = g_exp2_table[tid];
     if (tid <= k) sh.xs[tid] = tid < k ? __ldg(a.x + static_cast<long long>(b) * k + tid) : -1;
     RowConst rc;
@@ -341,11 +443,12 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
     }
     const int Kp = K < n ? K : n;
     const int P = (k - crank) / C + 1;  // owned positions crank + C p, p < P
+    const int r0 = tid * kWideEpt;      // this thread's kept-list entries
 
     for (int p = 0; p < P; ++p) {
         const int i = crank + C * p;
-        int* lidx = reinterpret_cast<int*>(dyn_smem + kWideWorkBytes + p * kWideSlotBytes);
-        float* lval = reinterpret_cast<float*>(dyn_smem + kWideWorkBytes + p * kWideSlotBytes + kWideKMax * 4);
+        int* lidx = reinterpret_cast<int*>(dyn_smem + work_bytes + p * kWideSlotBytes);
+        float* lval = reinterpret_cast<float*>(dyn_smem + work_bytes + p * kWideSlotBytes + kWideKMax * 4);
         const unsigned char* rowp = reinterpret_cast<const unsigned char*>(a.logits) +
                                     (static_cast<long long>(b) * (k + 1) + i) * static_cast<long long>(n) * esz;
         int h = static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(rowp) & 15)) & 15) / esz);
@@ -353,123 +456,85 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
         const int ng = (n - h) / G;
 
         // ------------------------------------------------ 1. radix select of key*
-        bool badl = false;
-        bool bad = false;
+        for (int d = tid; d < kWideHistBins; d += kWideThreads) work[d] = 0u;
+        __syncthreads();
+        bool bad = __syncthreads_or(wide_hist0<BF16>(rowp, n, h, ng, work) ? 1 : 0) != 0;
         uint32_t prefix = 0, c_above = 0;
-        const int nlev = BF16 ? 2 : 3;
-        int nb_last = 0;
-        for (int lev = 0; lev < nlev; ++lev) {
-            const int width = BF16 ? (lev == 0 ? 12 : 4) : (lev == 2 ? 8 : 12);
-            const int shift = BF16 ? (lev == 0 ? 4 : 0) : (lev == 0 ? 20 : (lev == 1 ? 8 : 0));
-            const int nb = 1 << width;
-            const bool last = lev == nlev - 1;
-            const int hs = shift + width;  // the bits above this digit must equal prefix
-            for (int d = tid; d < (last ? kWideWarps * nb : nb); d += kWideThreads) work[d] = 0u;
-            __syncthreads();
-            uint32_t* hist = last ? work + warp * nb : work;
-            wide_walk<BF16>(rowp, n, h, ng, warp, lane, badl, [&](int, const uint32_t* keys, uint32_t vm) {
-#pragma unroll
-                for (int q = 0; q < G; ++q)
-                    if ((vm >> q) & 1u) {
-                        const uint32_t key = keys[q];
-                        if (lev == 0 || (key >> hs) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
-                    }
-            });
-            if (lev == 0) {
-                bad = __syncthreads_or(badl ? 1 : 0) != 0;
-                if (bad) break;  // the row is non-finite: nothing more is needed of it
-            } else {
-                __syncthreads();
+        int pbits = BF16 ? 4 : 20;  // key bits below the digits found so far
+        if (!bad) {
+            wide_find_digit(work, kWideHistBins, static_cast<uint32_t>(Kp), sh);
+            if (sh.dstar < 0) bad = true;  // cannot happen on a finite row
+            else {
+                c_above = sh.dabove;
+                prefix = static_cast<uint32_t>(sh.dstar);
             }
-            const uint32_t need = static_cast<uint32_t>(Kp) - c_above;
-            if (last) {
-                for (int d = tid; d < nb; d += kWideThreads) {
-                    uint32_t s = 0;
-                    for (int w = 0; w < kWideWarps; ++w) s += work[w * nb + d];
-                    work[kWideWarps * nb + d] = s;
-                }
-                __syncthreads();
-                wide_find_digit(work + kWideWarps * nb, nb, need, sh);
-            } else {
-                wide_find_digit(work, nb, need, sh);
-            }
-            if (sh.dstar < 0) {  // fewer entries than top_k take part: only NaNs do that
-                bad = true;
-                break;
-            }
-            c_above += sh.dabove;
-            prefix = (prefix << width) | static_cast<uint32_t>(sh.dstar);
-            nb_last = nb;
         }
+        const int nlev = BF16 ? 1 : 2;  // digits after the first
+        for (int lev = 0; lev < nlev && !bad; ++lev) {
+            const int width = BF16 ? 4 : (lev == 0 ? 12 : 8);
+            const int shift = pbits - width;
+            const int nb = 1 << width;
+            for (int d = tid; d < nb; d += kWideThreads) work[d] = 0u;
+            __syncthreads();
+            float vmin = key_val<BF16>(prefix << pbits);
+            if (vmin != vmin) vmin = -INFINITY;
+            wide_scan<BF16>(rowp, n, h, ng, vmin, [&](int, uint32_t key) {
+                if ((key >> pbits) == prefix) atomicAdd(&work[(key >> shift) & (nb - 1)], 1u);
+            });
+            __syncthreads();
+            wide_find_digit(work, nb, static_cast<uint32_t>(Kp) - c_above, sh);
+            if (sh.dstar < 0) {
+                bad = true;
+            } else {
+                c_above += sh.dabove;
+                prefix = (prefix << width) | static_cast<uint32_t>(sh.dstar);
+                pbits = shift;
+            }
+        }
+
         int nl = 0;
         float M = -INFINITY;
         uint32_t cut = 0;
-        int m_cut = 0;
+        int cutidx = 0;
         df S = df_make(0.0f);
         if (!bad) {
+            // -------------------------------------------- 2. the kept list
             const uint32_t kstar = prefix;
-            const int dl = static_cast<int>(prefix & static_cast<uint32_t>(nb_last - 1));
-            const uint32_t t = static_cast<uint32_t>(Kp) - c_above;  // ties at key* that are kept (>= 1)
-            if (warp == 0) {
-                const uint32_t tie = lane < kWideWarps ? work[lane * nb_last + dl] : 0u;
-                uint32_t incl = tie;
-                for (int off = 1; off < 32; off <<= 1) {
-                    const uint32_t o = __shfl_up_sync(full, incl, off);
-                    if (lane >= off) incl += o;
-                }
-                const uint32_t excl = incl - tie;
-                if (lane < kWideWarps) sh.quota[lane] = t > excl ? min(tie, t - excl) : 0u;
-            }
+            const uint32_t t = static_cast<uint32_t>(Kp) - c_above;  // ties at key* kept (>= 1)
+            for (int d = tid; d < 2 * nwords; d += kWideThreads) work[d] = 0u;
             __syncthreads();
-
-            // -------------------------------------------- 2. the kept entries: bitmap, then the list
-            const int nwords = (n + 31) >> 5;
-            for (int d = tid; d < nwords; d += kWideThreads) work[d] = 0u;
-            __syncthreads();
-            const uint32_t quota = sh.quota[warp];
-            uint32_t seen = 0;  // ties at key* this warp has passed (the same in every lane)
-            wide_walk<BF16>(rowp, n, h, ng, warp, lane, badl, [&](int e0, const uint32_t* keys, uint32_t vm) {
-                uint32_t sel = 0, tm = 0;
-#pragma unroll
-                for (int q = 0; q < G; ++q)
-                    if ((vm >> q) & 1u) {
-                        if (keys[q] > kstar) sel |= 1u << q;
-                        else if (keys[q] == kstar) tm |= 1u << q;
-                    }
-                const uint32_t tc = __popc(tm);
-                if (__any_sync(full, tc != 0)) {
-                    // ranks of the ties in vocabulary order: lanes first, then a lane's entries
-                    uint32_t incl = tc;
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const uint32_t o = __shfl_up_sync(full, incl, off);
-                        if (lane >= off) incl += o;
-                    }
-                    uint32_t r = seen + incl - tc;
-                    for (uint32_t m = tm; m;) {
-                        const int q = __ffs(m) - 1;
-                        m &= m - 1;
-                        if (r < quota) sel |= 1u << q;
-                        ++r;
-                    }
-                    seen += __shfl_sync(full, incl, 31);
-                }
-                for (uint32_t m = sel; m;) {
-                    const int q = __ffs(m) - 1;
-                    m &= m - 1;
-                    const int e = e0 + q;
-                    atomicOr(&work[e >> 5], 1u << (e & 31));
-                }
+            wide_scan<BF16>(rowp, n, h, ng, key_val<BF16>(kstar), [&](int e, uint32_t key) {
+                if (key > kstar)
+                    atomicOr(&strict_bm[e >> 5], 1u << (e & 31));
+                else if (key == kstar)
+                    atomicOr(&tie_bm[e >> 5], 1u << (e & 31));
             });
             __syncthreads();
             {
                 const int wpt = (nwords + kWideThreads - 1) / kWideThreads;
                 const int w0 = min(nwords, tid * wpt), w1 = min(nwords, w0 + wpt);
-                uint32_t c = 0;
-                for (int w = w0; w < w1; ++w) c += __popc(work[w]);
+                uint32_t ct = 0;
+                for (int w = w0; w < w1; ++w) ct += __popc(tie_bm[w]);
+                uint32_t ttot;
+                uint32_t tseen = wide_excl_scan_u32(ct, sh.red_u, ttot);  // ties in lower words
+                // the ties this thread keeps: the first t of the row in vocabulary order
+                uint32_t keep[16];
+                uint32_t cs = 0;
+                for (int w = w0; w < w1; ++w) {
+                    uint32_t tm = tie_bm[w], kt = 0;
+                    while (tm && tseen < t) {
+                        const uint32_t low = tm & (0u - tm);
+                        kt |= low;
+                        tm ^= low;
+                        ++tseen;
+                    }
+                    keep[w - w0] = strict_bm[w] | kt;
+                    cs += __popc(keep[w - w0]);
+                }
                 uint32_t total;
-                uint32_t pos = wide_excl_scan_u32(c, sh.red_u, total);
+                uint32_t pos = wide_excl_scan_u32(cs, sh.red_u, total);
                 for (int w = w0; w < w1; ++w)
-                    for (uint32_t m = work[w]; m;) {
+                    for (uint32_t m = keep[w - w0]; m;) {
                         const int bit = __ffs(m) - 1;
                         m &= m - 1;
                         if (pos < static_cast<uint32_t>(kWideKMax)) lidx[pos] = w * 32 + bit;
@@ -482,8 +547,7 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
             for (int r = tid; r < nl; r += kWideThreads) lval[r] = ld_val<BF16>(rowp, lidx[r]);
             __syncthreads();
 
-            // -------------------------------------------- 3. weights, their sum, the top-p cut
-            const int r0 = tid * kWideEpt;
+            // -------------------------------------------- 3. the maximum, the weights' sum, the top-p cut
             float mx = -INFINITY;
             for (int q = 0; q < kWideEpt; ++q)
                 if (r0 + q < nl) mx = fmaxf(mx, lval[r0 + q]);
@@ -491,70 +555,141 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
             if (!(M > -INFINITY)) bad = true;
             if (!bad) {
                 rc.M = M;
-                df part = df_make(0.0f);
-                for (int q = 0; q < kWideEpt; ++q) {
-                    const int r = r0 + q;
-                    if (r < nl) {
-                        const float l = lval[r];
-                        const df e = l == -INFINITY ? df_make(0.0f) : precise_e<BF16>(l, rc, sh.exp2tab);
-                        ework[r] = e;
-                        part = df_sum(part, e);
-                    }
-                }
-                const df SK = wide_sum_df(part, sh.red_df);
-                S = SK;
                 if (top_p < 1.0f) {
-                    const df target = df_mul_f(SK, top_p);
-                    // the largest key whose entries and those above weigh at least target
-                    unsigned long long lo = 0, hi = 1ull << KB;
-                    while (hi - lo > 1) {
-                        const unsigned long long mid = (lo + hi) >> 1;
-                        df s = df_make(0.0f);
-                        for (int q = 0; q < kWideEpt; ++q) {
-                            const int r = r0 + q;
-                            if (r < nl && val_key<BF16>(lval[r]) >= mid) s = df_sum(s, ework[r]);
+                    uint32_t kmn = 0xffffffffu;
+                    for (int q = 0; q < kWideEpt; ++q)
+                        if (r0 + q < nl) kmn = min(kmn, val_key<BF16>(lval[r0 + q]));
+                    kmn = wide_min_u32(kmn, sh.red_u);
+                    const uint32_t kmx = val_key<BF16>(M);
+                    if (BF16 && kmx - kmn < static_cast<uint32_t>(kWideHistBins)) {
+                        // every entry with one key has one weight: bin b counts the
+                        // entries with key kmx - b (rank order), its mass is count * e
+                        const int R = static_cast<int>(kmx - kmn) + 1;
+                        uint32_t* cnt = work;
+                        for (int d = tid; d < R; d += kWideThreads) cnt[d] = 0u;
+                        __syncthreads();
+                        for (int q = 0; q < kWideEpt; ++q)
+                            if (r0 + q < nl) atomicAdd(&cnt[kmx - val_key<BF16>(lval[r0 + q])], 1u);
+                        __syncthreads();
+                        const int bpt = (R + kWideThreads - 1) / kWideThreads;
+                        const int b0 = min(R, tid * bpt), b1 = min(R, b0 + bpt);
+                        auto bin_e = [&](int bn) {
+                            const float l = key_val<BF16>(kmx - static_cast<uint32_t>(bn));
+                            return l == -INFINITY ? df_make(0.0f) : precise_e<BF16>(l, rc, sh.exp2tab);
+                        };
+                        df part = df_make(0.0f);
+                        for (int bn = b0; bn < b1; ++bn) {
+                            const uint32_t cn = cnt[bn];
+                            if (cn) part = df_sum(part, df_mul_f(bin_e(bn), static_cast<float>(cn)));
                         }
-                        const df tot = wide_sum_df(s, sh.red_df);
-                        if (!df_less(tot, target))
-                            lo = mid;
-                        else
-                            hi = mid;
-                    }
-                    cut = static_cast<uint32_t>(lo);
-                    df above = df_make(0.0f);
-                    uint32_t ceq = 0;
-                    for (int q = 0; q < kWideEpt; ++q) {
-                        const int r = r0 + q;
-                        if (r < nl) {
-                            const uint32_t key = val_key<BF16>(lval[r]);
-                            if (key > cut) {
-                                above = df_sum(above, ework[r]);
-                            } else if (key == cut) {
-                                ++ceq;
-                                sh.e_cut = ework[r];  // every tie has the same weight
+                        df SK;
+                        df c = wide_excl_scan_df(part, sh.red_df, SK);
+                        const df target = df_mul_f(SK, top_p);
+                        uint32_t cand = 0xffffffffu, ccount = 0;
+                        df above = df_make(0.0f), ecut = df_make(0.0f);
+                        for (int bn = b0; bn < b1; ++bn) {
+                            const uint32_t cn = cnt[bn];
+                            if (!cn) continue;
+                            const df eb = bin_e(bn);
+                            const df before = c;
+                            c = df_sum(c, df_mul_f(eb, static_cast<float>(cn)));
+                            if (cand == 0xffffffffu && !df_less(c, target)) {
+                                cand = static_cast<uint32_t>(bn);
+                                above = before;
+                                ecut = eb;
+                                ccount = cn;
                             }
                         }
-                    }
-                    const df mass_gt = wide_sum_df(above, sh.red_df);
-                    const int cnt_eq = static_cast<int>(wide_sum_u32(ceq, sh.red_u));
-                    if (tid == 0) {
-                        // the fewest ties at the cut that bring the mass to target
-                        const df ec = sh.e_cut;
-                        const df delta = df_sum(target, df_neg(mass_gt));
-                        int m = 1;
-                        if (ec.hi > 0.0f) {
-                            const float f = ceilf(df_val(delta) / df_val(ec));
-                            m = f < 1.0f ? 1 : (f > static_cast<float>(cnt_eq) ? cnt_eq : static_cast<int>(f));
+                        const uint32_t first = wide_min_u32(cand, sh.red_u);
+                        if (first != 0xffffffffu && cand == first) {
+                            // the fewest ties at this key that bring the mass to target
+                            const int ce = static_cast<int>(ccount);
+                            int m = 1;
+                            if (ecut.hi > 0.0f) {
+                                const float f = ceilf(df_val(df_sum(target, df_neg(above))) / df_val(ecut));
+                                m = f < 1.0f ? 1 : (f > static_cast<float>(ce) ? ce : static_cast<int>(f));
+                            }
+                            while (m > 1 && !df_less(df_sum(above, df_mul_f(ecut, static_cast<float>(m - 1))), target)) --m;
+                            while (m < ce && df_less(df_sum(above, df_mul_f(ecut, static_cast<float>(m))), target)) ++m;
+                            sh.mties = m;
+                            sh.S = df_sum(above, df_mul_f(ecut, static_cast<float>(m)));
                         }
-                        if (m < 1) m = 1;
-                        while (m > 1 && !df_less(df_sum(mass_gt, df_mul_f(ec, static_cast<float>(m - 1))), target)) --m;
-                        while (m < cnt_eq && df_less(df_sum(mass_gt, df_mul_f(ec, static_cast<float>(m))), target)) ++m;
-                        sh.m_cut = m;
-                        sh.S = df_sum(mass_gt, df_mul_f(ec, static_cast<float>(m)));
+                        __syncthreads();
+                        if (first == 0xffffffffu) {  // through rounding only: every entry
+                            S = SK;
+                        } else {
+                            // the cut: the m-th entry (vocabulary order) with the cut key
+                            cut = kmx - first;
+                            const uint32_t m = static_cast<uint32_t>(sh.mties);
+                            S = sh.S;
+                            uint32_t mine = 0;
+                            for (int q = 0; q < kWideEpt; ++q)
+                                if (r0 + q < nl && val_key<BF16>(lval[r0 + q]) == cut) ++mine;
+                            uint32_t tot;
+                            uint32_t seen = wide_excl_scan_u32(mine, sh.red_u, tot);
+                            if (seen < m && m <= seen + mine)
+                                for (int q = 0; q < kWideEpt; ++q)
+                                    if (r0 + q < nl && val_key<BF16>(lval[r0 + q]) == cut && ++seen == m) sh.cutidx = lidx[r0 + q];
+                            __syncthreads();
+                            cutidx = sh.cutidx;
+                        }
+                    } else {
+                        // rank order: key descending, then index ascending (one 64-bit key)
+                        int n2 = 2;
+                        while (n2 < nl) n2 <<= 1;
+                        for (int r = tid; r < n2; r += kWideThreads)
+                            skeys[r] = r < nl ? (static_cast<unsigned long long>(val_key<BF16>(lval[r])) << 32) |
+                                                    (0xffffffffu - static_cast<uint32_t>(lidx[r]))
+                                              : 0ull;
+                        __syncthreads();
+                        wide_sort_desc(skeys, n2);
+                        df ev[kWideEpt];
+                        df part = df_make(0.0f);
+#pragma unroll
+                        for (int q = 0; q < kWideEpt; ++q) {
+                            const int r = r0 + q;
+                            ev[q] = df_make(0.0f);
+                            if (r < nl) {
+                                const float l = key_val<BF16>(static_cast<uint32_t>(skeys[r] >> 32));
+                                if (l != -INFINITY) ev[q] = precise_e<BF16>(l, rc, sh.exp2tab);
+                            }
+                            part = df_sum(part, ev[q]);
+                        }
+                        df SK;
+                        df c = wide_excl_scan_df(part, sh.red_df, SK);
+                        const df target = df_mul_f(SK, top_p);
+                        // the first rank whose prefix reaches target, and the prefix there
+                        uint32_t cand = 0xffffffffu;
+                        df cS = df_make(0.0f);
+#pragma unroll
+                        for (int q = 0; q < kWideEpt; ++q) {
+                            const int r = r0 + q;
+                            c = df_sum(c, ev[q]);
+                            if (r < nl && cand == 0xffffffffu && !df_less(c, target)) {
+                                cand = static_cast<uint32_t>(r);
+                                cS = c;
+                            }
+                        }
+                        const uint32_t first = wide_min_u32(cand, sh.red_u);
+                        if (first != 0xffffffffu && cand == first) sh.S = cS;
+                        __syncthreads();
+                        if (first == 0xffffffffu) {  // through rounding only: every entry
+                            S = SK;
+                        } else {
+                            const unsigned long long ck = skeys[first];
+                            cut = static_cast<uint32_t>(ck >> 32);
+                            cutidx = static_cast<int>(0xffffffffu - static_cast<uint32_t>(ck));
+                            S = sh.S;
+                        }
+                        __syncthreads();  // the sort keys are not read again
                     }
-                    __syncthreads();
-                    m_cut = sh.m_cut;
-                    S = sh.S;
+                } else {
+                    df part = df_make(0.0f);
+                    for (int q = 0; q < kWideEpt; ++q) {
+                        const int r = r0 + q;
+                        if (r < nl && lval[r] != -INFINITY) part = df_sum(part, precise_e<BF16>(lval[r], rc, sh.exp2tab));
+                    }
+                    S = wide_sum_df(part, sh.red_df);
                 }
             }
         }
@@ -563,25 +698,19 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
         float px = 0.0f;
         if (!bad && i < k) {
             const int x = sh.xs[i];
-            if (tid == 0) sh.xr = -1;
+            if (tid == 0) sh.xpx = 0.0f;
             __syncthreads();
-            const int r0 = tid * kWideEpt;
-            for (int q = 0; q < kWideEpt; ++q)
-                if (r0 + q < nl && lidx[r0 + q] == x) sh.xr = r0 + q;
-            __syncthreads();
-            const int xr = sh.xr;
-            if (xr >= 0) {
-                const uint32_t xkey = val_key<BF16>(lval[xr]);
-                uint32_t before = 0;  // ties at the cut ahead of x in vocabulary order
-                if (cut != 0 && xkey == cut)
-                    for (int q = 0; q < kWideEpt; ++q) {
-                        const int r = r0 + q;
-                        if (r < xr && val_key<BF16>(lval[r]) == cut) ++before;
-                    }
-                const uint32_t rank = wide_sum_u32(before, sh.red_u);  // uniform branch: xkey is the same everywhere
-                const bool kept = xkey > cut || (xkey == cut && static_cast<int>(rank) < m_cut);
-                if (kept) px = df_val(ework[xr]) / df_val(S);
+            for (int q = 0; q < kWideEpt; ++q) {
+                const int r = r0 + q;
+                if (r < nl && lidx[r] == x) {
+                    const float l = lval[r];
+                    const uint32_t key = val_key<BF16>(l);
+                    if (l != -INFINITY && (key > cut || (key == cut && x <= cutidx)))
+                        sh.xpx = df_val(precise_e<BF16>(l, rc, sh.exp2tab)) / df_val(S);
+                }
             }
+            __syncthreads();
+            px = sh.xpx;
         }
         if (tid == 0) {
             sh.lpx[i] = px;
@@ -590,7 +719,7 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
             s.S = S;
             s.M = M;
             s.cut = cut;
-            s.m_cut = m_cut;
+            s.cutidx = cutidx;
             s.n = nl;
             s.bad = bad ? 1 : 0;
         }
@@ -666,20 +795,13 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
     // ---------------------------------------------------- the draw (the stop position's owner)
     const int p = j / C;
     const WideSlot sl = sh.slot[p];
-    const int* lidx = reinterpret_cast<const int*>(dyn_smem + kWideWorkBytes + p * kWideSlotBytes);
-    const float* lval = reinterpret_cast<const float*>(dyn_smem + kWideWorkBytes + p * kWideSlotBytes + kWideKMax * 4);
+    const int* lidx = reinterpret_cast<const int*>(dyn_smem + work_bytes + p * kWideSlotBytes);
+    const float* lval = reinterpret_cast<const float*>(dyn_smem + work_bytes + p * kWideSlotBytes + kWideKMax * 4);
     const int nl = sl.n;
-    const int r0 = tid * kWideEpt;
     const int mode = j < k ? (a.q ? MODE_RESIDUAL : MODE_ONEHOT) : MODE_BONUS;
     const int xj = j < k ? sh.xs[j] : -1;
     const float* qrow = a.q && j < k ? a.q + (static_cast<long long>(b) * k + j) * a.V : nullptr;
     rc.M = sl.M;
-    uint32_t tc = 0;
-    if (sl.cut != 0)
-        for (int q = 0; q < kWideEpt; ++q)
-            if (r0 + q < nl && val_key<BF16>(lval[r0 + q]) == sl.cut) ++tc;
-    uint32_t ttot;
-    uint32_t trank = wide_excl_scan_u32(tc, sh.red_u, ttot);
     df e[kWideEpt], w[kWideEpt];
     uint32_t inmask = 0;
     bool qbad = false;
@@ -692,18 +814,13 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
         if (r < nl) {
             const float l = lval[r];
             const uint32_t key = val_key<BF16>(l);
-            bool in = key > sl.cut;
-            if (sl.cut != 0 && key == sl.cut) {
-                in = static_cast<int>(trank) < sl.m_cut;
-                ++trank;
-            }
-            if (in) {
+            const int v = lidx[r];
+            if (key > sl.cut || (key == sl.cut && v <= sl.cutidx)) {
                 inmask |= 1u << q;
-                e[q] = l == -INFINITY ? df_make(0.0f) : precise_e<BF16>(l, rc, sh.exp2tab);
+                if (l != -INFINITY) e[q] = precise_e<BF16>(l, rc, sh.exp2tab);
                 if (mode == MODE_BONUS) {
                     w[q] = e[q];
                 } else {
-                    const int v = lidx[r];
                     const float qv = qrow ? __ldg(qrow + v) : (v == xj ? 1.0f : 0.0f);
                     qbad |= !(qv >= 0.0f && qv <= FLT_MAX);
                     const df rr = minus_sq(e[q], sl.S, qv);
@@ -727,7 +844,8 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
             W = wide_sum_df(local, sh.red_df);
         }
         const df target = df_mul_f(W, sh.du1);
-        df pre = wide_excl_scan_df(local, sh.red_df);
+        df tot;
+        df pre = wide_excl_scan_df(local, sh.red_df, tot);
         uint32_t cand = 0xffffffffu, lastpos = 0;  // lastpos: 1 + the last positive entry
 #pragma unroll
         for (int q = 0; q < kWideEpt; ++q) {
