@@ -915,7 +915,7 @@ def run_filtered(args, sv, dev, rank, ws, local, hbm_peak, peak_src):
                          "> 2x L2",
                    "launch": f"CUDA graph of {G} calls, two launches a call: the top-64 kernel "
                              f"({B * min(k + 1, 8)} CTAs in clusters of {min(k + 1, 8)}) and the radix-select "
-                             f"kernel ({B * min(k + 1, 16)} CTAs of 512 threads in clusters of {min(k + 1, 16)}); "
+                             f"kernel ({B * min(k + 1, 16)} CTAs of 256 threads in clusters of {min(k + 1, 16)}); "
                              f"the rows are the {'second' if wide else 'first'}'s, the other's CTAs exit at once"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak,

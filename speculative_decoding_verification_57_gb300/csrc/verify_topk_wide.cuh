@@ -10,7 +10,7 @@
 // residual max(0, p' - q) and the bonus live on P and are drawn in
 // vocabulary order.
 //
-// One thread-block cluster of C = min(k + 1, 16) CTAs of 512 threads per
+// One thread-block cluster of C = min(k + 1, 16) CTAs of 256 threads per
 // sequence; CTA c owns positions c and c + C.  A position's kept set is found
 // exactly, with no sort of the vocabulary:
 //   1. a radix select on the logits' order-preserving keys (bf16: 12 + 4
@@ -47,7 +47,7 @@
 
 namespace specv {
 
-constexpr int kWideThreads = 512;
+constexpr int kWideThreads = 256;
 constexpr int kWideWarps = kWideThreads / 32;
 constexpr int kWideEpt = kWideKMax / kWideThreads;  // kept-list entries per thread
 constexpr int kWideClusterMax = 16;                // CTAs per sequence
@@ -269,6 +269,8 @@ struct alignas(16) WideSmem {
     int dstar;
     uint32_t dabove;
     df S;
+    uint32_t hist1[16];          // bf16 fast path: the last digit of the entries in key*'s first-digit bin
+    uint32_t ncand;
     int mties;                   // ties at the top-p cut that are kept
     int cutidx;
     float xpx;
@@ -276,7 +278,7 @@ struct alignas(16) WideSmem {
     float du1;
 };
 
-// Block-wide helpers over the 512 threads; each ends with a barrier, so the
+// Block-wide helpers over the CTA's threads; each ends with a barrier, so the
 // scratch may be reused at once.
 __device__ __forceinline__ uint32_t wide_min_u32(uint32_t v, uint32_t* red) {
     v = __reduce_min_sync(0xffffffffu, v);
@@ -406,7 +408,7 @@ __device__ __forceinline__ void wide_sort_desc(unsigned long long* s, int n2) {
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const VerifyArgs a) {
+__global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const VerifyArgs a) {
     extern __shared__ __align__(128) unsigned char dyn_smem[];
     __shared__ WideSmem sh;
     constexpr int esz = BF16 ? 2 : 4;
@@ -469,7 +471,62 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
                 prefix = static_cast<uint32_t>(sh.dstar);
             }
         }
-        const int nlev = BF16 ? 1 : 2;  // digits after the first
+        // bf16 rows whose first-digit bin holds at most kWideKMax entries (the
+        // usual case): one more pass marks the entries of the higher bins in the
+        // first bitmap and lists those of the bin (index and last digit) in
+        // the second's place; key* and the kept ties then come from that list.
+        const uint32_t inbin = bad ? 0u : work[prefix];
+        __syncthreads();  // every thread has read the bin's count before the histogram is reused
+        const bool fast = BF16 && !bad && inbin <= static_cast<uint32_t>(kWideKMax);
+        uint32_t* cand = tie_bm;
+        if (fast) {
+            const uint32_t d1 = prefix;
+            for (int d = tid; d < nwords; d += kWideThreads) strict_bm[d] = 0u;
+            if (tid < 16) sh.hist1[tid] = 0u;
+            if (tid == 0) sh.ncand = 0u;
+            __syncthreads();
+            float vmin = key_val<BF16>(d1 << 4);
+            if (vmin != vmin) vmin = -INFINITY;
+            wide_scan<BF16>(rowp, n, h, ng, vmin, [&](int e, uint32_t key) {
+                const uint32_t dg = key >> 4;
+                if (dg > d1) {
+                    atomicOr(&strict_bm[e >> 5], 1u << (e & 31));
+                } else if (dg == d1) {
+                    const uint32_t slot = atomicAdd(&sh.ncand, 1u);
+                    if (slot < static_cast<uint32_t>(kWideKMax)) cand[slot] = (static_cast<uint32_t>(e) << 4) | (key & 15u);
+                    atomicAdd(&sh.hist1[key & 15u], 1u);
+                }
+            });
+            __syncthreads();
+            wide_find_digit(sh.hist1, 16, static_cast<uint32_t>(Kp) - c_above, sh);
+            if (sh.dstar < 0) {
+                bad = true;
+            } else {
+                c_above += sh.dabove;
+                prefix = (prefix << 4) | static_cast<uint32_t>(sh.dstar);
+                pbits = 0;
+                // the bin's entries above key* join the first bitmap; its ties go to
+                // the second, which replaces the list they came from
+                const uint32_t nc = min(sh.ncand, static_cast<uint32_t>(kWideKMax));
+                int tie_e[kWideEpt];
+                int nt = 0;
+                for (uint32_t r = tid; r < nc; r += kWideThreads) {
+                    const uint32_t cv = cand[r];
+                    const int e = static_cast<int>(cv >> 4);
+                    const uint32_t key = (d1 << 4) | (cv & 15u);
+                    if (key > prefix)
+                        atomicOr(&strict_bm[e >> 5], 1u << (e & 31));
+                    else if (key == prefix)
+                        tie_e[nt++] = e;
+                }
+                __syncthreads();
+                for (int d = tid; d < nwords; d += kWideThreads) tie_bm[d] = 0u;
+                __syncthreads();
+                for (int q = 0; q < nt; ++q) atomicOr(&tie_bm[tie_e[q] >> 5], 1u << (tie_e[q] & 31));
+                __syncthreads();
+            }
+        }
+        const int nlev = fast ? 0 : (BF16 ? 1 : 2);  // digits after the first, on the general path
         for (int lev = 0; lev < nlev && !bad; ++lev) {
             const int width = BF16 ? 4 : (lev == 0 ? 12 : 8);
             const int shift = pbits - width;
@@ -501,15 +558,17 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
             // -------------------------------------------- 2. the kept list
             const uint32_t kstar = prefix;
             const uint32_t t = static_cast<uint32_t>(Kp) - c_above;  // ties at key* kept (>= 1)
-            for (int d = tid; d < 2 * nwords; d += kWideThreads) work[d] = 0u;
-            __syncthreads();
-            wide_scan<BF16>(rowp, n, h, ng, key_val<BF16>(kstar), [&](int e, uint32_t key) {
-                if (key > kstar)
-                    atomicOr(&strict_bm[e >> 5], 1u << (e & 31));
-                else if (key == kstar)
-                    atomicOr(&tie_bm[e >> 5], 1u << (e & 31));
-            });
-            __syncthreads();
+            if (!fast) {
+                for (int d = tid; d < 2 * nwords; d += kWideThreads) work[d] = 0u;
+                __syncthreads();
+                wide_scan<BF16>(rowp, n, h, ng, key_val<BF16>(kstar), [&](int e, uint32_t key) {
+                    if (key > kstar)
+                        atomicOr(&strict_bm[e >> 5], 1u << (e & 31));
+                    else if (key == kstar)
+                        atomicOr(&tie_bm[e >> 5], 1u << (e & 31));
+                });
+                __syncthreads();
+            }
             {
                 const int wpt = (nwords + kWideThreads - 1) / kWideThreads;
                 const int w0 = min(nwords, tid * wpt), w1 = min(nwords, w0 + wpt);
@@ -517,8 +576,8 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
                 for (int w = w0; w < w1; ++w) ct += __popc(tie_bm[w]);
                 uint32_t ttot;
                 uint32_t tseen = wide_excl_scan_u32(ct, sh.red_u, ttot);  // ties in lower words
-                // the ties this thread keeps: the first t of the row in vocabulary order
-                uint32_t keep[16];
+                // the ties this thread keeps (the first t of the row in vocabulary
+                // order) join its words of the first bitmap, which then holds the list
                 uint32_t cs = 0;
                 for (int w = w0; w < w1; ++w) {
                     uint32_t tm = tie_bm[w], kt = 0;
@@ -528,13 +587,14 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
                         tm ^= low;
                         ++tseen;
                     }
-                    keep[w - w0] = strict_bm[w] | kt;
-                    cs += __popc(keep[w - w0]);
+                    const uint32_t kw = strict_bm[w] | kt;
+                    strict_bm[w] = kw;
+                    cs += __popc(kw);
                 }
                 uint32_t total;
                 uint32_t pos = wide_excl_scan_u32(cs, sh.red_u, total);
                 for (int w = w0; w < w1; ++w)
-                    for (uint32_t m = keep[w - w0]; m;) {
+                    for (uint32_t m = strict_bm[w]; m;) {
                         const int bit = __ffs(m) - 1;
                         m &= m - 1;
                         if (pos < static_cast<uint32_t>(kWideKMax)) lidx[pos] = w * 32 + bit;
@@ -544,7 +604,19 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
                 bad = total != static_cast<uint32_t>(Kp);  // cannot happen on a finite row
             }
             __syncthreads();
-            for (int r = tid; r < nl; r += kWideThreads) lval[r] = ld_val<BF16>(rowp, lidx[r]);
+            {
+                float lv[kWideEpt];  // the loads issued together, then stored
+#pragma unroll
+                for (int q = 0; q < kWideEpt; ++q) {
+                    const int r = tid + q * kWideThreads;
+                    lv[q] = r < nl ? ld_val<BF16>(rowp, lidx[r]) : 0.0f;
+                }
+#pragma unroll
+                for (int q = 0; q < kWideEpt; ++q) {
+                    const int r = tid + q * kWideThreads;
+                    if (r < nl) lval[r] = lv[q];
+                }
+            }
             __syncthreads();
 
             // -------------------------------------------- 3. the maximum, the weights' sum, the top-p cut
@@ -643,28 +715,22 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
                                               : 0ull;
                         __syncthreads();
                         wide_sort_desc(skeys, n2);
-                        df ev[kWideEpt];
+                        auto rank_e = [&](int r) {  // the weight at rank r (the same value on every call)
+                            if (r >= nl) return df_make(0.0f);
+                            const float l = key_val<BF16>(static_cast<uint32_t>(skeys[r] >> 32));
+                            return l == -INFINITY ? df_make(0.0f) : precise_e<BF16>(l, rc, sh.exp2tab);
+                        };
                         df part = df_make(0.0f);
-#pragma unroll
-                        for (int q = 0; q < kWideEpt; ++q) {
-                            const int r = r0 + q;
-                            ev[q] = df_make(0.0f);
-                            if (r < nl) {
-                                const float l = key_val<BF16>(static_cast<uint32_t>(skeys[r] >> 32));
-                                if (l != -INFINITY) ev[q] = precise_e<BF16>(l, rc, sh.exp2tab);
-                            }
-                            part = df_sum(part, ev[q]);
-                        }
+                        for (int q = 0; q < kWideEpt; ++q) part = df_sum(part, rank_e(r0 + q));
                         df SK;
                         df c = wide_excl_scan_df(part, sh.red_df, SK);
                         const df target = df_mul_f(SK, top_p);
                         // the first rank whose prefix reaches target, and the prefix there
                         uint32_t cand = 0xffffffffu;
                         df cS = df_make(0.0f);
-#pragma unroll
                         for (int q = 0; q < kWideEpt; ++q) {
                             const int r = r0 + q;
-                            c = df_sum(c, ev[q]);
+                            c = df_sum(c, rank_e(r));
                             if (r < nl && cand == 0xffffffffu && !df_less(c, target)) {
                                 cand = static_cast<uint32_t>(r);
                                 cS = c;
@@ -802,33 +868,44 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
     const int xj = j < k ? sh.xs[j] : -1;
     const float* qrow = a.q && j < k ? a.q + (static_cast<long long>(b) * k + j) * a.V : nullptr;
     rc.M = sl.M;
-    df e[kWideEpt], w[kWideEpt];
-    uint32_t inmask = 0;
+    // weights of the kept entries: e on P for the bonus, max(0, e - S q) on P
+    // at a rejection (e once the residual mass is zero), 0 off P; kept in
+    // the work area for the scan
+    df* wbuf = reinterpret_cast<df*>(dyn_smem);
+    float qv[kWideEpt];
+#pragma unroll
+    for (int q = 0; q < kWideEpt; ++q) {  // the draft probabilities at this thread's entries, loaded together
+        const int r = r0 + q;
+        qv[q] = 0.0f;
+        if (r < nl && mode != MODE_BONUS) {
+            const int v = lidx[r];
+            qv[q] = qrow ? __ldg(qrow + v) : (v == xj ? 1.0f : 0.0f);
+        }
+    }
     bool qbad = false;
+    uint32_t inmask = 0;
     df local = df_make(0.0f);
 #pragma unroll
     for (int q = 0; q < kWideEpt; ++q) {
         const int r = r0 + q;
-        e[q] = df_make(0.0f);
-        w[q] = df_make(0.0f);
+        df wr = df_make(0.0f);
         if (r < nl) {
             const float l = lval[r];
             const uint32_t key = val_key<BF16>(l);
-            const int v = lidx[r];
-            if (key > sl.cut || (key == sl.cut && v <= sl.cutidx)) {
+            if (key > sl.cut || (key == sl.cut && lidx[r] <= sl.cutidx)) {
                 inmask |= 1u << q;
-                if (l != -INFINITY) e[q] = precise_e<BF16>(l, rc, sh.exp2tab);
+                const df e = l == -INFINITY ? df_make(0.0f) : precise_e<BF16>(l, rc, sh.exp2tab);
                 if (mode == MODE_BONUS) {
-                    w[q] = e[q];
+                    wr = e;
                 } else {
-                    const float qv = qrow ? __ldg(qrow + v) : (v == xj ? 1.0f : 0.0f);
-                    qbad |= !(qv >= 0.0f && qv <= FLT_MAX);
-                    const df rr = minus_sq(e[q], sl.S, qv);
-                    w[q] = rr.hi + rr.lo > 0.0f ? rr : df_make(0.0f);
+                    qbad |= !(qv[q] >= 0.0f && qv[q] <= FLT_MAX);
+                    const df rr = minus_sq(e, sl.S, qv[q]);
+                    wr = rr.hi + rr.lo > 0.0f ? rr : df_make(0.0f);
                 }
-                local = df_sum(local, w[q]);
             }
+            wbuf[r] = wr;
         }
+        local = df_sum(local, wr);
     }
     if (__syncthreads_or(qbad ? 1 : 0)) st |= ST_QBAD;
     if (!(st & ST_ERRMASK)) {
@@ -836,10 +913,14 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
         if (mode != MODE_BONUS && !(W.hi + W.lo > 0.0f)) {  // zero residual mass: draw from p'
             st |= ST_ZERO_RESIDUAL;
             local = df_make(0.0f);
-#pragma unroll
             for (int q = 0; q < kWideEpt; ++q) {
-                w[q] = ((inmask >> q) & 1u) ? e[q] : df_make(0.0f);
-                local = df_sum(local, w[q]);
+                const int r = r0 + q;
+                if (r < nl) {
+                    const float l = lval[r];
+                    const df wr = ((inmask >> q) & 1u) && l != -INFINITY ? precise_e<BF16>(l, rc, sh.exp2tab) : df_make(0.0f);
+                    wbuf[r] = wr;
+                    local = df_sum(local, wr);
+                }
             }
             W = wide_sum_df(local, sh.red_df);
         }
@@ -847,12 +928,12 @@ __global__ void __launch_bounds__(kWideThreads, 2) verify_topk_wide_kernel(const
         df tot;
         df pre = wide_excl_scan_df(local, sh.red_df, tot);
         uint32_t cand = 0xffffffffu, lastpos = 0;  // lastpos: 1 + the last positive entry
-#pragma unroll
         for (int q = 0; q < kWideEpt; ++q) {
             const int r = r0 + q;
             if (r < nl) {
-                pre = df_sum(pre, w[q]);
-                if (w[q].hi + w[q].lo > 0.0f) {
+                const df wr = wbuf[r];
+                pre = df_sum(pre, wr);
+                if (wr.hi + wr.lo > 0.0f) {
                     lastpos = static_cast<uint32_t>(r + 1);
                     if (cand == 0xffffffffu && df_less(target, pre)) cand = static_cast<uint32_t>(r);
                 }
