@@ -269,8 +269,7 @@ struct alignas(16) WideSmem {
     int dstar;
     uint32_t dabove;
     df S;
-    uint32_t hist1[16];          // bf16 fast path: the last digit of the entries in key*'s first-digit bin
-    uint32_t ncand;
+    uint32_t hist1[16];          // bf16 rows: the last digit of the entries in key*'s first-digit bin
     int mties;                   // ties at the top-p cut that are kept
     int cutidx;
     float xpx;
@@ -471,19 +470,18 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                 prefix = static_cast<uint32_t>(sh.dstar);
             }
         }
-        // bf16 rows whose first-digit bin holds at most kWideKMax entries (the
-        // usual case): one more pass marks the entries of the higher bins in the
-        // first bitmap and lists those of the bin (index and last digit) in
-        // the second's place; key* and the kept ties then come from that list.
-        const uint32_t inbin = bad ? 0u : work[prefix];
-        __syncthreads();  // every thread has read the bin's count before the histogram is reused
-        const bool fast = BF16 && !bad && inbin <= static_cast<uint32_t>(kWideKMax);
-        uint32_t* cand = tie_bm;
+        // bf16 rows: one more pass marks the entries of the higher first-digit
+        // bins in the first bitmap and those of key*'s bin in the second, and
+        // counts the bin's last digits, which give key*; the bin's entries are
+        // then sorted into the two bitmaps by their logits, read again (a few
+        // thousand at most on ordinary rows).  No store in the pass waits for
+        // a reply.
+        const bool fast = BF16 && !bad;
         if (fast) {
             const uint32_t d1 = prefix;
-            for (int d = tid; d < nwords; d += kWideThreads) strict_bm[d] = 0u;
+            __syncthreads();  // the histogram is read no more
+            for (int d = tid; d < 2 * nwords; d += kWideThreads) work[d] = 0u;
             if (tid < 16) sh.hist1[tid] = 0u;
-            if (tid == 0) sh.ncand = 0u;
             __syncthreads();
             float vmin = key_val<BF16>(d1 << 4);
             if (vmin != vmin) vmin = -INFINITY;
@@ -492,8 +490,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                 if (dg > d1) {
                     atomicOr(&strict_bm[e >> 5], 1u << (e & 31));
                 } else if (dg == d1) {
-                    const uint32_t slot = atomicAdd(&sh.ncand, 1u);
-                    if (slot < static_cast<uint32_t>(kWideKMax)) cand[slot] = (static_cast<uint32_t>(e) << 4) | (key & 15u);
+                    atomicOr(&tie_bm[e >> 5], 1u << (e & 31));
                     atomicAdd(&sh.hist1[key & 15u], 1u);
                 }
             });
@@ -505,24 +502,36 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                 c_above += sh.dabove;
                 prefix = (prefix << 4) | static_cast<uint32_t>(sh.dstar);
                 pbits = 0;
-                // the bin's entries above key* join the first bitmap; its ties go to
-                // the second, which replaces the list they came from
-                const uint32_t nc = min(sh.ncand, static_cast<uint32_t>(kWideKMax));
-                int tie_e[kWideEpt];
-                int nt = 0;
-                for (uint32_t r = tid; r < nc; r += kWideThreads) {
-                    const uint32_t cv = cand[r];
-                    const int e = static_cast<int>(cv >> 4);
-                    const uint32_t key = (d1 << 4) | (cv & 15u);
-                    if (key > prefix)
-                        atomicOr(&strict_bm[e >> 5], 1u << (e & 31));
-                    else if (key == prefix)
-                        tie_e[nt++] = e;
-                }
-                __syncthreads();
-                for (int d = tid; d < nwords; d += kWideThreads) tie_bm[d] = 0u;
-                __syncthreads();
-                for (int q = 0; q < nt; ++q) atomicOr(&tie_bm[tie_e[q] >> 5], 1u << (tie_e[q] & 31));
+                // this thread's words: the bin's entries above key* move to the
+                // first bitmap, those below leave the second (ties stay)
+                const int wpt = (nwords + kWideThreads - 1) / kWideThreads;
+                const int w0 = min(nwords, tid * wpt), w1 = min(nwords, w0 + wpt);
+                constexpr int kBatch = 16;
+                int eb[kBatch];
+                int nbat = 0;
+                auto classify = [&]() {
+                    float vb[kBatch];
+#pragma unroll
+                    for (int q = 0; q < kBatch; ++q) vb[q] = q < nbat ? ld_val<BF16>(rowp, eb[q]) : 0.0f;
+#pragma unroll
+                    for (int q = 0; q < kBatch; ++q)
+                        if (q < nbat) {
+                            const uint32_t key = val_key<BF16>(vb[q]);
+                            const int e = eb[q];
+                            const uint32_t bit = 1u << (e & 31);
+                            if (key > prefix) strict_bm[e >> 5] |= bit;
+                            if (key != prefix) tie_bm[e >> 5] &= ~bit;
+                        }
+                    nbat = 0;
+                };
+                for (int w = w0; w < w1; ++w)
+                    for (uint32_t m = tie_bm[w]; m;) {
+                        const int bit = __ffs(m) - 1;
+                        m &= m - 1;
+                        eb[nbat++] = w * 32 + bit;
+                        if (nbat == kBatch) classify();
+                    }
+                classify();
                 __syncthreads();
             }
         }
