@@ -159,6 +159,7 @@ KERNEL_SOURCES = {
     "verify_cluster_kernel_onehot_B64_k5_V128256_bf16": _CLUSTER_SOURCES,
     "verify_cluster_kernel_tree_B64_M16_V128256_bf16": _CLUSTER_SOURCES,
     "verify_topk_kernel_B64_k5_V128256_bf16": ["verify_topk.cuh"] + _CLUSTER_SOURCES,
+    "verify_topk_wide_kernel_B64_k5_V128256_bf16_K4096": ["verify_topk_wide.cuh", "verify_topk.cuh"] + _CLUSTER_SOURCES,
     "rollback_kernel_B4096_k8": ["rollback.cuh", "specv.cu"],
 }
 
