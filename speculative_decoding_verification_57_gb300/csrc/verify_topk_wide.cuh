@@ -246,6 +246,63 @@ __device__ __forceinline__ void wide_scan(const unsigned char* rowp, int n, int 
     }
 }
 
+// The second pass of bf16 rows: every entry whose first digit is above d1
+// is marked in A, every entry of bin d1 in B, and the bin's last digits are
+// counted.  One packed compare a word finds a group's entries at or above
+// the bin (a few percent of the row); the warp then runs the marking as many
+// times as its busiest lane has such entries, instead of issuing a
+// predicated step for every entry.
+__device__ __forceinline__ void wide_pass2_bf16(const unsigned char* rowp, int n, int h, int ng, uint32_t d1, float vmin,
+                                                uint32_t* A, uint32_t* Bm, uint32_t* hist1) {
+    const int tid = threadIdx.x;
+    const unsigned full = 0xffffffffu;
+    auto mark = [&](int e, uint32_t key) {
+        const uint32_t dg = key >> 4;
+        if (dg > d1) {
+            atomicOr(&A[e >> 5], 1u << (e & 31));
+        } else if (dg == d1) {
+            atomicOr(&Bm[e >> 5], 1u << (e & 31));
+            atomicAdd(&hist1[key & 15u], 1u);
+        }
+    };
+    const unsigned short* row16 = reinterpret_cast<const unsigned short*>(rowp);
+    if (tid < h) mark(tid, key16(__ldg(row16 + tid)));
+    const int t0 = h + ng * 8;
+    if (tid < n - t0) mark(t0 + tid, key16(__ldg(row16 + t0 + tid)));
+    const __nv_bfloat162 vmin2 = __float2bfloat162_rn(vmin);  // exact: a bf16 value or -inf
+    for (int base = 0; base < ng; base += 4 * kWideThreads) {
+        uint4 w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int g = base + u * kWideThreads + tid;
+            w[u] = g < ng ? __ldg(reinterpret_cast<const uint4*>(rowp + (static_cast<long long>(h) + static_cast<long long>(g) * 8) * 2))
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int g = base + u * kWideThreads + tid;
+            uint32_t rel = 0;  // bit q: entry q of the group is at or above vmin
+            if (g < ng) {
+                const uint32_t m0 = __hge2_mask(as_bf2(w[u].x), vmin2), m1 = __hge2_mask(as_bf2(w[u].y), vmin2);
+                const uint32_t m2 = __hge2_mask(as_bf2(w[u].z), vmin2), m3 = __hge2_mask(as_bf2(w[u].w), vmin2);
+                rel = (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) | ((m2 & 1u) << 4) |
+                      ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
+            }
+            const int rounds = __reduce_max_sync(full, static_cast<unsigned>(__popc(rel)));
+            const int e0 = h + g * 8;
+            for (int it = 0; it < rounds; ++it) {
+                if (rel) {
+                    const int q = __ffs(rel) - 1;
+                    rel &= rel - 1;
+                    const int wi = q >> 1;  // (selects, not an indexed array: no local memory)
+                    const uint32_t wd = wi < 2 ? (wi == 0 ? w[u].x : w[u].y) : (wi == 2 ? w[u].z : w[u].w);
+                    mark(e0 + q, key16((q & 1) ? (wd >> 16) : (wd & 0xffffu)));
+                }
+            }
+        }
+    }
+}
+
 struct WideSlot {
     df S;             // mass of the kept set P, in e-units
     float M;          // the row maximum
@@ -485,15 +542,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
             __syncthreads();
             float vmin = key_val<BF16>(d1 << 4);
             if (vmin != vmin) vmin = -INFINITY;
-            wide_scan<BF16>(rowp, n, h, ng, vmin, [&](int e, uint32_t key) {
-                const uint32_t dg = key >> 4;
-                if (dg > d1) {
-                    atomicOr(&strict_bm[e >> 5], 1u << (e & 31));
-                } else if (dg == d1) {
-                    atomicOr(&tie_bm[e >> 5], 1u << (e & 31));
-                    atomicAdd(&sh.hist1[key & 15u], 1u);
-                }
-            });
+            wide_pass2_bf16(rowp, n, h, ng, d1, vmin, strict_bm, tie_bm, sh.hist1);
             __syncthreads();
             wide_find_digit(sh.hist1, 16, static_cast<uint32_t>(Kp) - c_above, sh);
             if (sh.dstar < 0) {
