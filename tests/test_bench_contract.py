@@ -107,3 +107,32 @@ def test_clock_sampler_keeps_the_timed_window_and_reasons(monkeypatch):
     assert d["in_window"] and d["samples"] == 3
     assert d["sm_mhz"] == 2070.0 and d["sm_max_mhz"] == 2070.0
     assert d["reasons"] == ["sw_power_cap"]  # the hw_slowdown row lies outside the window
+
+
+def test_filter_flags_and_profile_keys(monkeypatch):
+    """--top-k / --top-p reach the filtered variant (defaults 40 / 0.95);
+    the small-vocabulary kernel named in a profile key is the one the
+    library picks for the batch (one CTA per row up to twice the SM count,
+    SPECV_SMALLV forcing either), and every profile key has its sources."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from speculative_decoding_verification_57_gb300 import workloads as W
+
+    a = bench.parse_args(["--variant", "filtered", "--top-k", "4096", "--top-p", "0.9"])
+    assert (a.variant, a.top_k, a.top_p) == ("filtered", 4096, 0.9)
+    b = bench.parse_args(["--variant", "filtered"])
+    assert b.top_k is None and b.top_p is None and (bench.FILTER_TOP_K, bench.FILTER_TOP_P) == (40, 0.95)
+    monkeypatch.delenv("SPECV_SMALLV", raising=False)
+    assert bench.small_v_kernel(1, 152) == "verify_row_kernel"
+    assert bench.small_v_kernel(304, 152) == "verify_row_kernel"
+    assert bench.small_v_kernel(305, 152) == "verify_warp_kernel"
+    monkeypatch.setenv("SPECV_SMALLV", "warp")
+    assert bench.small_v_kernel(1, 152) == "verify_warp_kernel"
+    monkeypatch.delenv("SPECV_SMALLV")
+    toy = W.make_workload("toy")
+    assert bench.profile_name("toy", toy) in bench.KERNEL_SOURCES
+    assert bench.measured_traffic("no_such_profile") is None
+    for name, files in bench.KERNEL_SOURCES.items():
+        assert os.path.exists(os.path.join(ROOT, "profiles", name + ".md")), name
+        for f in files:
+            assert os.path.exists(os.path.join(ROOT, "speculative_decoding_verification_57_gb300", "csrc", f)), f
