@@ -96,3 +96,44 @@ def test_filter_errors():
     r = oracle.verify_warped(w.logits, w.q, w.x, w.u, w.T, [0, 3, 3, 3], np.array([1, 0, 1.5, 0.5], np.float32))
     assert r["row_status"].tolist()[:3] == [1024, 1024, 1024]
     assert r["row_status"][3] in (0, 16)
+
+
+def _inverse_cdf(w, uu):
+    """The smallest index whose prefix of w exceeds uu * sum(w) (vocabulary
+    order); the last positive entry if rounding leaves none."""
+    c = np.cumsum(w)
+    i = int(np.searchsorted(c, uu * c[-1], side="right"))
+    return i if i < len(w) else int(np.nonzero(w > 0)[0][-1])
+
+
+def test_large_top_k_and_ties_match_the_definition():
+    """top_k up to 4096 on rows with many equal logits (the K-th value tied
+    across the cut): one-draft rows verified by a numpy restatement of the
+    warped rule (lexsort ranks, p' on the kept prefix, accept test, residual
+    or bonus by inverse CDF) give the oracle's outputs on every row the
+    oracle does not flag as within 1e-6 of a decision edge."""
+    rng = np.random.default_rng(31)
+    B, V = 240, 5000
+    w = W.make_random(name="bigk", B=B, k=1, V=V, dtype="f32", seed=32, logit_sigma=2.0, draft_sigma=0.3,
+                      temperature=1.0)
+    L = (np.round(w.logits * 4.0) / 4.0).astype(np.float32)  # values on a 0.25 grid: ties everywhere
+    K = rng.choice([65, 100, 1000, 4096], size=B).astype(np.int32)
+    P = rng.choice([1.0, 0.9, 0.5], size=B).astype(np.float32)
+    r = oracle.verify_warped(L, w.q, w.x, w.u, w.T, K, P)
+    checked = 0
+    for b in range(B):
+        if r["boundary"][b] or r["row_status"][b] & ~16:
+            continue
+        T = float(w.T[b])
+        p0 = warped_p(L[b, 0], T, int(K[b]), float(P[b]))
+        x0 = int(w.x[b, 0])
+        rho = min(1.0, p0[x0] / max(float(w.q[b, 0, x0]), 1e-12))
+        if float(w.u[b, 0, 0]) < rho:
+            n_acc, tok = 1, _inverse_cdf(warped_p(L[b, 1], T, int(K[b]), float(P[b])), float(w.u[b, 1, 1]))
+        else:
+            res = np.where(p0 > 0, np.maximum(p0 - w.q[b, 0].astype(np.float64), 0.0), 0.0)
+            n_acc, tok = 0, _inverse_cdf(res if res.sum() > 0 else p0, float(w.u[b, 0, 1]))
+        assert r["num_accepted"][b] == n_acc, b
+        assert r["out_tokens"][b, n_acc] == tok, (b, K[b], P[b])
+        checked += 1
+    assert checked >= B * 0.9
