@@ -51,17 +51,22 @@ constexpr int kWideThreads = 256;
 constexpr int kWideWarps = kWideThreads / 32;
 constexpr int kWideEpt = kWideKMax / kWideThreads;  // kept-list entries per thread
 constexpr int kWideClusterMax = 16;                // CTAs per sequence
-constexpr int kWideSlotBytes = kWideKMax * 8;      // one position's kept list: index and logit
+constexpr int kWideListPad = kWideKMax + kWideKMax / 16;  // a kept list with a pad word after every 16 entries
+constexpr int kWideSlotBytes = kWideListPad * 8;   // one position's kept list: index and logit
 constexpr int kWideSlots = (kMaxK + kWideClusterMax) / kWideClusterMax;  // positions a CTA owns at most
 constexpr int kWideHistBins = 4096;                // 12-bit digits
 static_assert(kWideEpt * kWideThreads == kWideKMax, "the kept list is split evenly over the threads");
+
+// Place of kept-list entry r: one pad word after every 16 entries, so that
+// threads walking 16 consecutive entries each touch 32 different banks.
+__device__ __forceinline__ int lp(int r) { return r + (r >> 4); }
 
 inline int wide_cluster(int k) { return k + 1 < kWideClusterMax ? k + 1 : kWideClusterMax; }
 
 // Work area: the histogram, then the two bitmaps, then the sort keys.
 __host__ __device__ inline int wide_work_bytes(long long V) {
     const long long bitmaps = 2 * ((V + 31) / 32) * 4;
-    const long long least = kWideKMax * 8;  // the sort keys (and 4096 bins of 4 bytes)
+    const long long least = kWideListPad * 8;  // the draw's weights (and the sort keys, and 4096 bins)
     return static_cast<int>(bitmaps > least ? bitmaps : least);
 }
 
@@ -506,7 +511,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
     for (int p = 0; p < P; ++p) {
         const int i = crank + C * p;
         int* lidx = reinterpret_cast<int*>(dyn_smem + work_bytes + p * kWideSlotBytes);
-        float* lval = reinterpret_cast<float*>(dyn_smem + work_bytes + p * kWideSlotBytes + kWideKMax * 4);
+        float* lval = reinterpret_cast<float*>(dyn_smem + work_bytes + p * kWideSlotBytes + kWideListPad * 4);
         const unsigned char* rowp = reinterpret_cast<const unsigned char*>(a.logits) +
                                     (static_cast<long long>(b) * (k + 1) + i) * static_cast<long long>(n) * esz;
         int h = static_cast<int>(((16 - (reinterpret_cast<uintptr_t>(rowp) & 15)) & 15) / esz);
@@ -655,7 +660,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                     for (uint32_t m = strict_bm[w]; m;) {
                         const int bit = __ffs(m) - 1;
                         m &= m - 1;
-                        if (pos < static_cast<uint32_t>(kWideKMax)) lidx[pos] = w * 32 + bit;
+                        if (pos < static_cast<uint32_t>(kWideKMax)) lidx[lp(pos)] = w * 32 + bit;
                         ++pos;
                     }
                 nl = static_cast<int>(min(total, static_cast<uint32_t>(kWideKMax)));
@@ -667,12 +672,12 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
 #pragma unroll
                 for (int q = 0; q < kWideEpt; ++q) {
                     const int r = tid + q * kWideThreads;
-                    lv[q] = r < nl ? ld_val<BF16>(rowp, lidx[r]) : 0.0f;
+                    lv[q] = r < nl ? ld_val<BF16>(rowp, lidx[lp(r)]) : 0.0f;
                 }
 #pragma unroll
                 for (int q = 0; q < kWideEpt; ++q) {
                     const int r = tid + q * kWideThreads;
-                    if (r < nl) lval[r] = lv[q];
+                    if (r < nl) lval[lp(r)] = lv[q];
                 }
             }
             __syncthreads();
@@ -680,7 +685,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
             // -------------------------------------------- 3. the maximum, the weights' sum, the top-p cut
             float mx = -INFINITY;
             for (int q = 0; q < kWideEpt; ++q)
-                if (r0 + q < nl) mx = fmaxf(mx, lval[r0 + q]);
+                if (r0 + q < nl) mx = fmaxf(mx, lval[lp(r0 + q)]);
             M = wide_max_f(mx, sh.red_f);
             if (!(M > -INFINITY)) bad = true;
             if (!bad) {
@@ -688,7 +693,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                 if (top_p < 1.0f) {
                     uint32_t kmn = 0xffffffffu;
                     for (int q = 0; q < kWideEpt; ++q)
-                        if (r0 + q < nl) kmn = min(kmn, val_key<BF16>(lval[r0 + q]));
+                        if (r0 + q < nl) kmn = min(kmn, val_key<BF16>(lval[lp(r0 + q)]));
                     kmn = wide_min_u32(kmn, sh.red_u);
                     const uint32_t kmx = val_key<BF16>(M);
                     if (BF16 && kmx - kmn < static_cast<uint32_t>(kWideHistBins)) {
@@ -699,7 +704,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                         for (int d = tid; d < R; d += kWideThreads) cnt[d] = 0u;
                         __syncthreads();
                         for (int q = 0; q < kWideEpt; ++q)
-                            if (r0 + q < nl) atomicAdd(&cnt[kmx - val_key<BF16>(lval[r0 + q])], 1u);
+                            if (r0 + q < nl) atomicAdd(&cnt[kmx - val_key<BF16>(lval[lp(r0 + q)])], 1u);
                         __syncthreads();
                         const int bpt = (R + kWideThreads - 1) / kWideThreads;
                         const int b0 = min(R, tid * bpt), b1 = min(R, b0 + bpt);
@@ -754,12 +759,12 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                             S = sh.S;
                             uint32_t mine = 0;
                             for (int q = 0; q < kWideEpt; ++q)
-                                if (r0 + q < nl && val_key<BF16>(lval[r0 + q]) == cut) ++mine;
+                                if (r0 + q < nl && val_key<BF16>(lval[lp(r0 + q)]) == cut) ++mine;
                             uint32_t tot;
                             uint32_t seen = wide_excl_scan_u32(mine, sh.red_u, tot);
                             if (seen < m && m <= seen + mine)
                                 for (int q = 0; q < kWideEpt; ++q)
-                                    if (r0 + q < nl && val_key<BF16>(lval[r0 + q]) == cut && ++seen == m) sh.cutidx = lidx[r0 + q];
+                                    if (r0 + q < nl && val_key<BF16>(lval[lp(r0 + q)]) == cut && ++seen == m) sh.cutidx = lidx[lp(r0 + q)];
                             __syncthreads();
                             cutidx = sh.cutidx;
                         }
@@ -768,8 +773,8 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                         int n2 = 2;
                         while (n2 < nl) n2 <<= 1;
                         for (int r = tid; r < n2; r += kWideThreads)
-                            skeys[r] = r < nl ? (static_cast<unsigned long long>(val_key<BF16>(lval[r])) << 32) |
-                                                    (0xffffffffu - static_cast<uint32_t>(lidx[r]))
+                            skeys[r] = r < nl ? (static_cast<unsigned long long>(val_key<BF16>(lval[lp(r)])) << 32) |
+                                                    (0xffffffffu - static_cast<uint32_t>(lidx[lp(r)]))
                                               : 0ull;
                         __syncthreads();
                         wide_sort_desc(skeys, n2);
@@ -811,7 +816,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                     df part = df_make(0.0f);
                     for (int q = 0; q < kWideEpt; ++q) {
                         const int r = r0 + q;
-                        if (r < nl && lval[r] != -INFINITY) part = df_sum(part, precise_e<BF16>(lval[r], rc, sh.exp2tab));
+                        if (r < nl && lval[lp(r)] != -INFINITY) part = df_sum(part, precise_e<BF16>(lval[lp(r)], rc, sh.exp2tab));
                     }
                     S = wide_sum_df(part, sh.red_df);
                 }
@@ -826,8 +831,8 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
             __syncthreads();
             for (int q = 0; q < kWideEpt; ++q) {
                 const int r = r0 + q;
-                if (r < nl && lidx[r] == x) {
-                    const float l = lval[r];
+                if (r < nl && lidx[lp(r)] == x) {
+                    const float l = lval[lp(r)];
                     const uint32_t key = val_key<BF16>(l);
                     if (l != -INFINITY && (key > cut || (key == cut && x <= cutidx)))
                         sh.xpx = df_val(precise_e<BF16>(l, rc, sh.exp2tab)) / df_val(S);
@@ -920,7 +925,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
     const int p = j / C;
     const WideSlot sl = sh.slot[p];
     const int* lidx = reinterpret_cast<const int*>(dyn_smem + work_bytes + p * kWideSlotBytes);
-    const float* lval = reinterpret_cast<const float*>(dyn_smem + work_bytes + p * kWideSlotBytes + kWideKMax * 4);
+    const float* lval = reinterpret_cast<const float*>(dyn_smem + work_bytes + p * kWideSlotBytes + kWideListPad * 4);
     const int nl = sl.n;
     const int mode = j < k ? (a.q ? MODE_RESIDUAL : MODE_ONEHOT) : MODE_BONUS;
     const int xj = j < k ? sh.xs[j] : -1;
@@ -936,7 +941,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
         const int r = r0 + q;
         qv[q] = 0.0f;
         if (r < nl && mode != MODE_BONUS) {
-            const int v = lidx[r];
+            const int v = lidx[lp(r)];
             qv[q] = qrow ? __ldg(qrow + v) : (v == xj ? 1.0f : 0.0f);
         }
     }
@@ -948,9 +953,9 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
         const int r = r0 + q;
         df wr = df_make(0.0f);
         if (r < nl) {
-            const float l = lval[r];
+            const float l = lval[lp(r)];
             const uint32_t key = val_key<BF16>(l);
-            if (key > sl.cut || (key == sl.cut && lidx[r] <= sl.cutidx)) {
+            if (key > sl.cut || (key == sl.cut && lidx[lp(r)] <= sl.cutidx)) {
                 inmask |= 1u << q;
                 const df e = l == -INFINITY ? df_make(0.0f) : precise_e<BF16>(l, rc, sh.exp2tab);
                 if (mode == MODE_BONUS) {
@@ -961,7 +966,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
                     wr = rr.hi + rr.lo > 0.0f ? rr : df_make(0.0f);
                 }
             }
-            wbuf[r] = wr;
+            wbuf[lp(r)] = wr;
         }
         local = df_sum(local, wr);
     }
@@ -974,9 +979,9 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
             for (int q = 0; q < kWideEpt; ++q) {
                 const int r = r0 + q;
                 if (r < nl) {
-                    const float l = lval[r];
+                    const float l = lval[lp(r)];
                     const df wr = ((inmask >> q) & 1u) && l != -INFINITY ? precise_e<BF16>(l, rc, sh.exp2tab) : df_make(0.0f);
-                    wbuf[r] = wr;
+                    wbuf[lp(r)] = wr;
                     local = df_sum(local, wr);
                 }
             }
@@ -989,7 +994,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
         for (int q = 0; q < kWideEpt; ++q) {
             const int r = r0 + q;
             if (r < nl) {
-                const df wr = wbuf[r];
+                const df wr = wbuf[lp(r)];
                 pre = df_sum(pre, wr);
                 if (wr.hi + wr.lo > 0.0f) {
                     lastpos = static_cast<uint32_t>(r + 1);
@@ -1001,7 +1006,7 @@ __global__ void __launch_bounds__(kWideThreads, 3) verify_topk_wide_kernel(const
         lastpos = wide_max_u32(lastpos, sh.red_u);
         // only through rounding at the top edge: the last entry with positive weight
         const int rs = cand != 0xffffffffu ? static_cast<int>(cand) : static_cast<int>(lastpos) - 1;
-        const int token = rs >= 0 ? lidx[rs] : -1;
+        const int token = rs >= 0 ? lidx[lp(rs)] : -1;
         if (tid <= k) a.out_tokens[static_cast<long long>(b) * (k + 1) + tid] = tid < j ? sh.xs[tid] : (tid == j ? token : -1);
         if (tid == 0) {
             a.num_accepted[b] = j;
