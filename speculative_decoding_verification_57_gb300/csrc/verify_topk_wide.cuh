@@ -13,26 +13,33 @@
 // One thread-block cluster of C = min(k + 1, 16) CTAs of 256 threads per
 // sequence; CTA c owns positions c and c + C.  A position's kept set is found
 // exactly, with no sort of the vocabulary:
-//   1. a radix select on the logits' order-preserving keys (bf16: 12 + 4
-//      bits, fp32: 12 + 12 + 8 bits), one pass over the row a digit, finds
-//      the key of the K-th largest entry, key*, and how many entries lie
-//      above it.  The first pass counts every entry (two keys a 32-bit word
-//      for bf16); the later ones skip, with one packed maximum a 16-byte
-//      group, the groups whose entries all lie below the digit's range;
-//   2. one more pass marks the entries above key* and those equal to it in
-//      two bitmaps of the vocabulary; a block scan in vocabulary order turns
-//      them into the kept list (the ties up to the count that fits, the
-//      lowest indices first): index and logit, at most 4096 entries, in
-//      shared memory;
-//   3. on the list: the maximum M and, for top_p < 1, a bitonic sort of the
-//      list into rank order, a prefix sum of the weights e = exp((l - M) / T)
-//      (double-float exponential and sums) and the first rank where it
-//      reaches top_p of the total: that entry's (key, index) is the cut;
+//   1. a radix select on the logits' order-preserving keys finds key*, the key
+//      of the K-th largest entry, and how many entries lie above it.  The
+//      first pass counts every entry by its key's top 12 bits (two keys a
+//      32-bit word for bf16).  bf16 rows then take one more pass that marks
+//      the entries of the higher bins in one bitmap of the vocabulary and
+//      those of key*'s bin in a second, and counts that bin's last 4 bits
+//      (key*); the bin's entries are read again and sorted into the two
+//      bitmaps (above key*, equal to it).  fp32 rows take two more digit
+//      passes (12 and 8 bits) and a marking pass.  The later passes skip, by
+//      packed compares, the entries below the range that matters;
+//   2. a block scan over the two bitmaps in vocabulary order keeps the ties
+//      that fit (the lowest indices first) and writes the kept list, index
+//      and logit, at most 4096 entries, into shared memory;
+//   3. on the list: the maximum M and, for top_p < 1, the first rank (key
+//      descending, index ascending) where the prefix of the weights
+//      e = exp((l - M) / T) (double-float exponential and sums) reaches top_p
+//      of the total: that entry's (key, index) is the cut.  The prefix comes
+//      per key from a count histogram of the list when its keys span at most
+//      4096 values (bf16: a key's entries share one weight), else from a
+//      bitonic sort of the list;
 //   4. p'(x_i) goes to the leader CTA over distributed shared memory.
 // After a cluster barrier the leader's warp 0 walks the positions, and the
 // CTA that owns the stop position draws from its kept list: weights in
 // double-float, a block scan in vocabulary order, the first entry whose
-// prefix exceeds u * W.
+// prefix exceeds u * W.  Threads walk 16 consecutive list entries; the lists
+// hold a pad word after every 16 so that a warp's accesses spread over the
+// banks.
 #pragma once
 #include <cfloat>
 #include <climits>
@@ -63,7 +70,8 @@ __device__ __forceinline__ int lp(int r) { return r + (r >> 4); }
 
 inline int wide_cluster(int k) { return k + 1 < kWideClusterMax ? k + 1 : kWideClusterMax; }
 
-// Work area: the histogram, then the two bitmaps, then the sort keys.
+// Work area: the digit histogram, then the two bitmaps, then the top-p cut's
+// histogram or sort keys, then the draw's weights.
 __host__ __device__ inline int wide_work_bytes(long long V) {
     const long long bitmaps = 2 * ((V + 31) / 32) * 4;
     const long long least = kWideListPad * 8;  // the draw's weights (and the sort keys, and 4096 bins)
