@@ -120,7 +120,13 @@ typedef struct {
  * vocabularies up to `vocab` entries (1 <= vocab <= 262144: at most 16 CTAs
  * of 16384 entries a position).  Other values: SPECV_ERR_INVALID_ARGUMENT.
  * Queries the device; allocates no device memory.  Returns
- * SPECV_ERR_UNSUPPORTED if the device is not compute capability 10.3. */
+ * SPECV_ERR_UNSUPPORTED if the device is not compute capability 10.3.
+ * Two environment variables, read at every call, override the launch plan
+ * (for tests and tuning; the results do not depend on them):
+ * SPECV_CLUSTER=C (V > 2048: C CTAs per row, from the fewest the slice limit
+ * allows up to 16) and SPECV_SMALLV=row|warp (V <= 2048: one CTA of eight
+ * warps per row, or one warp per row; by default the first while the batch
+ * is at most twice the SM count). */
 specv_status specv_create(specv_handle *out, int device, int max_batch, int max_k, int64_t vocab);
 
 /* Sampled verification (rows with temperature 0 take the greedy rule).
